@@ -1,0 +1,240 @@
+/*
+ * mxfp8.h - C ABI of the GB300 (sm_103a) MXFP8 / per-tensor FP8 library.
+ *
+ * The library turns BF16 operands into FP8 payloads plus scales and runs the
+ * scaled GEMMs that consume them, all as hand-written CUDA kernels launched
+ * on the caller's stream.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named *_dev or documented as device pointers are CUDA device
+ *    memory owned and allocated by the caller.  The library allocates
+ *    nothing, frees nothing and keeps no reference after the call returns.
+ *  - Work is stream ordered on `stream` (NULL = the legacy default stream).
+ *    Calls never synchronize, except mxfp8_last_device_status().
+ *  - Errors the host can see (null pointers, bad shapes, misaligned pointers
+ *    or strides) are returned at once and launch nothing.  Errors only the
+ *    device can see (inconsistent group offsets, a wait that exceeded its
+ *    time limit) are recorded in a per-device status word that
+ *    mxfp8_last_device_status() reads; the kernels never trap.
+ *  - BF16 matrices are row-major with a leading dimension in elements.
+ *    "Alignment" below means the byte address is a multiple of 16.
+ *  - A GEMM computes C = A . B^T with A M x K and B N x K, both K-major
+ *    (the 32-value scale blocks run along K).  The forward, dgrad and wgrad
+ *    products of a linear layer (Y = X W^T, dX = dY W, dW = dY^T X) are all
+ *    expressed this way by quantizing each operand in the orientation whose
+ *    blocks run along that product's reduction axis ("Olmo-core MoE report,
+ *    Section 11: MXFP8 Training", Section 11.3.2, Eq. 60).
+ *
+ * Swizzled scale layout ("Olmo-core MoE report", Section 11.2.1, Figure 52):
+ *  the E8M0 scales of a rows x k operand (one per row and 32-value K-block j)
+ *  are stored in 512-byte tiles of 128 rows x 4 K-blocks; tile (r/128, j/4)
+ *  sits at byte ((r/128) * ceil(k/128) + j/4) * 512 and inside it scale (r, j)
+ *  sits at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 4).  This is the
+ *  order in which the tensor cores read block scales.  Padding rows and
+ *  blocks hold 0.  Size: mxfp8_scale_bytes(rows, k).
+ */
+#ifndef MXFP8_H
+#define MXFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* mxfp8_stream_t;
+
+typedef enum {
+    MXFP8_OK = 0,
+    MXFP8_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum  */
+    MXFP8_ERR_UNSUPPORTED_SHAPE = 2, /* divisibility or size limit violated   */
+    MXFP8_ERR_MISALIGNED = 3,        /* pointer or stride not 16-byte aligned */
+    MXFP8_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed   */
+    MXFP8_ERR_DEVICE_CHECK = 5,      /* device-side validation failed         */
+    MXFP8_ERR_TIMEOUT = 6            /* a device wait exceeded its time limit */
+} mxfp8_status;
+
+/* fp8_quantize_mx flags.  Scale rule default: rceil. */
+enum {
+    MX_ROWWISE = 1,     /* blocks along cols; q_row is rows x cols           */
+    MX_COLWISE = 2,     /* blocks along rows; q_col is cols x rows (= X^T)    */
+    MX_SCALE_FLOOR = 4  /* OCP v1.0 floor rule instead of rceil               */
+};
+
+/* FP8 payload formats. */
+enum { FP8_E4M3 = 0, FP8_E5M2 = 1 };
+
+/* fp8_scaled_gemm modes. */
+enum { GEMM_MX = 0, GEMM_TENSOR = 1 };
+
+/* Bytes of the swizzled E8M0 scale array of a rows x k operand whose blocks
+ * run along k: ceil(rows/128) * ceil(k/128) * 512.  Returns 0 for
+ * non-positive sizes.  ("Olmo-core MoE report", Section 11.2.1, Figure 52.) */
+size_t mxfp8_scale_bytes(int64_t rows, int64_t k);
+
+/* Upper bound on the bytes of a grouped scale array (see
+ * fp8_quantize_mx_grouped): (ceil(total_rows/128) + groups) * ceil(k/128) * 512. */
+size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t k, int32_t groups);
+
+/*
+ * fp8_quantize_mx - MXFP8 quantization of a BF16 matrix.
+ * ("Olmo-core MoE report", Section 11.2.1 Eq. 58 and Figure 50; scale rule
+ *  Section 11.3.5 / Table 24; one read emits both orientations, Section
+ *  11.1.4 and Figure 55.)
+ *
+ * Each 32-value block gets the E8M0 scale s = 2^e chosen from its largest
+ * magnitude amax:
+ *   rceil (default): the smallest e with amax <= 448 * 2^e;
+ *   MX_SCALE_FLOOR:  e = floor(log2 amax) - 8 (may saturate);
+ * e is clamped to [-127, 127] (an all-zero block gets byte 0); the payload is
+ * q = E4M3(x / s), round-to-nearest-even, saturating at +-448, zero keeps its
+ * sign.  A block holding NaN or Inf gets scale byte 0xFF and payload 0x7F.
+ *
+ *  x_bf16  device, rows x cols BF16, leading dimension ld (elements).
+ *  flags   MX_ROWWISE and/or MX_COLWISE, optionally MX_SCALE_FLOOR.
+ *  q_row   device, rows x cols bytes (row stride cols), when MX_ROWWISE.
+ *  s_row   device, mxfp8_scale_bytes(rows, cols) bytes, when MX_ROWWISE.
+ *  q_col   device, cols x rows bytes (row stride rows), when MX_COLWISE.
+ *  s_col   device, mxfp8_scale_bytes(cols, rows) bytes, when MX_COLWISE.
+ * Requirements: cols % 32 == 0; rows % 32 == 0 when MX_COLWISE; ld >= cols
+ * and ld % 8 == 0; every pointer 16-byte aligned.  Unused outputs may be NULL.
+ * Every byte of the scale arrays is written (padding = 0).
+ */
+mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                             unsigned flags, void* q_row, void* s_row, void* q_col,
+                             void* s_col, mxfp8_stream_t stream);
+
+/*
+ * fp8_quantize_mx_grouped - rowwise MXFP8 quantization of an expert-dispatched
+ * matrix whose rows are sorted by expert ("Olmo-core MoE report", Section
+ * 11.4.1: dispatch places each token row's qdata and scales in its expert's
+ * buffer).
+ *
+ * Group g owns rows [off[g], off[g+1]) of x.  Payload rows keep their
+ * positions (q is total_rows x cols).  Scales: each group is padded to a
+ * multiple of 128 rows, and group g's scales occupy rows
+ * P_g .. P_g + m_g - 1 of one swizzled array, P_g = sum_{h<g} ceil(m_h/128)*128;
+ * its padding rows are written as 0.  Bytes past the last padded group are
+ * not written.
+ *
+ *  group_offsets_dev  device, groups + 1 int32, off[0] = 0, non-decreasing,
+ *                     off[groups] = total_rows.  Checked on the device: a
+ *                     violation records MXFP8_ERR_DEVICE_CHECK and writes nothing.
+ *  s                  device, at least
+ *                     mxfp8_grouped_scale_bytes(total_rows, cols, groups) bytes.
+ * flags may hold MX_SCALE_FLOOR (MX_ROWWISE is implied).  1 <= groups <= 1024.
+ * Other requirements as fp8_quantize_mx.
+ */
+mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int64_t cols,
+                                     int64_t ld, const int32_t* group_offsets_dev,
+                                     int32_t groups, unsigned flags, void* q, void* s,
+                                     mxfp8_stream_t stream);
+
+/*
+ * fp8_quantize_tensor - per-tensor current-scaling FP8 quantization.
+ * ("3.8 Mixed Precision, bf16 & FP8 Training", "Per-tensor scaling and the
+ *  delayed-scaling recipe" and exercise 6; "FP8-LM: Training FP8 Large
+ *  Language Models", Section 3.4 tensor scaling.)
+ *
+ *   amax = max |x|;  s = fp32(fmax / max(amax, 1e-12));  q = FP8(fp32(x * s))
+ * with fmax = 448 (FP8_E4M3) or 57344 (FP8_E5M2, gradient operands), the FP8
+ * cast round-to-nearest-even and saturating.  x ~ q / s.
+ *
+ *  x_bf16     device, n BF16 values, 16-byte aligned.
+ *  amax_dev   device fp32 scalar, written (overwritten: not accumulated).
+ *  scale_dev  device fp32 scalar s, written.
+ *  q          device, n bytes, 16-byte aligned.
+ * n == 0 writes amax = 0 and s = fmax / 1e-12.
+ */
+mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
+                                 float* scale_dev, void* q, mxfp8_stream_t stream);
+
+/*
+ * fp8_scaled_gemm - C = A . B^T with FP32 accumulation and a BF16 epilogue
+ * (round to nearest even).
+ * ("Olmo-core MoE report", Section 11.1.1: block-scaled tcgen05.mma with an
+ *  epilogue converting the accumulator to BF16; "3.8 Mixed Precision, bf16 &
+ *  FP8 Training", exercise 6: per-tensor GEMM de-scaled by 1 / (s_x s_w).)
+ *
+ * GEMM_MX:     a, b E4M3 payloads (a_fmt = b_fmt = FP8_E4M3); a_scale, b_scale
+ *              device swizzled E8M0 arrays of mxfp8_scale_bytes(M, K) and
+ *              mxfp8_scale_bytes(N, K) bytes, as written by fp8_quantize_mx.
+ *              C[m,n] = bf16( sum_k s_a[m,k/32] q_a[m,k] * s_b[n,k/32] q_b[n,k] ).
+ *              K % 32 == 0.
+ * GEMM_TENSOR: a, b payloads in a_fmt / b_fmt (E4M3 or E5M2); a_scale, b_scale
+ *              device fp32 scalars s_a, s_b as written by fp8_quantize_tensor.
+ *              C[m,n] = bf16( (sum_k q_a[m,k] q_b[n,k]) / (s_a s_b) ).  K % 16 == 0.
+ *
+ *  a   device, M x K bytes (row stride K);  b  device, N x K bytes.
+ *  c   device BF16, M x N with leading dimension ldc (elements).
+ * Requirements: N % 8 == 0, ldc >= N, ldc % 8 == 0, all pointers 16-byte
+ * aligned.  M, N may be 0 (no work); K == 0 writes C = 0.
+ */
+mxfp8_status fp8_scaled_gemm(int mode, int a_fmt, int b_fmt, const void* a,
+                             const void* a_scale, const void* b, const void* b_scale,
+                             int64_t M, int64_t N, int64_t K, void* c_bf16, int64_t ldc,
+                             mxfp8_stream_t stream);
+
+/*
+ * fp8_grouped_gemm - per-expert MXFP8 GEMM over ragged, row-sorted groups.
+ * ("Olmo-core MoE report", Section 11.1.1 and 11.4.1: the grouped expert
+ *  GEMMs consume the dispatched activation and the cached expert weights.)
+ *
+ * For each group g with rows [off[g], off[g+1]):
+ *   C[off[g]:off[g+1], :] = MX-GEMM(A[off[g]:off[g+1], :], W_g)
+ *
+ *  a        device, total_rows x K E4M3 payload (row stride K).
+ *  a_scale  device, grouped swizzled scales as written by
+ *           fp8_quantize_mx_grouped with the same offsets.
+ *  b        device, groups x N x K E4M3 payload (expert g at b + g*N*K).
+ *  b_scale  device, groups consecutive swizzled arrays of
+ *           mxfp8_scale_bytes(N, K) bytes (expert g's at g times that size);
+ *           equivalently fp8_quantize_mx of the (groups*N) x K stack when
+ *           N % 128 == 0.
+ *  group_offsets_dev  as in fp8_quantize_mx_grouped; a violation records
+ *           MXFP8_ERR_DEVICE_CHECK and no output is written.
+ *  c        device BF16, total_rows x N, leading dimension ldc.
+ * Requirements: 1 <= groups <= 1024, K % 32 == 0, N % 8 == 0, ldc % 8 == 0,
+ * pointers 16-byte aligned.  Empty groups are allowed.
+ */
+mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
+                              const void* b_scale, const int32_t* group_offsets_dev,
+                              int32_t groups, int64_t total_rows, int64_t N, int64_t K,
+                              void* c_bf16, int64_t ldc, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_last_device_status - synchronize `stream`, then return and clear the
+ * device status word of the current device: MXFP8_OK, MXFP8_ERR_DEVICE_CHECK
+ * or MXFP8_ERR_TIMEOUT (the first one recorded since the last call), or
+ * MXFP8_ERR_CUDA if the synchronization itself failed.
+ */
+mxfp8_status mxfp8_last_device_status(mxfp8_stream_t stream);
+
+/* Static English text for a status code. */
+const char* mxfp8_status_string(mxfp8_status status);
+
+/* Detail of the most recent error returned on the calling thread ("" if none). */
+const char* mxfp8_last_error(void);
+
+/*
+ * Test hook: the time limit, in nanoseconds, after which a device-side wait
+ * gives up, records MXFP8_ERR_TIMEOUT and lets the kernel exit (default
+ * 2e9).  0 restores the default.  Affects launches issued after the call.
+ */
+void mxfp8_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook: when nonzero, the next GEMM launch makes its MMA-issuing thread
+ * wait on a barrier that nothing signals, so the wait runs out after the
+ * limit above and the kernel exits with MXFP8_ERR_TIMEOUT recorded.  The hook
+ * resets itself after one launch.
+ */
+void mxfp8_debug_inject_wait_timeout(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_H */

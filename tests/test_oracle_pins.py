@@ -1,0 +1,567 @@
+"""Pins of the FP64 oracle against facts fixed outside the oracle itself.
+
+Every test here runs on the CPU.  The pins are: values printed on the pages
+(tests/golden/*.txt), torch's own float8 conversions (an independent library
+implementation of the same encodings), brute force over all FP8 codes and
+all BF16 bit patterns, closed forms and invariants of the method, and numpy
+matmuls of operands dequantized without the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import pow2_or_float, read_golden, read_golden_table
+
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+ALL_CODES = np.arange(256, dtype=np.uint8)
+
+
+def torch_fp8_decode(codes, fmt):
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(dt).to(torch.float64).numpy()
+
+
+def torch_fp8_encode_f32(v32, fmt):
+    """torch's RNE cast of fp32 values (NOT saturating: out of range -> NaN/Inf)."""
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    return torch.from_numpy(np.asarray(v32, np.float32)).to(dt).view(torch.uint8).numpy()
+
+
+def all_bf16_bits():
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+def bf16_values_torch(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------ page values --
+
+def test_bf16_worked_value():
+    g = read_golden("bf16_worked_value.txt")
+    x32 = np.float32(float(g["input_fp32"]))
+    bits = oracle.bf16_round([float(x32)])[0]
+    assert bits == int(g["bf16_bits"], 16)
+    assert oracle.bf16_decode([bits])[0] == float(g["bf16_value"])
+
+
+def test_fig50_block():
+    g = read_golden("fig50_block.txt")
+    x = float(g["x"])
+    pos = int(g["position_1based"]) - 1
+    rng = np.random.default_rng(50)
+    # the other 31 values: any magnitudes at most 1.75, so x is the maximum
+    block = rng.uniform(-1.75, 1.75, 32)
+    block[pos] = x
+    bits = oracle.bf16_round(block)
+    assert oracle.bf16_decode([bits[pos]])[0] == x  # 2.28125 is a BF16 value
+    out = oracle.quantize_mx(bits.reshape(1, 32), oracle.ROWWISE)
+    s_byte = out["s_row"][oracle.swizzle_offset(0, 0, 32)]
+    assert s_byte == int(g["scale_byte"])
+    s = 2.0 ** (int(s_byte) - 127)
+    assert x / s == float(g["x_over_s"])
+    q = out["q_row"][0, pos]
+    assert q == int(g["q_bits"], 2)
+    assert oracle.fp8_decode([q])[0] == float(g["q_value"])
+    xhat = s * oracle.fp8_decode([q])[0]
+    assert xhat == float(g["xhat"])
+    assert round(100 * (xhat - x) / x, 1) == float(g["rel_error_percent"])
+    # the same byte for any block maximum in (1.75, 3.5]
+    for amax in (1.75 + 2**-6, 2.28125, 3.0, 3.5):
+        assert oracle.e8m0_scale_byte([amax])[0] == 120
+    assert oracle.e8m0_scale_byte([1.75])[0] == 119
+
+
+def test_scale_rule_a500():
+    g = read_golden("scale_rule_a500.txt")
+    a = float(g["amax"])
+    block = np.zeros(32)
+    block[0] = a
+    bits = oracle.bf16_round(block)
+    assert oracle.bf16_decode(bits[:1])[0] == 500.0
+    fl = oracle.quantize_mx(bits.reshape(1, 32), oracle.ROWWISE | oracle.SCALE_FLOOR)
+    rc = oracle.quantize_mx(bits.reshape(1, 32), oracle.ROWWISE)
+    assert fl["s_row"][0] == int(g["floor_scale_byte"])
+    assert 2.0 ** (int(fl["s_row"][0]) - 127) == float(g["floor_scale"])
+    assert fl["q_row"][0, 0] == int(g["floor_q_bits"], 16)
+    assert oracle.fp8_decode(fl["q_row"][0, :1])[0] == float(g["floor_q_value"])
+    assert rc["s_row"][0] == int(g["rceil_scale_byte"])
+    assert 2.0 ** (int(rc["s_row"][0]) - 127) == float(g["rceil_scale"])
+    assert rc["q_row"][0, 0] == int(g["rceil_q_bits_derived"], 16)
+    assert oracle.fp8_decode(rc["q_row"][0, :1])[0] == float(g["rceil_q_value_derived"])
+
+
+def _format_facts(fmt):
+    vals = oracle.fp8_decode(ALL_CODES, fmt)
+    pos = vals[(ALL_CODES < 0x80) & np.isfinite(vals) & (vals > 0)]
+    normal_codes = [c for c in range(1, 0x80)
+                    if np.isfinite(vals[c]) and ((c >> (3 if fmt == E4M3 else 2)) != 0)]
+    min_normal = min(vals[c] for c in normal_codes)
+    above_one = min(v for v in pos if v > 1.0)
+    return pos.max(), min_normal, pos.min(), above_one - 1.0
+
+
+def test_format_table():
+    rows = {r[0]: r[1:] for r in read_golden_table("format_table.txt")}
+    for name, fmt in (("E4M3", E4M3), ("E5M2", E5M2)):
+        mx, mn, sub, sp = _format_facts(fmt)
+        want = [pow2_or_float(v) for v in rows[name]]
+        assert (mx, mn, sub, sp) == tuple(want), name
+    # FP8-LM Section 3.4 decimals
+    assert abs(_format_facts(E4M3)[1] - 1.56e-2) < 1e-4
+    assert abs(_format_facts(E4M3)[2] - 1.95e-3) < 1e-5
+    assert abs(_format_facts(E5M2)[1] - 6.10e-5) < 1e-7
+    assert abs(_format_facts(E5M2)[2] - 1.53e-5) < 1e-7
+    # E8M0: bytes 0..254 are 2^-127 .. 2^127, 255 is NaN
+    assert oracle.e8m0_scale_byte([2.0 ** -200])[0] == 0
+    e8 = rows["E8M0"]
+    assert pow2_or_float(e8[0]) == 2.0 ** (254 - 127)
+    assert pow2_or_float(e8[1]) == 2.0 ** (0 - 127)
+    # BF16
+    b = oracle.bf16_decode(all_bf16_bits())
+    fin = b[np.isfinite(b) & (b > 0)]
+    bf = rows["BF16"]
+    assert abs(fin.max() / float(bf[0]) - 1) < 1e-3
+    assert fin[fin >= 2.0 ** -126].min() == pow2_or_float(bf[1])
+    assert fin.min() == pow2_or_float(bf[2])
+    assert fin[fin > 1.0].min() - 1.0 == pow2_or_float(bf[3])
+
+
+def test_storage_eq57():
+    g = read_golden("storage_eq57.txt")
+    per_value = 1 + 1 / 32
+    assert per_value == 33 / 32 == eval(g["bytes_per_value"])
+    assert round(100 * (1 - per_value / 2), 1) == float(g["saving_vs_bf16_percent"])
+    assert 2 * per_value == float(g["two_orientations_bytes_per_value"])
+    for rows, cols in ((128, 128), (256, 4096), (96, 64), (1, 32)):
+        x = oracle.bf16_round(np.random.default_rng(rows).normal(size=(rows, cols)))
+        out = oracle.quantize_mx(x, oracle.ROWWISE)
+        logical_scales = rows * cols // 32
+        assert out["q_row"].size + logical_scales == rows * cols * 33 // 32
+        # padded physical size follows the 128 x 4 tile geometry
+        assert out["s_row"].size == math.ceil(rows / 128) * math.ceil(cols / 128) * 512
+        if rows % 32 == 0:
+            both = oracle.quantize_mx(x, oracle.ROWWISE | oracle.COLWISE)
+            nbytes = both["q_row"].size + both["q_col"].size + 2 * logical_scales
+            assert nbytes == 2 * rows * cols * 33 // 32
+
+
+# ------------------------------------------------------ codecs vs torch --
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_fp8_decode_all_codes_vs_torch(fmt):
+    ours = oracle.fp8_decode(ALL_CODES, fmt)
+    ref = torch_fp8_decode(ALL_CODES, fmt)
+    both_nan = np.isnan(ours) & np.isnan(ref)
+    assert np.array_equal(ours[~both_nan], ref[~both_nan])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    # signed zeros
+    assert math.copysign(1, ours[0x80]) == -1 and ours[0x80] == 0
+    # NaN codes: E4M3 has exactly 0x7F / 0xFF, no infinity
+    if fmt == E4M3:
+        assert set(np.flatnonzero(np.isnan(ours))) == {0x7F, 0xFF}
+        assert not np.isinf(ours).any()
+    else:
+        assert set(np.flatnonzero(np.isinf(ours))) == {0x7C, 0xFC}
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_fp8_codes_monotone_and_roundtrip(fmt):
+    vals = oracle.fp8_decode(ALL_CODES, fmt)
+    top = 0x7E if fmt == E4M3 else 0x7B
+    pos = vals[: top + 1]
+    assert np.all(np.diff(pos) > 0)
+    finite = [c for c in range(256) if np.isfinite(vals[c])]
+    enc = oracle.fp8_encode(vals[finite], fmt)
+    assert np.array_equal(enc, np.array(finite, np.uint8))
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_fp8_encode_ties_to_even(fmt):
+    vals = oracle.fp8_decode(ALL_CODES, fmt)
+    top = 0x7E if fmt == E4M3 else 0x7B
+    for c in range(top):
+        mid = (vals[c] + vals[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.fp8_encode([mid], fmt)[0] == even
+        assert oracle.fp8_encode([-mid], fmt)[0] == even | 0x80
+        eps = (vals[c + 1] - vals[c]) * 1e-6
+        assert oracle.fp8_encode([mid - eps], fmt)[0] == c
+        assert oracle.fp8_encode([mid + eps], fmt)[0] == c + 1
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_fp8_encode_saturates(fmt):
+    top = 0x7E if fmt == E4M3 else 0x7B
+    mx = 448.0 if fmt == E4M3 else 57344.0
+    for v in (mx, mx * (1 + 2**-10), mx * 1.5, mx * 4, 1e30, math.inf):
+        assert oracle.fp8_encode([v], fmt)[0] == top
+        assert oracle.fp8_encode([-v], fmt)[0] == top | 0x80
+    assert oracle.fp8_encode([math.nan], fmt)[0] == 0x7F
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_fp8_encode_all_bf16_times_all_scales_vs_torch(fmt):
+    """Every BF16 pattern divided by every E8M0 scale: the MX payload step."""
+    b = all_bf16_bits()
+    x = bf16_values_torch(b)
+    x = x[np.isfinite(x)]
+    limit = 464.0 if fmt == E4M3 else 61440.0  # torch rounds |v| >= limit to NaN/Inf
+    mx = 448.0 if fmt == E4M3 else 57344.0
+    checked = 0
+    for e in range(-127, 128):
+        v = np.ldexp(x, -e)
+        # keep v exactly representable in fp32 so torch's fp32 cast sees it exactly
+        keep = (np.abs(v) >= 2.0 ** -140) & (np.abs(v) < 2.0 ** 100) | (v == 0)
+        v = v[keep]
+        if v.size == 0:
+            continue
+        ours = oracle.fp8_encode(v, fmt)
+        small = np.abs(v) < limit
+        ref = torch_fp8_encode_f32(v[small].astype(np.float32), fmt)
+        assert np.array_equal(ours[small], ref), e
+        big = ~small
+        want = np.where(np.signbit(v[big]), 0x80, 0) | (0x7E if fmt == E4M3 else 0x7B)
+        assert np.array_equal(ours[big], want.astype(np.uint8))
+        assert np.all(np.abs(oracle.fp8_decode(ours, fmt)) <= mx)
+        checked += v.size
+    assert checked > 5_000_000
+
+
+def test_bf16_round_vs_torch():
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.normal(size=20000), rng.normal(size=20000) * 1e-38,
+                        rng.normal(size=20000) * 1e30, [0.0, -0.0, 1.0, 3.1415927]])
+    v32 = v.astype(np.float32)
+    ref = torch.from_numpy(v32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = oracle.bf16_round(v32.astype(np.float64))
+    assert np.array_equal(ours, ref)
+    # decode agrees with torch for every pattern (NaNs aside)
+    b = all_bf16_bits()
+    ref_d = bf16_values_torch(b)
+    d = oracle.bf16_decode(b)
+    ok = ~np.isnan(ref_d)
+    assert np.array_equal(d[ok], ref_d[ok]) and np.isnan(d[~ok]).all()
+
+
+# ------------------------------------------------------------ E8M0 rules --
+
+def _positive_finite_bf16():
+    b = all_bf16_bits()
+    v = bf16_values_torch(b)
+    return v[np.isfinite(v) & (v > 0)]
+
+
+def test_rceil_all_bf16_amax():
+    a = _positive_finite_bf16()
+    byte = oracle.e8m0_scale_byte(a)
+    e = byte.astype(np.int64) - 127
+    # float evaluation of "amax / 448 rounded up to a power of two"
+    ef = np.ceil(np.log2(a / 448.0)).astype(np.int64)
+    assert np.array_equal(e, np.clip(ef, -127, 127))
+    # the definition: smallest e with amax <= 448 * 2^e (where not clamped)
+    free = e > -127
+    assert np.all(a[free] <= np.ldexp(448.0, e[free]))
+    assert np.all(a[free] > np.ldexp(448.0, e[free] - 1))
+    assert np.all(a[~free] <= np.ldexp(448.0, -127))
+    # rceil never saturates: amax / s <= 448
+    assert np.all(a / np.ldexp(1.0, e) <= 448.0)
+
+
+def test_floor_all_bf16_amax():
+    a = _positive_finite_bf16()
+    byte = oracle.e8m0_scale_byte(a, floor=True)
+    e = byte.astype(np.int64) - 127
+    _, x = np.frexp(a)
+    assert np.array_equal(e, np.clip(x - 1 - 8, -127, 127))
+    ef = np.floor(np.log2(a)).astype(np.int64) - 8
+    assert np.array_equal(e, np.clip(ef, -127, 127))
+    # floor is at most one binade finer than rceil
+    rc = oracle.e8m0_scale_byte(a).astype(np.int64)
+    assert np.all((rc - byte >= 0) & (rc - byte <= 1))
+
+
+def test_zero_and_tiny_blocks():
+    assert oracle.e8m0_scale_byte([0.0])[0] == 0
+    assert oracle.e8m0_scale_byte([0.0], floor=True)[0] == 0
+    assert oracle.e8m0_scale_byte([2.0 ** -133])[0] == 0
+    x = np.zeros((1, 32), np.uint16)
+    x[0, 5] = 0x8000  # -0
+    out = oracle.quantize_mx(x)
+    assert out["s_row"][0] == 0
+    assert out["q_row"][0, 5] == 0x80 and out["q_row"][0, 0] == 0x00
+    # a subnormal-only block: scale 2^-127, payload x * 2^127 is still exact
+    sub = np.zeros((1, 32), np.uint16)
+    sub[0, :] = np.arange(1, 33)  # bf16 subnormals k * 2^-133
+    out = oracle.quantize_mx(sub)
+    assert out["s_row"][0] == 0
+    want = oracle.fp8_encode(np.arange(1, 33) * 2.0 ** -133 * 2.0 ** 127)
+    assert np.array_equal(out["q_row"][0], want)
+
+
+def test_negative_values_rounding_to_zero_keep_sign():
+    block = np.full(32, 0.0)
+    block[0] = 300.0
+    block[1] = -1e-6
+    out = oracle.quantize_mx(oracle.bf16_round(block).reshape(1, 32))
+    assert out["q_row"][0, 1] == 0x80
+
+
+def test_nonfinite_block():
+    x = oracle.bf16_round(np.ones(64)).reshape(1, 64)
+    x[0, 3] = 0x7FC0  # NaN
+    x[0, 40] = 0x7F80  # Inf
+    out = oracle.quantize_mx(x)
+    assert out["s_row"][oracle.swizzle_offset(0, 0, 64)] == 0xFF
+    assert out["s_row"][oracle.swizzle_offset(0, 1, 64)] == 0xFF
+    assert np.all(out["q_row"] == 0x7F)
+
+
+# ------------------------------------------------ MX quantize, whole matrix --
+
+def _blocked_swizzle_index(rows, kblocks):
+    """Byte position of every logical scale (r, j), built by array reshapes:
+    pad to (R_t*128, K_t*4), view as (R_t, 4 groups, 32, K_t, 4), and order
+    the bytes as (R_t, K_t, 32, 4 groups, 4).  Written without the oracle."""
+    rt, kt = math.ceil(rows / 128), math.ceil(kblocks / 4)
+    idx = np.arange(rt * 128 * kt * 4).reshape(rt, 4, 32, kt, 4)
+    # idx[t, g, i, u, c] is the logical (row = t*128 + g*32 + i, block = u*4 + c)
+    logical = idx.reshape(rt * 128, kt * 4)
+    order = np.transpose(idx, (0, 3, 2, 1, 4)).reshape(-1)
+    pos = np.empty_like(order)
+    pos[order] = np.arange(order.size)
+    return pos[logical.reshape(-1)].reshape(rt * 128, kt * 4)[:rows, :kblocks]
+
+
+def _torch_mx_recipe(x_bits, floor=False):
+    """Independent MX quantization with torch ops: block amax, power-of-two
+    scale from a float evaluation, payload by torch's float8 cast of x / s."""
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    rows, cols = x.shape
+    blocks = x.reshape(rows, cols // 32, 32)
+    amax = blocks.abs().amax(dim=-1)
+    if floor:
+        e = torch.floor(torch.log2(amax)) - 8
+    else:
+        e = torch.ceil(torch.log2(amax / 448.0))
+    e = torch.where(amax == 0, torch.full_like(e, -127), e).clamp(-127, 127)
+    v = (blocks * torch.pow(2.0, -e).unsqueeze(-1)).to(torch.float32)
+    vs = v.clamp(-448.0, 448.0)  # torch's cast does not saturate by itself
+    q = vs.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, cols)
+    return q.numpy(), (e + 127).to(torch.int64).numpy()
+
+
+@pytest.mark.parametrize("dist", ["normal", "student", "loguniform", "outliers"])
+@pytest.mark.parametrize("floor", [False, True])
+def test_quantize_mx_vs_torch_recipe(dist, floor):
+    rng = np.random.default_rng(11)
+    rows, cols = 160, 320  # a ragged 128-row tile and a ragged K tile
+    if dist == "normal":
+        v = rng.normal(size=(rows, cols))
+    elif dist == "student":
+        v = rng.standard_t(4, size=(rows, cols))
+    elif dist == "loguniform":
+        v = 10 ** rng.uniform(-8, -2, size=(rows, cols)) * rng.choice([-1, 1], size=(rows, cols))
+    else:
+        v = rng.normal(size=(rows, cols)) * 0.02
+        v[:, rng.permutation(cols)[:4]] *= 50
+    x = oracle.bf16_round(v)
+    out = oracle.quantize_mx(x, oracle.ROWWISE | oracle.COLWISE | (oracle.SCALE_FLOOR if floor else 0))
+    q_ref, byte_ref = _torch_mx_recipe(x, floor)
+    assert np.array_equal(out["q_row"], q_ref)
+    pos = _blocked_swizzle_index(rows, cols // 32)
+    assert np.array_equal(out["s_row"][pos], byte_ref)
+    # colwise = the same recipe on the transposed matrix
+    qt_ref, bt_ref = _torch_mx_recipe(np.ascontiguousarray(x.T), floor)
+    assert np.array_equal(out["q_col"], qt_ref)
+    pos_t = _blocked_swizzle_index(cols, rows // 32)
+    assert np.array_equal(out["s_col"][pos_t], bt_ref)
+    # every byte not holding a logical scale is padding = 0
+    mask = np.ones(out["s_row"].size, bool)
+    mask[pos.reshape(-1)] = False
+    assert not out["s_row"][mask].any()
+
+
+def test_quantize_mx_error_bound():
+    """|x - x^| <= half an E4M3 spacing at x/s, times s (no saturation: rceil)."""
+    rng = np.random.default_rng(3)
+    x = oracle.bf16_round(rng.standard_t(3, size=(64, 256)))
+    out = oracle.quantize_mx(x)
+    xv = oracle.bf16_decode(x)
+    pos = _blocked_swizzle_index(64, 8)
+    s = np.ldexp(1.0, out["s_row"][pos].astype(int) - 127)
+    s_full = np.repeat(s, 32, axis=1)
+    v = xv / s_full
+    q = oracle.fp8_decode(out["q_row"])
+    assert np.all(np.abs(v) <= 448)
+    _, ex = np.frexp(np.abs(v))
+    spacing = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)  # E4M3: 3 mantissa bits, min normal 2^-6
+    assert np.all(np.abs(v - q) <= spacing / 2)
+
+
+def test_swizzle_bijective_and_geometry():
+    for rows, k in ((128, 128), (300, 96), (1, 32), (257, 4096)):
+        kb = k // 32
+        offs = np.array([[oracle.swizzle_offset(r, j, k) for j in range(kb)] for r in range(rows)])
+        assert len(np.unique(offs)) == rows * kb
+        assert offs.min() >= 0 and offs.max() < oracle.scale_bytes(rows, k)
+        kt = math.ceil(k / 128)
+        for r in range(0, rows, 37):
+            for j in range(kb):
+                assert offs[r, j] // 512 == (r // 128) * kt + j // 4  # its 128 x 4 tile
+        # 32-row groups of one 4-column tile: the 4 K-blocks of a row are adjacent
+        for r in range(0, rows, 29):
+            for j in range(0, kb - kb % 4, 4):
+                assert list(offs[r, j:j + 4] - offs[r, j]) == [0, 1, 2, 3]
+        assert np.array_equal(offs, _blocked_swizzle_index(rows, kb))
+
+
+def test_quantize_grouped_matches_per_group():
+    rng = np.random.default_rng(5)
+    counts = [0, 130, 1, 0, 255, 128]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = oracle.bf16_round(rng.normal(size=(off[-1], 96)))
+    q, s = oracle.quantize_mx_grouped(x, off)
+    base = 0
+    for g, m in enumerate(counts):
+        if m == 0:
+            continue
+        sub = oracle.quantize_mx(x[off[g]:off[g + 1]])
+        assert np.array_equal(q[off[g]:off[g + 1]], sub["q_row"])
+        nb = sub["s_row"].size
+        start = base // 128 * math.ceil(96 / 128) * 512
+        assert np.array_equal(s[start:start + nb], sub["s_row"])
+        base += (m + 127) // 128 * 128
+    assert s.size == base // 128 * 512
+
+
+# ------------------------------------------------------------ per-tensor --
+
+def _page_recipe(x_bits, fmt):
+    """The book's exercise-6 quantizer written with torch ops (fp32 tensors)."""
+    fmax = 448.0 if fmt == E4M3 else 57344.0
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).float()
+    amax = x.abs().amax().clamp_min(1e-12)
+    # the quotient as one correctly rounded fp32 division (tensor / tensor);
+    # torch's python-scalar / tensor form multiplies by a reciprocal instead
+    scale = torch.tensor(fmax, dtype=torch.float32) / amax
+    q = (x * scale).to(dt)
+    return x.abs().amax().item(), scale.item(), q.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("case", ["outliers", "tiny", "zeros", "loguniform"])
+def test_quantize_tensor_vs_page_recipe(fmt, case):
+    rng = np.random.default_rng(2)
+    if case == "outliers":
+        v = rng.normal(size=(64, 512))
+        v[:, rng.permutation(512)[:5]] *= 50
+    elif case == "tiny":
+        v = rng.normal(size=(37, 19)) * 1e-30
+    elif case == "zeros":
+        v = np.zeros((4, 8))
+    else:
+        v = 10 ** rng.uniform(-8, -2, size=(128, 64)) * rng.choice([-1, 1], size=(128, 64))
+    x = oracle.bf16_round(v)
+    amax, scale, q = oracle.quantize_tensor(x, fmt)
+    r_amax, r_scale, r_q = _page_recipe(x, fmt)
+    assert np.float32(amax) == np.float32(r_amax)
+    assert np.float32(scale).view(np.uint32) == np.float32(r_scale).view(np.uint32)
+    assert np.array_equal(q, r_q)
+    if amax >= np.float32(1e-12):  # below the clamp everything is tiny
+        top = 0x7E if fmt == E4M3 else 0x7B
+        i = np.argmax(np.abs(oracle.bf16_decode(x)))
+        assert q.reshape(-1)[i] & 0x7F == top  # amax * s rounds to the format max
+    else:
+        assert not np.any(q & 0x7F)
+
+
+# ------------------------------------------------------------------ GEMMs --
+
+def _deq_independent(q, s_bytes, rows, k):
+    """Dequantize with torch's float8 decode and the reshape-built swizzle."""
+    vals = torch_fp8_decode(q, E4M3).reshape(rows, k)
+    pos = _blocked_swizzle_index(rows, k // 32)
+    scales = np.ldexp(1.0, s_bytes[pos].astype(np.int64) - 127)
+    return vals * np.repeat(scales, 32, axis=1)
+
+
+def test_gemm_mx_vs_numpy():
+    rng = np.random.default_rng(9)
+    M, N, K = 130, 72, 160
+    a = oracle.quantize_mx(oracle.bf16_round(rng.standard_t(4, size=(M, K))))
+    b = oracle.quantize_mx(oracle.bf16_round(rng.normal(size=(N, K)) * 0.02))
+    ref = _deq_independent(a["q_row"], a["s_row"], M, K) @ _deq_independent(b["q_row"], b["s_row"], N, K).T
+    got = oracle.gemm_mx(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    rows = np.array([129, 0, 64])
+    got_r = oracle.gemm_mx(a["q_row"], a["s_row"], b["q_row"], b["s_row"], rows=rows)
+    assert np.array_equal(got_r, got[rows])
+
+
+def test_gemm_mx_special_cases_exact():
+    rng = np.random.default_rng(4)
+    N, K = 40, 64
+    b = oracle.quantize_mx(oracle.bf16_round(rng.normal(size=(N, K))))
+    bdeq = _deq_independent(b["q_row"], b["s_row"], N, K)
+    # one-hot A rows (value 1.0 = code 0x38 with scale byte 127)
+    M = K
+    qa = np.zeros((M, K), np.uint8)
+    qa[np.arange(M), np.arange(K)] = 0x38
+    sa = np.zeros(oracle.scale_bytes(M, K), np.uint8)
+    for r in range(M):
+        for j in range(K // 32):
+            sa[oracle.swizzle_offset(r, j, K)] = 127
+    got = oracle.gemm_mx(qa, sa, b["q_row"], b["s_row"])
+    assert np.array_equal(got, bdeq.T)  # C[m, n] = deq(B)[n, m], exactly
+    # K = 32 of small powers of two: the FP64 sum is exact
+    vals = 2.0 ** rng.integers(-3, 4, size=(8, 32)) * rng.choice([-1, 1], size=(8, 32))
+    a2 = oracle.quantize_mx(oracle.bf16_round(vals))
+    got2 = oracle.gemm_mx(a2["q_row"], a2["s_row"], a2["q_row"], a2["s_row"])
+    assert np.array_equal(got2, vals @ vals.T)
+
+
+@pytest.mark.parametrize("fa,fb", [(E4M3, E4M3), (E4M3, E5M2), (E5M2, E4M3)])
+def test_gemm_tensor_vs_page_recipe(fa, fb):
+    rng = np.random.default_rng(6)
+    X = oracle.bf16_round(rng.normal(size=(33, 96)))
+    W = oracle.bf16_round(rng.normal(size=(24, 96)) * 0.02)
+    ax, sx, qx = oracle.quantize_tensor(X, fa)
+    aw, sw, qw = oracle.quantize_tensor(W, fb)
+    got = oracle.gemm_tensor(qx.reshape(33, 96), fa, sx, qw.reshape(24, 96), fb, sw)
+    xf = torch_fp8_decode(qx, fa).reshape(33, 96)
+    wf = torch_fp8_decode(qw, fb).reshape(24, 96)
+    ref = (xf @ wf.T) / (float(sx) * float(sw))
+    assert np.allclose(got, ref, rtol=1e-12, atol=0)
+
+
+def test_gemm_grouped_vs_numpy():
+    rng = np.random.default_rng(8)
+    counts = [3, 0, 140, 1, 64]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    G, N, K = len(counts), 48, 96
+    x = oracle.bf16_round(rng.normal(size=(off[-1], K)))
+    qa, sa = oracle.quantize_mx_grouped(x, off)
+    w = oracle.bf16_round(rng.normal(size=(G * N, K)) * 0.02)
+    wq = oracle.quantize_mx(w)
+    qw = wq["q_row"].reshape(G, N, K)
+    # N % 128 != 0 here, so build the per-expert scale arrays one by one
+    sw = np.concatenate([oracle.quantize_mx(w[g * N:(g + 1) * N])["s_row"] for g in range(G)])
+    got = oracle.gemm_grouped(qa, sa, qw, sw, off)
+    base = 0
+    for g, m in enumerate(counts):
+        if m:
+            # group g's A rows are rows 0..m-1 of a padded block starting at `base`
+            start = base // 128 * math.ceil(K / 128) * 512
+            nb = oracle.scale_bytes(m, K)
+            adeq = _deq_independent(qa[off[g]:off[g + 1]], sa[start:start + nb], m, K)
+            wdeq = _deq_independent(qw[g], sw[g * oracle.scale_bytes(N, K):(g + 1) * oracle.scale_bytes(N, K)], N, K)
+            assert np.allclose(got[off[g]:off[g + 1]], adeq @ wdeq.T, rtol=1e-12, atol=1e-15)
+        base += (m + 127) // 128 * 128
+    want = [1, 150, 207]
+    got_w = oracle.gemm_grouped(qa, sa, qw, sw, off, want=want)
+    assert np.array_equal(got_w[want], got[want])
