@@ -1,0 +1,214 @@
+"""Python binding of the GB300 MXFP8 / per-tensor FP8 library (libmxfp8.so).
+
+Argument marshalling only: every step of quantization and GEMM runs in the
+library's CUDA kernels.  PyTorch supplies device memory (outputs are
+allocated with ``torch.empty`` when not passed in) and the current stream.
+The function names match the C ABI in ``include/mxfp8.h``.  There is no CPU
+fallback: calling any op without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxfp8.so")
+
+MXFP8_OK = 0
+MXFP8_ERR_INVALID_ARG = 1
+MXFP8_ERR_UNSUPPORTED_SHAPE = 2
+MXFP8_ERR_MISALIGNED = 3
+MXFP8_ERR_CUDA = 4
+MXFP8_ERR_DEVICE_CHECK = 5
+MXFP8_ERR_TIMEOUT = 6
+
+MX_ROWWISE, MX_COLWISE, MX_SCALE_FLOOR = 1, 2, 4
+FP8_E4M3, FP8_E5M2 = 0, 1
+GEMM_MX, GEMM_TENSOR = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXFP8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"mxfp8 status {status}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types set.  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I32, I, U = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                 ctypes.c_int, ctypes.c_uint)
+            st = ctypes.c_int
+            sigs = {
+                "mxfp8_scale_bytes": (ctypes.c_size_t, [I64, I64]),
+                "mxfp8_grouped_scale_bytes": (ctypes.c_size_t, [I64, I64, I32]),
+                "fp8_quantize_mx": (st, [P, I64, I64, I64, U, P, P, P, P, P]),
+                "fp8_quantize_mx_grouped": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
+                "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P]),
+                "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
+                "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
+                "mxfp8_last_device_status": (st, [P]),
+                "mxfp8_status_string": (ctypes.c_char_p, [st]),
+                "mxfp8_last_error": (ctypes.c_char_p, []),
+                "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+                "mxfp8_debug_inject_wait_timeout": (None, [I]),
+            }
+            for name, (res, args) in sigs.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != MXFP8_OK:
+        raise MXFP8Error(status, lib().mxfp8_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts) -> None:
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors passed to the library must live on a CUDA device")
+
+
+# ------------------------------------------------------------- sizes --
+
+def mxfp8_scale_bytes(rows: int, k: int) -> int:
+    return int(lib().mxfp8_scale_bytes(rows, k))
+
+
+def mxfp8_grouped_scale_bytes(total_rows: int, k: int, groups: int) -> int:
+    return int(lib().mxfp8_grouped_scale_bytes(total_rows, k, groups))
+
+
+# -------------------------------------------------------- quantization --
+
+def fp8_quantize_mx(x: torch.Tensor, flags: int = MX_ROWWISE, q_row=None, s_row=None,
+                    q_col=None, s_col=None, stream=None) -> dict:
+    """MXFP8-quantize a 2D BF16 tensor (row stride = x.stride(0)).
+
+    Returns {"q_row", "s_row"} and/or {"q_col", "s_col"} as uint8 tensors."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _need_cuda(x)
+    rows, cols = x.shape
+    dev = x.device
+    out = {}
+    if flags & MX_ROWWISE:
+        q_row = q_row if q_row is not None else torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        s_row = s_row if s_row is not None else torch.empty(mxfp8_scale_bytes(rows, cols), dtype=torch.uint8, device=dev)
+        out["q_row"], out["s_row"] = q_row, s_row
+    if flags & MX_COLWISE:
+        q_col = q_col if q_col is not None else torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        s_col = s_col if s_col is not None else torch.empty(mxfp8_scale_bytes(cols, rows), dtype=torch.uint8, device=dev)
+        out["q_col"], out["s_col"] = q_col, s_col
+    _check(lib().fp8_quantize_mx(_ptr(x), rows, cols, x.stride(0), flags, _ptr(q_row), _ptr(s_row),
+                                 _ptr(q_col), _ptr(s_col), _stream(stream)))
+    return out
+
+
+def fp8_quantize_mx_grouped(x: torch.Tensor, offsets: torch.Tensor, flags: int = 0, q=None, s=None,
+                            stream=None):
+    """Rowwise MXFP8 quantization of expert-sorted rows; offsets: int32 device tensor (G+1)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert offsets.dtype == torch.int32
+    _need_cuda(x, offsets)
+    rows, cols = x.shape
+    groups = offsets.numel() - 1
+    q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty(max(1, mxfp8_grouped_scale_bytes(rows, cols, groups)), dtype=torch.uint8,
+                        device=x.device)
+    _check(lib().fp8_quantize_mx_grouped(_ptr(x), rows, cols, x.stride(0), _ptr(offsets), groups,
+                                         flags, _ptr(q), _ptr(s), _stream(stream)))
+    return q, s
+
+
+def fp8_quantize_tensor(x: torch.Tensor, fmt: int = FP8_E4M3, q=None, amax=None, scale=None,
+                        stream=None):
+    """Per-tensor FP8 quantization; returns (q uint8, amax fp32[1], scale fp32[1])."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    _need_cuda(x)
+    q = q if q is not None else torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    amax = amax if amax is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    scale = scale if scale is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().fp8_quantize_tensor(_ptr(x), x.numel(), fmt, _ptr(amax), _ptr(scale), _ptr(q),
+                                     _stream(stream)))
+    return q, amax, scale
+
+
+# --------------------------------------------------------------- GEMMs --
+
+def fp8_scaled_gemm(mode: int, a: torch.Tensor, a_scale: torch.Tensor, b: torch.Tensor,
+                    b_scale: torch.Tensor, c=None, a_fmt: int = FP8_E4M3, b_fmt: int = FP8_E4M3,
+                    stream=None) -> torch.Tensor:
+    """C = A . B^T (A: M x K, B: N x K uint8 payloads) -> BF16 M x N."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8 and a.dim() == 2 and b.dim() == 2
+    _need_cuda(a, b, a_scale, b_scale)
+    M, K = a.shape
+    N = b.shape[0]
+    assert b.shape[1] == K and a.is_contiguous() and b.is_contiguous()
+    c = c if c is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check(lib().fp8_scaled_gemm(mode, a_fmt, b_fmt, _ptr(a), _ptr(a_scale), _ptr(b), _ptr(b_scale),
+                                 M, N, K, _ptr(c), c.stride(0), _stream(stream)))
+    return c
+
+
+def fp8_grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, b: torch.Tensor, b_scale: torch.Tensor,
+                     offsets: torch.Tensor, c=None, stream=None) -> torch.Tensor:
+    """Per-expert MX GEMM: a (total_rows x K), b (G x N x K), offsets int32 (G+1)."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8 and b.dim() == 3
+    _need_cuda(a, a_scale, b, b_scale, offsets)
+    total, K = a.shape
+    G, N, Kb = b.shape
+    assert Kb == K and offsets.numel() == G + 1 and offsets.dtype == torch.int32
+    c = c if c is not None else torch.empty((total, N), dtype=torch.bfloat16, device=a.device)
+    _check(lib().fp8_grouped_gemm(_ptr(a), _ptr(a_scale), _ptr(b), _ptr(b_scale), _ptr(offsets), G,
+                                  total, N, K, _ptr(c), c.stride(0), _stream(stream)))
+    return c
+
+
+# -------------------------------------------------------------- status --
+
+def mxfp8_last_device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device status word."""
+    return int(lib().mxfp8_last_device_status(_stream(stream)))
+
+
+def mxfp8_status_string(status: int) -> str:
+    return lib().mxfp8_status_string(status).decode()
+
+
+def mxfp8_last_error() -> str:
+    return lib().mxfp8_last_error().decode()
+
+
+def mxfp8_set_wait_limit_ns(ns: int) -> None:
+    lib().mxfp8_set_wait_limit_ns(ns)
+
+
+def mxfp8_debug_inject_wait_timeout(enable: bool) -> None:
+    lib().mxfp8_debug_inject_wait_timeout(1 if enable else 0)

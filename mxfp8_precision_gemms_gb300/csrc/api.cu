@@ -1,0 +1,269 @@
+// C ABI of the library (declared in include/mxfp8.h): argument validation,
+// then stream-ordered kernel launches.  Nothing here allocates device memory
+// or synchronizes, except mxfp8_last_device_status().
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace mxfp8 {
+
+namespace {
+
+thread_local char g_err[256] = "";
+std::atomic<uint64_t> g_wait_limit{2000000000ull};
+std::atomic<int> g_inject{0};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+mxfp8_status fail(mxfp8_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+mxfp8_status fail(mxfp8_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+mxfp8_status ok() {
+    g_err[0] = '\0';
+    return MXFP8_OK;
+}
+
+mxfp8_status cuda_result(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit.load(); }
+bool take_inject_timeout() { return g_inject.exchange(0) != 0; }
+
+int sm_count_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = g_sm_count[dev].load();
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        g_sm_count[dev].store(n);
+    }
+    return n;
+}
+
+}  // namespace mxfp8
+
+using namespace mxfp8;
+
+extern "C" {
+
+size_t mxfp8_scale_bytes(int64_t rows, int64_t k) {
+    if (rows <= 0 || k <= 0) return 0;
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((k + 127) / 128) * 512u;
+}
+
+size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t k, int32_t groups) {
+    if (total_rows < 0 || k <= 0 || groups <= 0) return 0;
+    return static_cast<size_t>((total_rows + 127) / 128 + groups) *
+           static_cast<size_t>((k + 127) / 128) * 512u;
+}
+
+mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                             unsigned flags, void* q_row, void* s_row, void* q_col, void* s_col,
+                             mxfp8_stream_t stream) {
+    const bool row = flags & MX_ROWWISE, col = flags & MX_COLWISE;
+    if (flags & ~7u) return fail(MXFP8_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+    if (!row && !col) return fail(MXFP8_ERR_INVALID_ARG, "flags select no orientation");
+    if (rows < 0 || cols < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (rows == 0 || cols == 0) return ok();
+    if (!x_bf16) return fail(MXFP8_ERR_INVALID_ARG, "x is NULL");
+    if (row && (!q_row || !s_row)) return fail(MXFP8_ERR_INVALID_ARG, "rowwise output is NULL");
+    if (col && (!q_col || !s_col)) return fail(MXFP8_ERR_INVALID_ARG, "colwise output is NULL");
+    if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (cols=%lld)", (long long)cols);
+    if (col && rows % 32)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "colwise needs rows %% 32 == 0 (rows=%lld)", (long long)rows);
+    if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");
+    if (ld % 8 || !aligned16(x_bf16)) return fail(MXFP8_ERR_MISALIGNED, "x or ld not 16-byte aligned");
+    if ((row && (!aligned16(q_row) || !aligned16(s_row))) || (col && (!aligned16(q_col) || !aligned16(s_col))))
+        return fail(MXFP8_ERR_MISALIGNED, "output pointer not 16-byte aligned");
+    QuantMxArgs a{};
+    a.x = static_cast<const uint16_t*>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld = ld;
+    a.q_row = static_cast<uint8_t*>(q_row);
+    a.s_row = static_cast<uint8_t*>(s_row);
+    a.q_col = static_cast<uint8_t*>(q_col);
+    a.s_col = static_cast<uint8_t*>(s_col);
+    a.flags = flags;
+    return cuda_result(launch_quantize_mx(a, reinterpret_cast<cudaStream_t>(stream)), "fp8_quantize_mx launch");
+}
+
+mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int64_t cols,
+                                     int64_t ld, const int32_t* group_offsets_dev, int32_t groups,
+                                     unsigned flags, void* q, void* s, mxfp8_stream_t stream) {
+    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
+        return fail(MXFP8_ERR_INVALID_ARG, "grouped quantization is rowwise only");
+    if (groups <= 0) return fail(MXFP8_ERR_INVALID_ARG, "groups must be >= 1");
+    if (groups > 1024) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "groups > 1024");
+    if (total_rows < 0 || cols < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (total_rows > 0x7FFFFFFF) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "total_rows >= 2^31");
+    if (!group_offsets_dev) return fail(MXFP8_ERR_INVALID_ARG, "group_offsets is NULL");
+    if (cols == 0) return ok();
+    if (!x_bf16 && total_rows > 0) return fail(MXFP8_ERR_INVALID_ARG, "x is NULL");
+    if (!q || !s) return fail(MXFP8_ERR_INVALID_ARG, "output is NULL");
+    if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0");
+    if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");
+    if (ld % 8 || !aligned16(x_bf16) || !aligned16(q) || !aligned16(s))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer or ld not 16-byte aligned");
+    QuantMxArgs a{};
+    a.x = static_cast<const uint16_t*>(x_bf16);
+    a.rows = total_rows;
+    a.cols = cols;
+    a.ld = ld;
+    a.q_row = static_cast<uint8_t*>(q);
+    a.s_row = static_cast<uint8_t*>(s);
+    a.offsets = group_offsets_dev;
+    a.groups = groups;
+    a.flags = flags | MX_ROWWISE;
+    return cuda_result(launch_quantize_mx_grouped(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_mx_grouped launch");
+}
+
+mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
+                                 float* scale_dev, void* q, mxfp8_stream_t stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (!amax_dev || !scale_dev) return fail(MXFP8_ERR_INVALID_ARG, "amax/scale is NULL");
+    if (n > 0 && (!x_bf16 || !q)) return fail(MXFP8_ERR_INVALID_ARG, "x or q is NULL");
+    if ((n > 0 && (!aligned16(x_bf16) || !aligned16(q))) ||
+        (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
+    return cuda_result(launch_quantize_tensor(static_cast<const uint16_t*>(x_bf16), n, fmt, amax_dev,
+                                              scale_dev, static_cast<uint8_t*>(q),
+                                              reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_tensor launch");
+}
+
+mxfp8_status fp8_scaled_gemm(int mode, int a_fmt, int b_fmt, const void* a, const void* a_scale,
+                             const void* b, const void* b_scale, int64_t M, int64_t N, int64_t K,
+                             void* c_bf16, int64_t ldc, mxfp8_stream_t stream) {
+    if (mode != GEMM_MX && mode != GEMM_TENSOR) return fail(MXFP8_ERR_INVALID_ARG, "unknown mode %d", mode);
+    if ((a_fmt != FP8_E4M3 && a_fmt != FP8_E5M2) || (b_fmt != FP8_E4M3 && b_fmt != FP8_E5M2))
+        return fail(MXFP8_ERR_INVALID_ARG, "unknown format");
+    if (mode == GEMM_MX && (a_fmt != FP8_E4M3 || b_fmt != FP8_E4M3))
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode takes E4M3 payloads");
+    if (M < 0 || N < 0 || K < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (M == 0 || N == 0) return ok();
+    if (!c_bf16) return fail(MXFP8_ERR_INVALID_ARG, "c is NULL");
+    if (ldc < N) return fail(MXFP8_ERR_INVALID_ARG, "ldc < N");
+    if (N % 8 || ldc % 8 || !aligned16(c_bf16))
+        return fail(MXFP8_ERR_MISALIGNED, "N, ldc or c not 16-byte aligned");
+    if (K == 0) return cuda_result(launch_zero_fill_bf16(static_cast<uint16_t*>(c_bf16), M, N, ldc,
+                                                         reinterpret_cast<cudaStream_t>(stream)),
+                                   "zero fill");
+    if (!a || !b || !a_scale || !b_scale) return fail(MXFP8_ERR_INVALID_ARG, "operand or scale is NULL");
+    if (mode == GEMM_MX && K % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode needs K %% 32 == 0");
+    if (K % 16) return fail(MXFP8_ERR_MISALIGNED, "K %% 16 != 0 (row stride of A/B)");
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    if (!aligned16(a) || !aligned16(b)) return fail(MXFP8_ERR_MISALIGNED, "operand not 16-byte aligned");
+    if (mode == GEMM_MX && (!aligned16(a_scale) || !aligned16(b_scale)))
+        return fail(MXFP8_ERR_MISALIGNED, "scale array not 16-byte aligned");
+    if (mode == GEMM_TENSOR &&
+        ((reinterpret_cast<uintptr_t>(a_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_scale) & 3u)))
+        return fail(MXFP8_ERR_MISALIGNED, "scale scalar not 4-byte aligned");
+    GemmArgs g{};
+    g.mode = mode;
+    g.a_fmt = a_fmt;
+    g.b_fmt = b_fmt;
+    g.a = static_cast<const uint8_t*>(a);
+    g.a_scale = a_scale;
+    g.b = static_cast<const uint8_t*>(b);
+    g.b_scale = b_scale;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.c = static_cast<uint16_t*>(c_bf16);
+    g.ldc = ldc;
+    return cuda_result(launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "fp8_scaled_gemm launch");
+}
+
+mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b, const void* b_scale,
+                              const int32_t* group_offsets_dev, int32_t groups, int64_t total_rows,
+                              int64_t N, int64_t K, void* c_bf16, int64_t ldc, mxfp8_stream_t stream) {
+    if (groups <= 0) return fail(MXFP8_ERR_INVALID_ARG, "groups must be >= 1");
+    if (groups > 1024) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "groups > 1024");
+    if (total_rows < 0 || N < 0 || K < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (!group_offsets_dev) return fail(MXFP8_ERR_INVALID_ARG, "group_offsets is NULL");
+    if (total_rows == 0 || N == 0) return ok();
+    if (!c_bf16) return fail(MXFP8_ERR_INVALID_ARG, "c is NULL");
+    if (ldc < N) return fail(MXFP8_ERR_INVALID_ARG, "ldc < N");
+    if (N % 8 || ldc % 8 || !aligned16(c_bf16))
+        return fail(MXFP8_ERR_MISALIGNED, "N, ldc or c not 16-byte aligned");
+    if (K == 0) return cuda_result(launch_zero_fill_bf16(static_cast<uint16_t*>(c_bf16), total_rows, N, ldc,
+                                                         reinterpret_cast<cudaStream_t>(stream)),
+                                   "zero fill");
+    if (!a || !b || !a_scale || !b_scale) return fail(MXFP8_ERR_INVALID_ARG, "operand or scale is NULL");
+    if (K % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "K %% 32 != 0");
+    if (total_rows > 0x7FFFFFFF || static_cast<int64_t>(groups) * N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    if (!aligned16(a) || !aligned16(b) || !aligned16(a_scale) || !aligned16(b_scale))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer not 16-byte aligned");
+    GemmArgs g{};
+    g.mode = GEMM_MX;
+    g.a_fmt = g.b_fmt = FP8_E4M3;
+    g.a = static_cast<const uint8_t*>(a);
+    g.a_scale = a_scale;
+    g.b = static_cast<const uint8_t*>(b);
+    g.b_scale = b_scale;
+    g.M = total_rows;
+    g.N = N;
+    g.K = K;
+    g.c = static_cast<uint16_t*>(c_bf16);
+    g.ldc = ldc;
+    g.offsets = group_offsets_dev;
+    g.groups = groups;
+    return cuda_result(launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "fp8_grouped_gemm launch");
+}
+
+mxfp8_status mxfp8_last_device_status(mxfp8_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+    unsigned q = 0, g = 0;
+    if ((e = take_status_quant(&q)) != cudaSuccess || (e = take_status_gemm(&g)) != cudaSuccess)
+        return fail(MXFP8_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    const unsigned st = q ? q : g;
+    if (st) return fail(static_cast<mxfp8_status>(st), "device reported %s",
+                        mxfp8_status_string(static_cast<mxfp8_status>(st)));
+    return ok();
+}
+
+const char* mxfp8_status_string(mxfp8_status s) {
+    switch (s) {
+        case MXFP8_OK: return "ok";
+        case MXFP8_ERR_INVALID_ARG: return "invalid argument";
+        case MXFP8_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MXFP8_ERR_MISALIGNED: return "misaligned pointer or stride";
+        case MXFP8_ERR_CUDA: return "CUDA error";
+        case MXFP8_ERR_DEVICE_CHECK: return "device-side check failed";
+        case MXFP8_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* mxfp8_last_error(void) { return g_err; }
+
+void mxfp8_set_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns ? ns : 2000000000ull); }
+
+void mxfp8_debug_inject_wait_timeout(int enable) { g_inject.store(enable ? 1 : 0); }
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mxfp8.h"
+
+namespace mxfp8 {
+
+// Launch parameters of the MX quantizer (plain or grouped rows).
+struct QuantMxArgs {
+    const uint16_t* x;
+    int64_t rows;       // plain: rows of x; grouped: total rows
+    int64_t cols;
+    int64_t ld;
+    uint8_t* q_row;
+    uint8_t* s_row;
+    uint8_t* q_col;
+    uint8_t* s_col;
+    const int32_t* offsets;  // grouped only (device)
+    int32_t groups;          // grouped only
+    unsigned flags;
+};
+
+cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
+                                   float* scale, uint8_t* q, cudaStream_t s);
+
+struct GemmArgs {
+    int mode;          // GEMM_MX or GEMM_TENSOR
+    int a_fmt, b_fmt;  // FP8_E4M3 / FP8_E5M2
+    const uint8_t* a;
+    const void* a_scale;
+    const uint8_t* b;
+    const void* b_scale;
+    int64_t M, N, K;   // grouped: M = total rows
+    uint16_t* c;
+    int64_t ldc;
+    const int32_t* offsets;  // grouped only (device)
+    int32_t groups;          // grouped: number of experts; plain: 0
+};
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc,
+                                  cudaStream_t s);
+
+// Per-translation-unit device status words: read (and clear) after a sync.
+cudaError_t take_status_quant(unsigned* out);
+cudaError_t take_status_gemm(unsigned* out);
+
+// Time limit for device waits (ns) and the one-shot timeout-injection hook.
+uint64_t wait_limit_ns();
+bool take_inject_timeout();
+
+int sm_count_current_device();
+
+}  // namespace mxfp8

@@ -1,0 +1,397 @@
+// Quantizer kernels: MXFP8 (32-value blocks, E8M0 scales written straight
+// into the swizzled tensor-core layout, rowwise and/or colwise from one read
+// of the BF16 input) and per-tensor current-scaling FP8 (amax + cast).
+//
+// MX rule ("Olmo-core MoE report, Section 11: MXFP8 Training", Eq. 58 and
+// Section 11.3.5): per block, amax -> E8M0 scale s = 2^e (rceil: smallest e
+// with amax <= 448 * 2^e; floor: e = floor(log2 amax) - 8), clamped to
+// [-127, 127]; payload q = E4M3(x / s), round to nearest even, saturating.
+// Per-tensor rule ("3.8 Mixed Precision, bf16 & FP8 Training", exercise 6):
+// s = fp32(fmax / max(amax, 1e-12)), q = FP8(fp32(x * s)).
+#include <algorithm>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace mxfp8 {
+
+__device__ unsigned int g_status_quant = 0;
+
+namespace {
+
+constexpr int kTile = 128;     // rows and columns of one quantizer tile
+constexpr int kThreads = 256;  // 8 warps; each half-warp covers one tile row
+
+__device__ __forceinline__ void record_status(unsigned code) {
+    atomicCAS(&g_status_quant, 0u, code);
+}
+
+// E8M0 byte (e + 127) of a block from the bit pattern of its largest BF16
+// magnitude.  BF16 magnitude bits order like the magnitudes, with Inf and
+// NaN (>= 0x7F80) above every finite value.  For a normal amax with exponent
+// field f and mantissa field m: amax = (1 + m/128) 2^(f-127) and 448 = 1.75 2^8,
+// so rceil gives e = f - 135 + (m > 0x60) and floor gives e = f - 135.
+// Zero and subnormal amax fall below the clamp (byte 0).
+__device__ __forceinline__ uint32_t e8m0_byte(uint32_t amax_bits, bool floor_rule) {
+    if (amax_bits >= 0x7F80u) return 0xFFu;
+    const int f = static_cast<int>(amax_bits >> 7);
+    const int byte = f - 8 + ((!floor_rule && (amax_bits & 0x7Fu) > 0x60u) ? 1 : 0);
+    return byte < 0 ? 0u : static_cast<uint32_t>(byte);
+}
+
+// 1 / s = 2^(127 - byte) as an fp32 power of two (byte <= 247 for finite
+// BF16 input, so the exponent field 254 - byte stays normal).
+__device__ __forceinline__ float inv_scale(uint32_t byte) {
+    return __uint_as_float((254u - byte) << 23);
+}
+
+// Largest BF16 magnitude bits among the 8 values of a 16-byte vector.
+__device__ __forceinline__ uint32_t amax8(const uint4& v) {
+    uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Saturating RNE conversion of two fp32 values; `lo` lands in the low byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == FP8_E4M3) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
+// Four consecutive BF16 values (two words) times a factor -> four E4M3 bytes.
+// The product by a power of two is exact (no FTZ in this file).
+__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float f) {
+    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
+    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
+    return a | (b << 16);
+}
+
+// Same for four values held in the low (or high) halves of four words.
+template <bool HIGH>
+__device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                uint32_t w3, float f) {
+    auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
+    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
+    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
+    return a | (b << 16);
+}
+
+// Byte offset, inside its 512-byte tile, of the 4-byte group of scales of
+// tile row r (0..127): 32-row groups x 4 K-blocks per tile.
+__device__ __forceinline__ int swz_word(int r) { return (r & 31) * 16 + (r >> 5) * 4; }
+
+// One CTA quantizes a 128 x 128 tile.  blockIdx.x = 128-row scale tile,
+// blockIdx.y = 128-column tile.  Rowwise: a half-warp owns one tile row per
+// step (16 lanes x 8 values), 4 lanes per 32-value block.  Colwise: the tile
+// is staged in shared memory and each thread quantizes two columns of one
+// 32-row block.
+template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
+__global__ void __launch_bounds__(kThreads)
+    quantize_mx_kernel(QuantMxArgs a, int64_t nkc_row, int64_t nkc_col) {
+    __shared__ __align__(16) uint32_t tile[COL ? kTile * kTile / 2 : 4];
+    __shared__ __align__(16) uint8_t col_scales[COL ? kTile * 4 : 16];
+    __shared__ int64_t s_rows[2];
+    __shared__ int s_ok;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int64_t rt = blockIdx.x;
+    const int64_t ct = blockIdx.y;
+    int64_t row_begin, row_end;
+
+    if constexpr (GROUPED) {
+        // Find the group owning padded row tile rt; validate the offsets.
+        if (tid < 32) {
+            const int32_t* off = a.offsets;
+            const int G = a.groups;
+            bool ok = (off[0] == 0) && (static_cast<int64_t>(off[G]) == a.rows);
+            int64_t base = 0, found_begin = -1, found_end = -1;
+            for (int g0 = 0; g0 < G; g0 += 32) {
+                const int g = g0 + lane;
+                int64_t tiles = 0, b = 0, e = 0;
+                if (g < G) {
+                    b = off[g];
+                    e = off[g + 1];
+                    if (e < b) ok = false;
+                    tiles = e > b ? (e - b + kTile - 1) / kTile : 0;
+                }
+                int64_t incl = tiles;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += v;
+                }
+                const int64_t excl = base + incl - tiles;
+                if (g < G && rt >= excl && rt < excl + tiles) {
+                    found_begin = b + (rt - excl) * kTile;
+                    found_end = min(e, found_begin + kTile);
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            const unsigned who = __ballot_sync(0xffffffffu, found_begin >= 0);
+            if (lane == 0) {
+                s_ok = ok ? 1 : 0;
+                s_rows[0] = -1;
+                s_rows[1] = -1;
+            }
+            __syncwarp();
+            if (who && lane == __ffs(who) - 1) {
+                s_rows[0] = found_begin;
+                s_rows[1] = found_end;
+            }
+        }
+        __syncthreads();
+        if (!s_ok) {
+            if (rt == 0 && ct == 0 && tid == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
+            return;
+        }
+        row_begin = s_rows[0];
+        row_end = s_rows[1];
+        if (row_begin < 0) return;  // past the last padded tile
+    } else {
+        row_begin = rt * kTile;
+        row_end = min(a.rows, row_begin + kTile);
+    }
+
+    // ---- load the tile: 8 x 16 bytes per thread, all issued up front
+    const int seg = tid & 15;
+    const int64_t col = ct * kTile + seg * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = it * 16 + (tid >> 4);
+        const int64_t row = row_begin + r;
+        if (row < row_end && col < a.cols) {
+            v[it] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + col));
+        } else {
+            v[it] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    if constexpr (ROW) {
+        uint8_t* s_tile = a.s_row + (rt * nkc_row + ct) * 512;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 16 + (tid >> 4);
+            uint32_t m = amax8(v[it]);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t byte = e8m0_byte(m, FLOOR);
+            uint2 q;
+            if (byte == 0xFFu) {
+                q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            } else {
+                const float f = inv_scale(byte);
+                q.x = quant4_e4m3(v[it].x, v[it].y, f);
+                q.y = quant4_e4m3(v[it].z, v[it].w, f);
+            }
+            const int64_t row = row_begin + r;
+            if (row < row_end && col < a.cols) {
+                *reinterpret_cast<uint2*>(a.q_row + row * a.cols + col) = q;
+            }
+            const int hb = lane & 16;
+            const uint32_t b0 = __shfl_sync(0xffffffffu, byte, hb + 0);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, byte, hb + 4);
+            const uint32_t b2 = __shfl_sync(0xffffffffu, byte, hb + 8);
+            const uint32_t b3 = __shfl_sync(0xffffffffu, byte, hb + 12);
+            if (seg == 0) {
+                *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) =
+                    b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+        }
+    }
+
+    if constexpr (COL) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 16 + (tid >> 4);
+            reinterpret_cast<uint4*>(tile)[r * (kTile / 8) + seg] = v[it];
+        }
+        __syncthreads();
+        const int cp = tid & 63;  // column pair: tile columns 2cp, 2cp+1
+        const int j = tid >> 6;   // 32-row block of the tile
+        uint32_t w[32];
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            w[i] = tile[(j * 32 + i) * (kTile / 2) + cp];
+            m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+        }
+        const uint32_t byte_lo = e8m0_byte(m & 0xFFFFu, FLOOR);
+        const uint32_t byte_hi = e8m0_byte(m >> 16, FLOOR);
+        col_scales[(2 * cp) * 4 + j] = static_cast<uint8_t>(byte_lo);
+        col_scales[(2 * cp + 1) * 4 + j] = static_cast<uint8_t>(byte_hi);
+        uint32_t qlo[8], qhi[8];
+        const float flo = byte_lo == 0xFFu ? 0.f : inv_scale(byte_lo);
+        const float fhi = byte_hi == 0xFFu ? 0.f : inv_scale(byte_hi);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qlo[i] = byte_lo == 0xFFu
+                         ? 0x7F7F7F7Fu
+                         : quant4_half<false>(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3], flo);
+            qhi[i] = byte_hi == 0xFFu
+                         ? 0x7F7F7F7Fu
+                         : quant4_half<true>(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3], fhi);
+        }
+        const int64_t k0 = ct * kTile + 2 * cp;  // output row (an input column)
+        const int64_t r0 = rt * kTile + j * 32;  // output column (an input row)
+        if (r0 < a.rows) {
+            if (k0 < a.cols) {
+                uint4* dst = reinterpret_cast<uint4*>(a.q_col + k0 * a.rows + r0);
+                dst[0] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
+                dst[1] = make_uint4(qlo[4], qlo[5], qlo[6], qlo[7]);
+            }
+            if (k0 + 1 < a.cols) {
+                uint4* dst = reinterpret_cast<uint4*>(a.q_col + (k0 + 1) * a.rows + r0);
+                dst[0] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
+                dst[1] = make_uint4(qhi[4], qhi[5], qhi[6], qhi[7]);
+            }
+        }
+        __syncthreads();
+        if (tid < kTile) {
+            uint8_t* s_tile = a.s_col + (ct * nkc_col + rt) * 512;
+            *reinterpret_cast<uint32_t*>(s_tile + swz_word(tid)) =
+                reinterpret_cast<const uint32_t*>(col_scales)[tid];
+        }
+    }
+}
+
+// ---------------------------------------------------------- per-tensor --
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t m) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    return m;
+}
+
+// amax of |x| as BF16 magnitude bits, merged into *amax_bits (pre-zeroed) as
+// the fp32 bit pattern (positive fp32 patterns order like their values).
+__global__ void __launch_bounds__(256)
+    tensor_amax_kernel(const uint16_t* __restrict__ x, int64_t n, unsigned* amax_bits) {
+    __shared__ uint32_t red[8];
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    uint32_t m = 0;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+        const uint4 a0 = x8[i], a1 = x8[i + stride], a2 = x8[i + 2 * stride],
+                    a3 = x8[i + 3 * stride];
+        m = max(m, max(max(amax8(a0), amax8(a1)), max(amax8(a2), amax8(a3))));
+    }
+    for (; i < n8; i += stride) m = max(m, amax8(x8[i]));
+    for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+         t += stride)
+        m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0u;
+        m = warp_max(m);
+        if (threadIdx.x == 0 && m) atomicMax(amax_bits, m << 16);
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256)
+    tensor_cast_kernel(const uint16_t* __restrict__ x, int64_t n, const unsigned* amax_bits,
+                       float* scale_out, uint8_t* __restrict__ q) {
+    const float amax = __uint_as_float(*amax_bits);
+    const float fmax = FMT == FP8_E4M3 ? 448.0f : 57344.0f;
+    const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += stride) {
+        const uint4 v = x8[i];
+        uint2 o;
+        o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
+              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
+        o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
+              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
+        reinterpret_cast<uint2*>(q)[i] = o;
+    }
+    for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+         t += stride) {
+        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[t]) << 16), s);
+        q[t] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+    }
+}
+
+template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
+cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
+    const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
+    const int64_t nkc_row = col_tiles;                   // K tiles of the rowwise operand
+    const int64_t nkc_col = (a.rows + kTile - 1) / kTile;  // K tiles of the transposed one
+    if (row_tiles <= 0 || col_tiles <= 0) return cudaSuccess;
+    if (col_tiles > 65535 || row_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
+    quantize_mx_kernel<ROW, COL, FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, nkc_col);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s) {
+    const bool row = a.flags & MX_ROWWISE, col = a.flags & MX_COLWISE;
+    const bool fl = a.flags & MX_SCALE_FLOOR;
+    const int64_t row_tiles = (a.rows + kTile - 1) / kTile;
+    if (row && col) {
+        return fl ? launch_mx<true, true, true, false>(a, row_tiles, s)
+                  : launch_mx<true, true, false, false>(a, row_tiles, s);
+    }
+    if (row) {
+        return fl ? launch_mx<true, false, true, false>(a, row_tiles, s)
+                  : launch_mx<true, false, false, false>(a, row_tiles, s);
+    }
+    return fl ? launch_mx<false, true, true, false>(a, row_tiles, s)
+              : launch_mx<false, true, false, false>(a, row_tiles, s);
+}
+
+cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s) {
+    // sum_g ceil(m_g / 128) <= floor(total / 128) + groups
+    const int64_t row_tiles = a.rows / kTile + a.groups;
+    return (a.flags & MX_SCALE_FLOOR) ? launch_mx<true, false, true, true>(a, row_tiles, s)
+                                      : launch_mx<true, false, false, true>(a, row_tiles, s);
+}
+
+cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
+                                   float* scale, uint8_t* q, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    const int64_t chunks = n / 8 + 1;
+    const int64_t max_blocks = static_cast<int64_t>(sm_count_current_device()) * 8;
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((chunks + 255) / 256, max_blocks)));
+    unsigned* bits = reinterpret_cast<unsigned*>(amax);
+    if (n > 0) tensor_amax_kernel<<<blocks, 256, 0, s>>>(x, n, bits);
+    if (fmt == FP8_E5M2) {
+        tensor_cast_kernel<FP8_E5M2><<<blocks, 256, 0, s>>>(x, n, bits, scale, q);
+    } else {
+        tensor_cast_kernel<FP8_E4M3><<<blocks, 256, 0, s>>>(x, n, bits, scale, q);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t take_status_quant(unsigned* out) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_status_quant, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_status_quant, &zero, sizeof(unsigned));
+}
+
+}  // namespace mxfp8

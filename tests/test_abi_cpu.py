@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/mxfp8.h declares, and rejects
+bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mxfp8.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if not n.startswith("__")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_precision_gemms_gb300 import _build
+    _build.build()
+    import mxfp8_precision_gemms_gb300 as m
+    return m.lib()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for n in ("fp8_quantize_mx", "fp8_quantize_tensor", "fp8_scaled_gemm", "fp8_grouped_gemm",
+              "fp8_quantize_mx_grouped", "mxfp8_scale_bytes", "mxfp8_last_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_scale_bytes_matches_oracle(lib):
+    import oracle
+    for rows, k in ((1, 32), (128, 128), (129, 4096), (8192, 4096), (4096, 8192), (300, 96)):
+        assert lib.mxfp8_scale_bytes(rows, k) == oracle.scale_bytes(rows, k)
+    assert lib.mxfp8_scale_bytes(0, 128) == 0
+    assert lib.mxfp8_grouped_scale_bytes(1000, 256, 4) == (1000 // 128 + 1 + 4) * 2 * 512
+
+
+def test_host_validation(lib):
+    import mxfp8_precision_gemms_gb300 as m
+    P = 0x10000  # an aligned fake device address: never dereferenced on these paths
+    # null input
+    assert lib.fp8_quantize_mx(None, 64, 64, 64, m.MX_ROWWISE, P, P, None, None, None) == m.MXFP8_ERR_INVALID_ARG
+    # no orientation / unknown flags
+    assert lib.fp8_quantize_mx(P, 64, 64, 64, 0, P, P, None, None, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_mx(P, 64, 64, 64, 9, P, P, None, None, None) == m.MXFP8_ERR_INVALID_ARG
+    # cols % 32, colwise rows % 32
+    assert lib.fp8_quantize_mx(P, 64, 48, 48, m.MX_ROWWISE, P, P, None, None, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert lib.fp8_quantize_mx(P, 48, 64, 64, m.MX_COLWISE, None, None, P, P, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    # misaligned pointer / stride
+    assert lib.fp8_quantize_mx(P + 2, 64, 64, 64, m.MX_ROWWISE, P, P, None, None, None) == m.MXFP8_ERR_MISALIGNED
+    assert lib.fp8_quantize_mx(P, 64, 64, 68, m.MX_ROWWISE, P, P, None, None, None) == m.MXFP8_ERR_MISALIGNED
+    # empty input is a no-op
+    assert lib.fp8_quantize_mx(None, 0, 64, 64, m.MX_ROWWISE, None, None, None, None, None) == m.MXFP8_OK
+    # per-tensor
+    assert lib.fp8_quantize_tensor(P, 100, 7, P, P, P, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_tensor(P, 100, 0, None, P, P, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_tensor(P + 1, 100, 0, P, P, P, None) == m.MXFP8_ERR_MISALIGNED
+    # GEMM
+    G = lib.fp8_scaled_gemm
+    assert G(5, 0, 0, P, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
+    assert G(m.GEMM_MX, 1, 0, P, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert G(m.GEMM_MX, 0, 0, P, P, P, P, 128, 128, 48, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert G(m.GEMM_MX, 0, 0, P, P, P, P, 128, 132, 128, P, 136, None) == m.MXFP8_ERR_MISALIGNED
+    assert G(m.GEMM_MX, 0, 0, None, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
+    assert G(m.GEMM_MX, 0, 0, P, P, P, P, 128, 128, 128, P, 64, None) == m.MXFP8_ERR_INVALID_ARG
+    assert G(m.GEMM_MX, 0, 0, P + 16, P + 8, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_MISALIGNED
+    assert G(m.GEMM_MX, 0, 0, P, P, P, P, 0, 128, 128, P, 128, None) == m.MXFP8_OK
+    # grouped
+    GG = lib.fp8_grouped_gemm
+    assert GG(P, P, P, P, P, 0, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
+    assert GG(P, P, P, P, P, 2000, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert GG(P, P, P, P, None, 4, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
+    assert GG(P, P, P, P, P, 4, 128, 128, 96 + 16, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert lib.fp8_quantize_mx_grouped(P, 128, 64, 64, P, 4, m.MX_COLWISE, P, P, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_mx_grouped(P, 128, 64, 64, P, 0, 0, P, P, None) == m.MXFP8_ERR_INVALID_ARG
+    # every failure leaves a message; status strings exist
+    assert lib.mxfp8_last_error()
+    for s in range(7):
+        assert lib.mxfp8_status_string(s)
+
+
+def test_ops_fail_loudly_without_cuda_tensors(lib):
+    import torch
+    import mxfp8_precision_gemms_gb300 as m
+    x = torch.zeros(32, 32, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        m.fp8_quantize_mx(x)

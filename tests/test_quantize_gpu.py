@@ -1,0 +1,206 @@
+"""GPU parity of the quantizer kernels against the FP64 oracle: every payload
+byte and every scale byte (padding included) must match exactly."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_precision_gemms_gb300 as m
+import oracle
+import workloads
+from gpu_util import assert_ok, device, filled, host, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+ROW, COL, FLOOR = m.MX_ROWWISE, m.MX_COLWISE, m.MX_SCALE_FLOOR
+
+
+def random_bits(shape, dist, seed):
+    g = torch.Generator().manual_seed(seed)
+    if dist == "normal":
+        x = torch.randn(*shape, generator=g)
+    elif dist == "student":
+        return workloads.bits(workloads.student_t(shape, 4, seed, 0))
+    elif dist == "loguniform":
+        return workloads.bits(workloads.log_uniform_signed(shape, 1e-8, 1e-2, seed, 0))
+    elif dist == "wide":  # magnitudes over ~60 binades
+        x = torch.randn(*shape, generator=g) * torch.pow(2.0, torch.randint(-40, 20, shape, generator=g).float())
+    else:
+        raise ValueError(dist)
+    return workloads.bits(x.to(torch.bfloat16))
+
+
+def run_mx(bits, flags, ld=None):
+    rows, cols = bits.shape
+    if ld is not None and ld != cols:
+        wide = np.zeros((rows, ld), np.uint16)
+        wide[:, :cols] = bits
+        x = to_dev_bf16(wide)[:, :cols]
+    else:
+        x = to_dev_bf16(bits)
+    out = {}
+    if flags & ROW:
+        out["q_row"] = filled((rows, cols), 0xA5)
+        out["s_row"] = filled(m.mxfp8_scale_bytes(rows, cols), 0xA5)
+    if flags & COL:
+        out["q_col"] = filled((cols, rows), 0xA5)
+        out["s_col"] = filled(m.mxfp8_scale_bytes(cols, rows), 0xA5)
+    m.fp8_quantize_mx(x, flags, **out)
+    assert_ok()
+    return {k: host(v) for k, v in out.items()}
+
+
+SHAPES = [(32, 32), (128, 128), (160, 320), (96, 4096), (1056, 96), (4128, 160), (64, 8192)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("flags", [ROW, COL, ROW | COL, ROW | FLOOR, ROW | COL | FLOOR])
+def test_quantize_mx_matches_oracle(shape, flags):
+    bits = random_bits(shape, "student", seed=shape[0] * 7 + shape[1])
+    got = run_mx(bits, flags)
+    want = oracle.quantize_mx(bits, flags)
+    for k in want:
+        assert np.array_equal(got[k], want[k]), k
+
+
+@pytest.mark.parametrize("dist", ["normal", "loguniform", "wide"])
+def test_quantize_mx_distributions(dist):
+    bits = random_bits((256, 512), dist, seed=3)
+    got = run_mx(bits, ROW | COL)
+    want = oracle.quantize_mx(bits, ROW | COL)
+    for k in want:
+        assert np.array_equal(got[k], want[k]), k
+
+
+def test_quantize_mx_leading_dimension():
+    bits = random_bits((192, 256), "normal", seed=5)
+    got = run_mx(bits, ROW | COL, ld=264)
+    want = oracle.quantize_mx(bits, ROW | COL)
+    for k in want:
+        assert np.array_equal(got[k], want[k]), k
+
+
+def _anchor_blocks(floor):
+    """Blocks whose scale byte is fixed by an anchor value, filled with every
+    finite BF16 pattern at or below the anchor: all BF16 values x all scales."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_decode(allb)
+    fin = np.isfinite(vals)
+    b_fin, v_fin = allb[fin], np.abs(vals[fin])
+    order = np.argsort(v_fin, kind="stable")
+    b_sorted, v_sorted = b_fin[order], v_fin[order]
+    blocks, bytes_expected = [], []
+    top = 246 if floor else 247
+    for byte in range(0, top + 1, 1):
+        if floor:
+            anchor_bits = np.uint16(((byte + 8) << 7) | 0x7F)
+        else:
+            anchor_bits = np.uint16(((byte + 8) << 7) | 0x60) if byte < 247 else np.uint16(0x7F7F)
+        a = oracle.bf16_decode(np.array([anchor_bits]))[0]
+        cand = b_sorted[v_sorted <= a]
+        pad = (-cand.size) % 31
+        cand = np.concatenate([cand, np.zeros(pad, np.uint16)]).reshape(-1, 31)
+        anchors = np.full((cand.shape[0], 1), anchor_bits, np.uint16)
+        anchors[1::2] |= 0x8000
+        blocks.append(np.concatenate([anchors, cand], axis=1))
+        bytes_expected.append(np.full(cand.shape[0], byte))
+    blocks = np.concatenate(blocks)
+    nb = blocks.shape[0]
+    per_row = 128
+    rows = -(-nb // per_row)
+    full = np.zeros((rows * per_row, 32), np.uint16)
+    full[:nb] = blocks
+    return full.reshape(rows, per_row * 32), np.concatenate(bytes_expected), nb
+
+
+@pytest.mark.parametrize("floor", [False, True])
+def test_quantize_all_bf16_at_every_scale(floor):
+    bits, want_bytes, nb = _anchor_blocks(floor)
+    flags = ROW | (FLOOR if floor else 0)
+    got = run_mx(bits, flags)
+    want = oracle.quantize_mx(bits, flags)
+    # the construction really pins each block's scale
+    rows, cols = bits.shape
+    r = np.arange(nb) // (cols // 32)
+    j = np.arange(nb) % (cols // 32)
+    offs = (r // 128) * ((cols + 127) // 128) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4 \
+        + (j // 4) * 512
+    assert np.array_equal(want["s_row"][offs], want_bytes)
+    assert np.array_equal(got["s_row"], want["s_row"])
+    assert np.array_equal(got["q_row"], want["q_row"])
+
+
+def test_special_blocks():
+    x = np.zeros((32, 128), np.uint16)
+    x[0, 3] = 0x7FC0          # NaN -> whole block 0xFF / 0x7F
+    x[1, 40] = 0x7F80         # +Inf
+    x[2, 70] = 0xFF80         # -Inf
+    x[3, :] = 0x8000          # all -0
+    x[4, 0:32] = 0x0001       # smallest subnormal
+    x[5, 32] = 0x43FA         # 500 -> floor saturates, rceil does not
+    x[5, 33] = 0xB586         # a tiny negative value next to it
+    for flags in (ROW | COL, ROW | COL | FLOOR):
+        got = run_mx(x, flags)
+        want = oracle.quantize_mx(x, flags)
+        for k in want:
+            assert np.array_equal(got[k], want[k]), (flags, k)
+
+
+def test_quantize_grouped_matches_oracle():
+    counts = [0, 1, 127, 128, 129, 0, 300, 5, 0]
+    off = workloads.offsets_from_counts(counts)
+    bits = random_bits((int(off[-1]), 256), "student", seed=9)
+    x = to_dev_bf16(bits)
+    G = len(counts)
+    q = filled((int(off[-1]), 256), 0xA5)
+    s = filled(m.mxfp8_grouped_scale_bytes(int(off[-1]), 256, G), 0xA5)
+    m.fp8_quantize_mx_grouped(x, torch.from_numpy(off).to(device()), 0, q=q, s=s)
+    assert_ok()
+    wq, ws = oracle.quantize_mx_grouped(bits, off)
+    assert np.array_equal(host(q), wq)
+    assert np.array_equal(host(s)[: ws.size], ws)
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "last", "first"])
+def test_quantize_grouped_bad_offsets_recorded(bad):
+    off = np.array([0, 64, 128, 256], np.int32)
+    if bad == "decreasing":
+        off[2] = 32
+    elif bad == "last":
+        off[3] = 200
+    else:
+        off[0] = 4
+    bits = random_bits((256, 64), "normal", seed=1)
+    q = filled((256, 64), 0x5A)
+    s = filled(m.mxfp8_grouped_scale_bytes(256, 64, 3), 0x5A)
+    m.fp8_quantize_mx_grouped(to_dev_bf16(bits), torch.from_numpy(off).to(device()), 0, q=q, s=s)
+    assert m.mxfp8_last_device_status() == m.MXFP8_ERR_DEVICE_CHECK
+    assert m.mxfp8_last_device_status() == m.MXFP8_OK  # the word was cleared
+    assert (host(q) == 0x5A).all() and (host(s) == 0x5A).all()
+
+
+@pytest.mark.parametrize("fmt", [m.FP8_E4M3, m.FP8_E5M2])
+@pytest.mark.parametrize("case", ["outliers", "loguniform", "tiny", "zeros", "odd", "empty"])
+def test_quantize_tensor_matches_oracle(fmt, case):
+    if case == "outliers":
+        w = workloads.tensor4096(seed=1, device="cpu", m=512, n=8, k=1024)
+        bits = workloads.bits(w["X"])
+    elif case == "loguniform":
+        bits = random_bits((1024, 777 * 8 // 8), "loguniform", seed=2)
+    elif case == "tiny":
+        bits = workloads.bits((torch.randn(300, 40) * 1e-30).to(torch.bfloat16))
+    elif case == "zeros":
+        bits = np.zeros((64, 64), np.uint16)
+    elif case == "odd":
+        bits = random_bits((1000003,), "normal", seed=4)
+    else:
+        bits = np.zeros((0,), np.uint16)
+    x = to_dev_bf16(bits.reshape(-1))
+    q = filled(bits.size, 0xA5)
+    amax = filled(1, -1.0, torch.float32)
+    scale = filled(1, -1.0, torch.float32)
+    m.fp8_quantize_tensor(x, fmt, q=q, amax=amax, scale=scale)
+    assert_ok()
+    wa, ws, wq = oracle.quantize_tensor(bits.reshape(-1), fmt)
+    assert np.array_equal(host(q), wq.reshape(-1))
+    assert host(amax).view(np.uint32)[0] == np.float32(wa).view(np.uint32)
+    assert host(scale).view(np.uint32)[0] == np.float32(ws).view(np.uint32)
