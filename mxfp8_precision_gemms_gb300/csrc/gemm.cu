@@ -11,16 +11,27 @@
 //   grouped      the MX GEMM over ragged, row-sorted expert groups, expert g
 //                using its own weight ("Olmo-core MoE report", Section 11.4.1).
 //
-// Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles.
-//   warp 0       TMA producer: 128 x 128 A box + 256 x 128 B box (128-byte
-//                swizzle) and the 512-byte scale tiles per K step, into a
-//                4-stage shared-memory ring guarded by mbarriers.
-//   warp 1       TMEM allocator and MMA issuer: tcgen05.cp of the block scales
-//                into TMEM, 4 MMAs of K = 32 per stage, tcgen05.commit frees the
-//                stage and, after the last K step, hands the accumulator over.
-//   warps 2-9    epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator (each
-//                warp one 32-lane quarter x 128 columns), release TMEM, convert
-//                to BF16 and store, overlapping the next tile's main loop.
+// Structure: a persistent kernel, one CTA per SM.  In the default PAIR form
+// two CTAs of a cluster drive one 2-SM tensor-core operation (cta_group::2)
+// on a 256 x 256 output tile: each CTA holds 128 rows of A and 128 rows of B
+// per K step (32 KB instead of the 48 KB a single-SM 128 x 256 tile needs),
+// so the same shared memory keeps 6 stages in flight and each staged byte
+// feeds 1.5x the FLOPs.  The kernel is limited by how many bytes can be in
+// flight from L2, not by raw L2 bandwidth (multicasting B across CTAs did
+// not help), which is why the 2-SM form pays.
+//   warp 0       TMA producer (both CTAs): A box, this CTA's half of the B box
+//                (128-byte swizzle) and the 512-byte scale tiles per K step
+//                into a shared-memory ring; every load of both CTAs completes
+//                on the leader CTA's "full" mbarrier.
+//   warp 1       TMEM allocator (both CTAs, collectively) and, in the leader
+//                only, the MMA issuer: tcgen05.cp of the block scales into
+//                TMEM, 4 MMAs of K = 32 per stage, tcgen05.commit releasing the
+//                stage in both CTAs and, after the last K step, handing the
+//                accumulators over.
+//   warps 2-9    epilogue (both CTAs): tcgen05.ld of this CTA's 128 x 256 FP32
+//                accumulator, release it to the leader, convert to BF16 and
+//                store while the next tile's main loop runs.
+// The single-SM form (PAIR = false) is the same pipeline with one CTA.
 // Every wait is bounded; a wait that runs out records MXFP8_ERR_TIMEOUT,
 // the CTA drains its outstanding copies and MMAs, frees TMEM and exits.
 #include <algorithm>
@@ -40,43 +51,51 @@ __device__ unsigned int g_status_gemm = 0;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;  // rows of A / C per CTA
+constexpr int BN = 256;  // columns of C per tile
 constexpr int BK = 128;  // bytes = FP8 elements per K step (one 128-byte swizzle row)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
 constexpr int SFA_BYTES = 512;   // one 128-row x 4-block scale tile
-constexpr int SFB_BYTES = 1024;  // two of them (256 rows)
+constexpr int SFB_BYTES = 1024;  // two of them (the tile's 256 B rows)
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = BN;        // 128 lanes x 256 FP32 columns
+constexpr uint32_t ACC_COLS = BN;           // 128 lanes x 256 FP32 columns
 constexpr uint32_t SF_COLS_PER_STAGE = 12;  // A: 4 columns, B: 8 columns
 
-// Shared memory map (offsets from a 1024-byte aligned base).
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 4;  // full, empty, tmem_full, tmem_empty, drain, never
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t OFF_PREFIX = OFF_MISC + 32;
-constexpr uint32_t SMEM_PLAIN = OFF_PREFIX;
-constexpr uint32_t SMEM_GROUPED = OFF_PREFIX + 2 * (MAX_GROUPS + 1) * 4;
+#ifndef GEMM_PAIR
+#define GEMM_PAIR 1
+#endif
 
-static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024B alignment");
-static_assert(ACC_COLS + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+template <bool PAIR>
+struct Cfg {
+    static constexpr int CG = PAIR ? 2 : 1;  // CTAs per tensor-core operation
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int B_ROWS = BN / CG;   // B rows one CTA holds
+    static constexpr int B_BYTES = B_ROWS * BK;
+    // shared memory map (offsets from a 1024-byte aligned base)
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4;  // full, empty, tmem_full/empty, drain, never
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t OFF_PREFIX = OFF_MISC + 32;
+    static constexpr uint32_t SMEM_PLAIN = OFF_PREFIX;
+    static constexpr uint32_t SMEM_GROUPED = OFF_PREFIX + 3 * (MAX_GROUPS + 1) * 4;
+    static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024B alignment");
+    static_assert(ACC_COLS + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_GROUPED + 1024 <= 232448, "shared memory budget");
+};
 
 struct KParams {
     int64_t M, N, K;
     int32_t num_m_tiles, num_n_tiles, num_k_tiles;
+    int32_t num_m_groups;        // ceil(num_m_tiles / CG) (plain GEMM)
     int32_t n_scale_tiles;       // ceil(N / 128): 128-row scale tiles of one B
-    const uint8_t* sfa;
-    const uint8_t* sfb;
-    int64_t sfb_group_stride;    // bytes between experts' B scale arrays
+    int64_t sfb_group_chunks;    // 512-byte scale tiles between experts' B scales
     const float* s_a;            // GEMM_TENSOR scalars
     const float* s_b;
     uint16_t* c;
@@ -88,40 +107,47 @@ struct KParams {
     uint32_t idesc_tensor;
 };
 
+// One CTA's share of a work unit: the unit covers CG consecutive 128-row
+// tiles of A (one per CTA of the pair) and one 256-column tile of B.
 struct Tile {
-    int64_t a_row;     // first row of A (and of C)
+    int64_t a_row;     // first row of A (and of C) of this CTA
     int64_t row_end;   // rows of C valid below this
     int64_t sfa_tile;  // 128-row tile index in A's scale array
-    int64_t b_row;     // first row of B (grouped: of the experts' stack)
+    int64_t b_row;     // first row of the B tile (grouped: of the experts' stack)
     int32_t n_tile;
     int32_t group;
+    bool a_valid;      // false: a padding tile (nothing to store)
 };
 
 __device__ __forceinline__ void record_status(unsigned code) {
     atomicCAS(&g_status_gemm, 0u, code);
 }
 
-template <bool GROUPED>
-__device__ __forceinline__ Tile decode_tile(const KParams& p, int64_t t, const int32_t* prefix,
-                                            const int32_t* offs) {
+template <bool GROUPED, int CG>
+__device__ __forceinline__ Tile decode_unit(const KParams& p, int64_t u, uint32_t rank,
+                                            const int32_t* mtile_prefix,
+                                            const int32_t* mgroup_prefix, const int32_t* offs) {
     Tile tl;
     if constexpr (GROUPED) {
-        const int64_t gm = t / p.num_n_tiles;
-        tl.n_tile = static_cast<int32_t>(t % p.num_n_tiles);
-        int lo = 0, hi = p.groups - 1;  // largest g with prefix[g] <= gm
+        const int64_t gmg = u / p.num_n_tiles;
+        tl.n_tile = static_cast<int32_t>(u % p.num_n_tiles);
+        int lo = 0, hi = p.groups - 1;  // largest g with mgroup_prefix[g] <= gmg
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= gm) lo = mid; else hi = mid - 1;
+            if (mgroup_prefix[mid] <= gmg) lo = mid; else hi = mid - 1;
         }
+        const int64_t mt = (gmg - mgroup_prefix[lo]) * CG + rank;
         tl.group = lo;
-        tl.a_row = offs[lo] + (gm - prefix[lo]) * BM;
+        tl.a_valid = mt < mtile_prefix[lo + 1] - mtile_prefix[lo];
+        tl.a_row = offs[lo] + mt * BM;
         tl.row_end = min(static_cast<int64_t>(offs[lo + 1]), tl.a_row + BM);
-        tl.sfa_tile = gm;
+        tl.sfa_tile = mtile_prefix[lo] + mt;
         tl.b_row = static_cast<int64_t>(lo) * p.N + static_cast<int64_t>(tl.n_tile) * BN;
     } else {
-        const int64_t mt = t % p.num_m_tiles;
-        tl.n_tile = static_cast<int32_t>(t / p.num_m_tiles);
+        const int64_t mt = (u % p.num_m_groups) * CG + rank;
+        tl.n_tile = static_cast<int32_t>(u / p.num_m_groups);
         tl.group = 0;
+        tl.a_valid = mt < p.num_m_tiles;
         tl.a_row = mt * BM;
         tl.row_end = min(p.M, tl.a_row + BM);
         tl.sfa_tile = mt;
@@ -135,26 +161,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <bool MX, bool GROUPED>
+// tm_a / tm_b: payload boxes (128 x 128 and B_ROWS x 128 bytes, 128-byte
+// swizzle).  tm_sa / tm_sb: the scale arrays seen as rows of 256 bytes,
+// boxes of 2 rows = one 512-byte scale tile (out-of-range tiles read as 0).
+template <bool MX, bool GROUPED, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
                 const KParams p) {
+    using C = Cfg<PAIR>;
+    constexpr int CG = C::CG;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int64_t pair_id = blockIdx.x / CG;
+    const int64_t num_pairs = gridDim.x / CG;
 
-    auto bar = [&](uint32_t i) { return sbase + OFF_BAR + 8 * i; };
+    auto bar = [&](uint32_t i) { return sbase + C::OFF_BAR + 8 * i; };
     const uint32_t BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_TMEM_FULL = 2 * STAGES,
                    BAR_TMEM_EMPTY = 2 * STAGES + 1, BAR_DRAIN = 2 * STAGES + 2,
                    BAR_NEVER = 2 * STAGES + 3;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-    int32_t* prefix = reinterpret_cast<int32_t*>(smem + OFF_PREFIX);
-    int32_t* offs = prefix + (MAX_GROUPS + 1);
-    __shared__ int64_t s_total_tiles;
+    int32_t* mtile_prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
+    int32_t* mgroup_prefix = mtile_prefix + (MAX_GROUPS + 1);
+    int32_t* offs = mgroup_prefix + (MAX_GROUPS + 1);
+    __shared__ int64_t s_total_units;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < STAGES; ++s) {
@@ -162,18 +200,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(BAR_EMPTY + s), 1);
         }
         mbar_init(bar(BAR_TMEM_FULL), 1);
-        mbar_init(bar(BAR_TMEM_EMPTY), EPI_WARPS);
+        mbar_init(bar(BAR_TMEM_EMPTY), EPI_WARPS * CG);  // both CTAs' epilogues
         mbar_init(bar(BAR_DRAIN), 1);
         mbar_init(bar(BAR_NEVER), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if constexpr (GROUPED) {
-        // Validate the offsets and build the prefix of 128-row tiles per group.
+        // Validate the offsets; prefix sums of 128-row tiles and of units of
+        // CG tiles per expert group.
         if (warp == 0) {
             const int G = p.groups;
             bool ok = (p.offsets[0] == 0) && (static_cast<int64_t>(p.offsets[G]) == p.M);
-            int32_t base = 0;
+            int32_t tbase = 0, gbase = 0;
             for (int g0 = 0; g0 <= G; g0 += 32) {
                 const int g = g0 + lane;
                 int32_t tiles = 0;
@@ -183,34 +222,44 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (m < 0) ok = false;
                     tiles = m > 0 ? (m + BM - 1) / BM : 0;
                 }
-                int32_t incl = tiles;
+                const int32_t mgs = (tiles + CG - 1) / CG;
+                int32_t ti = tiles, gi = mgs;
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
-                    const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += v;
+                    const int32_t v = __shfl_up_sync(0xffffffffu, ti, d);
+                    const int32_t w = __shfl_up_sync(0xffffffffu, gi, d);
+                    if (lane >= d) {
+                        ti += v;
+                        gi += w;
+                    }
                 }
-                if (g <= G) prefix[g] = base + incl - tiles;
-                base += __shfl_sync(0xffffffffu, incl, 31);
+                if (g <= G) {
+                    mtile_prefix[g] = tbase + ti - tiles;
+                    mgroup_prefix[g] = gbase + gi - mgs;
+                }
+                tbase += __shfl_sync(0xffffffffu, ti, 31);
+                gbase += __shfl_sync(0xffffffffu, gi, 31);
             }
             ok = __all_sync(0xffffffffu, ok);
             if (lane == 0) {
-                s_total_tiles = ok ? static_cast<int64_t>(base) * p.num_n_tiles : 0;
+                s_total_units = ok ? static_cast<int64_t>(gbase) * p.num_n_tiles : 0;
                 if (!ok && blockIdx.x == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
             }
         }
     } else {
         if (threadIdx.x == 0)
-            s_total_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+            s_total_units = static_cast<int64_t>(p.num_m_groups) * p.num_n_tiles;
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(misc), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(misc), TMEM_COLS);  // with CG = 2: both CTAs, same columns
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int64_t total = s_total_tiles;
+    const int64_t total = s_total_units;
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -222,36 +271,51 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_b);
+            if constexpr (MX) {
+                tma_prefetch_desc(&tm_sa);
+                tma_prefetch_desc(&tm_sb);
+            }
             uint32_t stage = 0, phase = 0;
-            uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks
+            uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks (leader's drain)
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<GROUPED>(p, t, prefix, offs);
-                const uint8_t* sfb_g = p.sfb + static_cast<int64_t>(tl.group) * p.sfb_group_stride;
-                const bool two_sfb = (2 * tl.n_tile + 1) < p.n_scale_tiles;
+            constexpr uint32_t kStageTx =
+                CG * (A_BYTES + C::B_BYTES + (MX ? SFA_BYTES + SFB_BYTES : 0));
+            for (int64_t u = pair_id; u < total && ok; u += num_pairs) {
+                const Tile tl = decode_unit<GROUPED, CG>(p, u, rank, mtile_prefix, mgroup_prefix, offs);
+                const int64_t sfb_base = static_cast<int64_t>(tl.group) * p.sfb_group_chunks +
+                                         2 * static_cast<int64_t>(tl.n_tile) * p.num_k_tiles;
+                const int32_t b_row = static_cast<int32_t>(tl.b_row + rank * C::B_ROWS);
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar(BAR_FULL + stage);
-                    uint32_t bytes = A_BYTES + B_BYTES;
-                    if constexpr (MX) bytes += SFA_BYTES + (two_sfb ? 1024u : 512u);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tm_a, fb, kt * BK,
-                                static_cast<int32_t>(tl.a_row));
-                    tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, fb, kt * BK,
-                                static_cast<int32_t>(tl.b_row));
-                    if constexpr (MX) {
-                        bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
-                                  p.sfa + (tl.sfa_tile * p.num_k_tiles + kt) * 512, 512, fb);
-                        const int64_t nb = 2 * static_cast<int64_t>(tl.n_tile);
-                        bulk_load(sbase + OFF_SFB + stage * SFB_BYTES,
-                                  sfb_g + (nb * p.num_k_tiles + kt) * 512, 512, fb);
-                        if (two_sfb) {
-                            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + 512,
-                                      sfb_g + ((nb + 1) * p.num_k_tiles + kt) * 512, 512, fb);
+                    const uint32_t fb_local = bar(BAR_FULL + stage);
+                    if (leader) mbar_arrive_expect_tx(fb_local, kStageTx);
+                    const uint32_t dA = sbase + C::OFF_A + stage * A_BYTES;
+                    const uint32_t dB = sbase + C::OFF_B + stage * C::B_BYTES;
+                    const uint32_t dSA = sbase + C::OFF_SFA + stage * SFA_BYTES;
+                    const uint32_t dSB = sbase + C::OFF_SFB + stage * SFB_BYTES;
+                    const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt));
+                    const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt));
+                    const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
+                    if constexpr (PAIR) {
+                        const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
+                        tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
+                        tma_load_2d_pair(dB, &tm_b, fb, kt * BK, b_row);
+                        if constexpr (MX) {
+                            tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
+                            tma_load_2d_pair(dSB, &tm_sb, fb, 0, yb0);
+                            tma_load_2d_pair(dSB + 512, &tm_sb, fb, 0, yb1);
+                        }
+                    } else {
+                        tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
+                        tma_load_2d(dB, &tm_b, fb_local, kt * BK, b_row);
+                        if constexpr (MX) {
+                            tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
+                            tma_load_2d(dSB, &tm_sb, fb_local, 0, yb0);
+                            tma_load_2d(dSB + 512, &tm_sb, fb_local, 0, yb1);
                         }
                     }
                     issued |= 1u << stage;
@@ -262,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // let every copy already in flight land before the CTA exits
                 const int never = 0;
                 for (uint32_t s = 0; s < STAGES; ++s) {
@@ -273,8 +337,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (leader)
+        if (lane == 0 && leader) {
             const int never = 0;
             bool ok = true;
             if (p.inject_timeout) {
@@ -284,9 +348,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                 }
             }
+            constexpr uint16_t kPairMask = PAIR ? 3 : 1;
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             const uint64_t sf_desc_base = smem_desc(0, 0, 128, SWZ_NONE);
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int64_t u = pair_id; u < total && ok; u += num_pairs) {
                 if (!mbar_wait(bar(BAR_TMEM_EMPTY), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                     fail();
                     break;
@@ -299,50 +364,54 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t da = smem_desc(sbase + OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
-                    const uint64_t db = smem_desc(sbase + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
+                    const uint64_t da = smem_desc(sbase + C::OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
+                    const uint64_t db = smem_desc(sbase + C::OFF_B + stage * C::B_BYTES, 16, 1024, SWZ_128B);
                     if constexpr (MX) {
                         const uint32_t sfa_t = tmem + ACC_COLS + stage * SF_COLS_PER_STAGE;
                         const uint32_t sfb_t = sfa_t + 4;
-                        const uint32_t sa = sbase + OFF_SFA + stage * SFA_BYTES;
-                        const uint32_t sb = sbase + OFF_SFB + stage * SFB_BYTES;
-                        tc_cp_32x128b_warpx4(sfa_t, sf_desc_base | ((sa & 0x3FFFFu) >> 4));
-                        tc_cp_32x128b_warpx4(sfb_t, sf_desc_base | ((sb & 0x3FFFFu) >> 4));
-                        tc_cp_32x128b_warpx4(sfb_t + 4, sf_desc_base | (((sb + 512) & 0x3FFFFu) >> 4));
+                        const uint32_t sa = sbase + C::OFF_SFA + stage * SFA_BYTES;
+                        const uint32_t sb = sbase + C::OFF_SFB + stage * SFB_BYTES;
+                        tc_cp_32x128b_warpx4<CG>(sfa_t, sf_desc_base | ((sa & 0x3FFFFu) >> 4));
+                        tc_cp_32x128b_warpx4<CG>(sfb_t, sf_desc_base | ((sb & 0x3FFFFu) >> 4));
+                        tc_cp_32x128b_warpx4<CG>(sfb_t + 4, sf_desc_base | (((sb + 512) & 0x3FFFFu) >> 4));
 #pragma unroll
                         for (uint32_t kk = 0; kk < BK / 32; ++kk) {
-                            mma_mxf8(tmem, da + 2 * kk, db + 2 * kk, idesc_mxf8(BM, BN, kk), sfa_t,
-                                     sfb_t, (kt | kk) != 0);
+                            mma_mxf8<CG>(tmem, da + 2 * kk, db + 2 * kk, idesc_mxf8(BM * CG, BN, kk),
+                                         sfa_t, sfb_t, (kt | kk) != 0);
                         }
                     } else {
 #pragma unroll
                         for (uint32_t kk = 0; kk < BK / 32; ++kk) {
-                            mma_f8(tmem, da + 2 * kk, db + 2 * kk, p.idesc_tensor, (kt | kk) != 0);
+                            mma_f8<CG>(tmem, da + 2 * kk, db + 2 * kk, p.idesc_tensor, (kt | kk) != 0);
                         }
                     }
-                    tc_commit(bar(BAR_EMPTY + stage));
+                    // the stage is free in both CTAs once these MMAs completed
+                    if constexpr (PAIR) tc_commit_multicast<CG>(bar(BAR_EMPTY + stage), kPairMask);
+                    else tc_commit<CG>(bar(BAR_EMPTY + stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar(BAR_TMEM_FULL));
+                if constexpr (PAIR) tc_commit_multicast<CG>(bar(BAR_TMEM_FULL), kPairMask);
+                else tc_commit<CG>(bar(BAR_TMEM_FULL));
                 acc_phase ^= 1u;
             }
             // every MMA / copy this thread issued completes before teardown
-            tc_commit(bar(BAR_DRAIN));
+            tc_commit<CG>(bar(BAR_DRAIN));
             mbar_wait(bar(BAR_DRAIN), 0, p.wait_limit_ns, &never);
         }
     } else {
         // ------------------------------------------------ epilogue
         const int quarter = warp & 3;        // TMEM lanes this warp may read
         const int half = (warp - 2) >> 2;    // which 128 accumulator columns
+        const uint32_t empty_bar = PAIR ? mapa_shared(bar(BAR_TMEM_EMPTY), 0) : bar(BAR_TMEM_EMPTY);
         float alpha = 1.0f;
         if constexpr (!MX) alpha = __fdiv_rn(1.0f, *p.s_a) * __fdiv_rn(1.0f, *p.s_b);
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile tl = decode_tile<GROUPED>(p, t, prefix, offs);
+        for (int64_t u = pair_id; u < total; u += num_pairs) {
+            const Tile tl = decode_unit<GROUPED, CG>(p, u, rank, mtile_prefix, mgroup_prefix, offs);
             if (!mbar_wait(bar(BAR_TMEM_FULL), acc_phase, p.wait_limit_ns, abort_flag)) {
                 fail();
                 break;
@@ -357,9 +426,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_TMEM_EMPTY));
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(empty_bar);
+                else mbar_arrive(empty_bar);
+            }
             const int64_t row = tl.a_row + quarter * 32 + lane;
-            if (row < tl.row_end) {
+            if (tl.a_valid && row < tl.row_end) {
                 uint16_t* crow = p.c + row * p.ldc;
                 const int64_t col0 = static_cast<int64_t>(tl.n_tile) * BN + half * 128;
 #pragma unroll
@@ -385,10 +457,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // the leader's MMAs (which also write the peer's TMEM) have drained and
+    // both epilogues are done before either CTA frees its TMEM
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc<CG>(tmem, TMEM_COLS);
     }
+    if constexpr (PAIR) cluster_sync();
 }
 
 __global__ void zero_fill_kernel(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc) {
@@ -416,42 +492,65 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// 2D tensor map over a rows x k byte matrix (row stride k), box_rows x 128.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, uint32_t box_rows) {
+// 2D tensor map over a rows x width byte matrix (row stride width).
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t width, uint32_t box_w,
+              uint32_t box_rows, CUtensorMapSwizzle swz) {
     auto enc = get_encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(width)};
+    const cuuint32_t box[2] = {box_w, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <bool MX, bool GROUPED>
-cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& p,
-                          int grid, cudaStream_t s) {
-    const uint32_t smem = (GROUPED ? SMEM_GROUPED : SMEM_PLAIN) + 1024;
-    auto k = gemm_kernel<MX, GROUPED>;
+template <bool MX, bool GROUPED, bool PAIR>
+cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                          const CUtensorMap& tsb, const KParams& p, int64_t units, cudaStream_t s) {
+    using C = Cfg<PAIR>;
+    const uint32_t smem = (GROUPED ? C::SMEM_GROUPED : C::SMEM_PLAIN) + 1024;
+    auto k = gemm_kernel<MX, GROUPED, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k<<<grid, THREADS, smem, s>>>(ta, tb, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent grid: as many pairs (or CTAs) as can be resident at once
+    int max_clusters = 0;
+    cfg.gridDim = dim3(C::CG * 64, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
+    if (e != cudaSuccess || max_clusters <= 0) {
+        (void)cudaGetLastError();
+        max_clusters = sm_count_current_device() / C::CG;
+    }
+    const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, max_clusters));
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::CG), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, k, ta, tb, tsa, tsb, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
+
+constexpr bool kPair = GEMM_PAIR != 0;
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+    using C = Cfg<kPair>;
     const bool grouped = g.groups > 0;
     const bool mx = g.mode == GEMM_MX;
     const int64_t b_rows = grouped ? static_cast<int64_t>(g.groups) * g.N : g.N;
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, g.a, g.M, g.K, BM) || !make_map(&tb, g.b, b_rows, g.K, BN))
-        return cudaErrorInvalidValue;
     KParams p{};
     p.M = g.M;
     p.N = g.N;
@@ -459,15 +558,28 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     p.num_m_tiles = static_cast<int32_t>((g.M + BM - 1) / BM);
     p.num_n_tiles = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.num_k_tiles = static_cast<int32_t>((g.K + BK - 1) / BK);
+    p.num_m_groups = (p.num_m_tiles + C::CG - 1) / C::CG;
     p.n_scale_tiles = static_cast<int32_t>((g.N + 127) / 128);
+    p.sfb_group_chunks = static_cast<int64_t>(p.n_scale_tiles) * p.num_k_tiles;
+    CUtensorMap ta, tb, tsa, tsb;
+    if (!make_map(&ta, g.a, g.M, g.K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tb, g.b, b_rows, g.K, BK, C::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     if (mx) {
-        p.sfa = static_cast<const uint8_t*>(g.a_scale);
-        p.sfb = static_cast<const uint8_t*>(g.b_scale);
-        p.sfb_group_stride = static_cast<int64_t>(p.n_scale_tiles) * p.num_k_tiles * 512;
+        // scale arrays as 256-byte rows; a 512-byte scale tile is a 2-row box
+        const int64_t a_tiles = grouped ? (g.M + 127) / 128 + g.groups : p.num_m_tiles;
+        const int64_t a_chunks = a_tiles * p.num_k_tiles;
+        const int64_t b_chunks = (grouped ? g.groups : 1) * p.sfb_group_chunks;
+        if (!make_map(&tsa, g.a_scale, 2 * a_chunks, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map(&tsb, g.b_scale, 2 * b_chunks, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
     } else {
+        tsa = ta;  // unused
+        tsb = tb;
         p.s_a = static_cast<const float*>(g.a_scale);
         p.s_b = static_cast<const float*>(g.b_scale);
-        p.idesc_tensor = idesc_f8(BM, BN, static_cast<uint32_t>(g.a_fmt), static_cast<uint32_t>(g.b_fmt));
+        p.idesc_tensor = idesc_f8(BM * C::CG, BN, static_cast<uint32_t>(g.a_fmt),
+                                  static_cast<uint32_t>(g.b_fmt));
     }
     p.c = g.c;
     p.ldc = g.ldc;
@@ -475,19 +587,15 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     p.groups = g.groups;
     p.wait_limit_ns = wait_limit_ns();
     p.inject_timeout = take_inject_timeout() ? 1 : 0;
-    const int sms = sm_count_current_device();
-    int grid;
-    if (grouped) {
-        grid = sms;
-    } else {
-        const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-        grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-    }
+    // grouped: the unit count depends on device offsets; this bound only caps the grid
+    const int64_t units = grouped
+        ? (static_cast<int64_t>(p.num_m_tiles) / C::CG + g.groups + 1) * p.num_n_tiles
+        : static_cast<int64_t>(p.num_m_groups) * p.num_n_tiles;
     if (mx) {
-        return grouped ? launch_kernel<true, true>(ta, tb, p, grid, s)
-                       : launch_kernel<true, false>(ta, tb, p, grid, s);
+        return grouped ? launch_kernel<true, true, kPair>(ta, tb, tsa, tsb, p, units, s)
+                       : launch_kernel<true, false, kPair>(ta, tb, tsa, tsb, p, units, s);
     }
-    return launch_kernel<false, false>(ta, tb, p, grid, s);
+    return launch_kernel<false, false, kPair>(ta, tb, tsa, tsb, p, units, s);
 }
 
 cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc,

@@ -63,6 +63,7 @@ def _load():
                 "orc_gemm_tensor_rows": (None, [P, I, ctypes.c_float, P, I, ctypes.c_float,
                                                 I64, I64, I64, P, I64, P]),
                 "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, P]),
+                "orc_num_threads": (I, []),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -117,6 +118,11 @@ def e8m0_scale_byte(amax, floor: bool = False) -> np.ndarray:
     out = np.empty(a.shape, np.int32)
     _load().orc_e8m0_array(_p(a), a.size, 1 if floor else 0, _p(out))
     return out
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().orc_num_threads())
 
 
 def scale_bytes(rows: int, k: int) -> int:

@@ -477,3 +477,11 @@ void orc_e8m0_array(const double* amax, int64_t n, int floor_rule, int32_t* out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = floor_rule ? orc_e8m0_floor(amax[i]) : orc_e8m0_rceil(amax[i]);
 }
+
+/* Threads the OpenMP loops above use (1 without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+int orc_num_threads(void) { return omp_get_max_threads(); }
+#else
+int orc_num_threads(void) { return 1; }
+#endif
