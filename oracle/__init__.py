@@ -62,7 +62,7 @@ def _load():
                 "orc_gemm_mx_rows": (None, [P, P, P, P, I64, I64, I64, P, I64, P]),
                 "orc_gemm_tensor_rows": (None, [P, I, ctypes.c_float, P, I, ctypes.c_float,
                                                 I64, I64, I64, P, I64, P]),
-                "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, P]),
+                "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, I64, P]),
                 "orc_num_threads": (I, []),
             }
             for name, (res, args) in sig.items():
@@ -219,18 +219,20 @@ def gemm_tensor(qa, fa, s_a, qb, fb, s_b, rows=None) -> np.ndarray:
     return out
 
 
-def gemm_grouped(qa, sa, qw, sw, offsets, want=None) -> np.ndarray:
-    """FP64 grouped GEMM; returns total_rows x N (rows not in ``want`` are 0)."""
+def gemm_grouped(qa, sa, qw, sw, offsets, rows=None) -> np.ndarray:
+    """FP64 grouped GEMM: C rows listed in ``rows`` (ascending global row
+    indices), or all total_rows x N when rows is None."""
     qa = np.ascontiguousarray(qa, np.uint8); sa = np.ascontiguousarray(sa, np.uint8)
     qw = np.ascontiguousarray(qw, np.uint8); sw = np.ascontiguousarray(sw, np.uint8)
     off = np.ascontiguousarray(offsets, dtype=np.int32)
     G, N, K = qw.shape
     total = int(off[-1])
-    out = np.zeros((total, N), np.float64)
-    w = None
-    if want is not None:
-        w = np.zeros(total, np.uint8)
-        w[np.asarray(want, dtype=np.int64)] = 1
+    r = None
+    if rows is not None:
+        r = np.ascontiguousarray(np.sort(np.asarray(rows, dtype=np.int64)))
+        assert r.size == 0 or (r[0] >= 0 and r[-1] < total)
+    nr = total if r is None else r.size
+    out = np.zeros((nr, N), np.float64)
     _load().orc_gemm_grouped_rows(_p(qa), _p(sa), _p(qw), _p(sw), _p(off), G, N, K,
-                                  None if w is None else _p(w), _p(out))
+                                  None if r is None else _p(r), nr, _p(out))
     return out

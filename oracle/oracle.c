@@ -417,38 +417,51 @@ void orc_gemm_tensor_rows(const uint8_t* qa, int fa, float s_a, const uint8_t* q
 /* Grouped MX GEMM: for each group g, C[off[g]:off[g+1]] = A_g W_g^T, where
  * A's scales use the grouped padded layout of orc_quantize_mx_grouped and
  * expert g's weight is the N x K matrix at qw + g*N*K with its own swizzled
- * scale array at sw + g * orc_scale_bytes(N, K).  Only output rows flagged in
- * want (length off[groups]; NULL = all rows) are computed; out has one row of
- * N values per global row (rows not wanted are left untouched). */
+ * scale array at sw + g * orc_scale_bytes(N, K).  Computes the output rows
+ * listed in rows (global row indices, ascending); out row i is C[rows[i]].
+ * rows == NULL means all rows in order (nrows = off[groups]). */
 void orc_gemm_grouped_rows(const uint8_t* qa, const uint8_t* sa, const uint8_t* qw,
                            const uint8_t* sw, const int32_t* off, int32_t groups,
-                           int64_t N, int64_t K, const uint8_t* want, double* out) {
+                           int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                           double* out) {
     int64_t wsb = orc_scale_bytes(N, K);
     int64_t padded = 0;
+    int64_t next = 0; /* first entry of rows not yet computed */
     double* bd = (double*)malloc(sizeof(double) * (size_t)(N * K));
     for (int32_t g = 0; g < groups; ++g) {
         int64_t m = (int64_t)off[g + 1] - off[g];
-        const uint8_t* qg = qw + (int64_t)g * N * K;
-        const uint8_t* sg = sw + (int64_t)g * wsb;
+        /* the wanted rows of this group: entries [first, last) of rows */
+        int64_t first = next, last = next;
+        if (rows) {
+            while (last < nrows && rows[last] < off[g + 1]) ++last;
+        } else {
+            first = off[g];
+            last = off[g + 1];
+        }
+        next = last;
+        if (last > first) {
+            const uint8_t* qg = qw + (int64_t)g * N * K;
+            const uint8_t* sg = sw + (int64_t)g * wsb;
 #pragma omp parallel for schedule(static)
-        for (int64_t n = 0; n < N; ++n) deq_row(qg, sg, n, K, 0, bd + n * K);
+            for (int64_t n = 0; n < N; ++n) deq_row(qg, sg, n, K, 0, bd + n * K);
 #pragma omp parallel for schedule(static)
-        for (int64_t i = 0; i < m; ++i) {
-            int64_t r = off[g] + i;
-            if (want && !want[r]) continue;
-            double* ad = (double*)malloc(sizeof(double) * (size_t)K);
-            /* A row r is row i of group g, at padded scale row padded + i */
-            for (int64_t k = 0; k < K; ++k) {
-                uint8_t s = sa[orc_swizzle_offset(padded + i, k / 32, K)];
-                ad[k] = orc_e4m3_decode(qa[r * K + k]) * orc_e8m0_decode(s);
+            for (int64_t i = first; i < last; ++i) {
+                int64_t r = rows ? rows[i] : i;
+                int64_t local = r - off[g];
+                double* ad = (double*)malloc(sizeof(double) * (size_t)K);
+                /* A row r is row `local` of group g, at padded scale row padded + local */
+                for (int64_t k = 0; k < K; ++k) {
+                    uint8_t s = sa[orc_swizzle_offset(padded + local, k / 32, K)];
+                    ad[k] = orc_e4m3_decode(qa[r * K + k]) * orc_e8m0_decode(s);
+                }
+                for (int64_t n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    const double* b = bd + n * K;
+                    for (int64_t k = 0; k < K; ++k) acc += ad[k] * b[k];
+                    out[i * N + n] = acc;
+                }
+                free(ad);
             }
-            for (int64_t n = 0; n < N; ++n) {
-                double acc = 0.0;
-                const double* b = bd + n * K;
-                for (int64_t k = 0; k < K; ++k) acc += ad[k] * b[k];
-                out[r * N + n] = acc;
-            }
-            free(ad);
         }
         padded += (m + 127) / 128 * 128;
     }
