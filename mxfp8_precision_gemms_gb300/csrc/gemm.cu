@@ -35,6 +35,7 @@
 // Every wait is bounded; a wait that runs out records MXFP8_ERR_TIMEOUT,
 // the CTA drains its outstanding copies and MMAs, frees TMEM and exits.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -507,15 +508,22 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t width, uin
     return r == CUDA_SUCCESS;
 }
 
+// Per device: the dynamic shared memory attribute is set once and the number
+// of co-resident clusters is queried once (both are host-side driver calls
+// too slow to repeat on every launch).
+constexpr int kMaxDevices = 64;
+
 template <bool MX, bool GROUPED, bool PAIR>
 cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const KParams& p, int64_t units, cudaStream_t s) {
     using C = Cfg<PAIR>;
+    static std::atomic<int> resident[kMaxDevices];  // 0 = not yet queried
     const uint32_t smem = (GROUPED ? C::SMEM_GROUPED : C::SMEM_PLAIN) + 1024;
     auto k = gemm_kernel<MX, GROUPED, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -527,13 +535,19 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // persistent grid: as many pairs (or CTAs) as can be resident at once
-    int max_clusters = 0;
-    cfg.gridDim = dim3(C::CG * 64, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
-    if (e != cudaSuccess || max_clusters <= 0) {
-        (void)cudaGetLastError();
-        max_clusters = sm_count_current_device() / C::CG;
+    int max_clusters = resident[dev].load(std::memory_order_relaxed);
+    if (max_clusters <= 0) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        // persistent grid: as many pairs (or CTAs) as can be resident at once
+        cfg.gridDim = dim3(C::CG * 64, 1, 1);
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
+        if (e != cudaSuccess || max_clusters <= 0) {
+            (void)cudaGetLastError();
+            max_clusters = sm_count_current_device() / C::CG;
+        }
+        resident[dev].store(max_clusters, std::memory_order_relaxed);
     }
     const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, max_clusters));
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::CG), 1, 1);
