@@ -6,7 +6,11 @@
 #include <cstdio>
 #include <cstring>
 
+#include <mutex>
+
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "internal.h"
 
@@ -57,6 +61,40 @@ int sm_count_current_device() {
         g_sm_count[dev].store(n);
     }
     return n;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        }
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                          int64_t rows, int64_t width, int64_t row_stride_bytes, uint32_t box_w,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_bytes)};
+    const cuuint32_t box[2] = {box_w, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace mxfp8
@@ -117,8 +155,8 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
     if (total_rows < 0 || cols < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
     if (total_rows > 0x7FFFFFFF) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "total_rows >= 2^31");
     if (!group_offsets_dev) return fail(MXFP8_ERR_INVALID_ARG, "group_offsets is NULL");
-    if (cols == 0) return ok();
-    if (!x_bf16 && total_rows > 0) return fail(MXFP8_ERR_INVALID_ARG, "x is NULL");
+    if (cols == 0 || total_rows == 0) return ok();
+    if (!x_bf16) return fail(MXFP8_ERR_INVALID_ARG, "x is NULL");
     if (!q || !s) return fail(MXFP8_ERR_INVALID_ARG, "output is NULL");
     if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0");
     if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");

@@ -41,7 +41,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -448,7 +447,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                                           __uint_as_float(v[8 * j + 5]) * alpha);
                         o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * alpha,
                                           __uint_as_float(v[8 * j + 7]) * alpha);
-                        *reinterpret_cast<uint4*>(crow + col) = o;
+                        // evict-first: C streams out to HBM while the GEMM
+                        // runs instead of lingering in L2 as dirty lines
+                        __stcs(reinterpret_cast<uint4*>(crow + col), o);
                     }
                 }
             }
@@ -478,34 +479,11 @@ __global__ void zero_fill_kernel(uint16_t* c, int64_t rows, int64_t cols, int64_
 
 // ------------------------------------------------------------ host side --
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess) {
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        }
-    });
-    return fn;
-}
-
 // 2D tensor map over a rows x width byte matrix (row stride width).
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t width, uint32_t box_w,
               uint32_t box_rows, CUtensorMapSwizzle swz) {
-    auto enc = get_encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(width)};
-    const cuuint32_t box[2] = {box_w, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_tensor_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rows, width, width, box_w,
+                                box_rows, swz);
 }
 
 // Per device: the dynamic shared memory attribute is set once and the number

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mxfp8.h"
@@ -56,5 +57,12 @@ uint64_t wait_limit_ns();
 bool take_inject_timeout();
 
 int sm_count_current_device();
+
+// 2D tensor map (TMA descriptor) over a rows x width matrix of `dtype`
+// elements with the given row stride in bytes; box of box_w x box_rows
+// elements.  Returns false when the driver rejects it.
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                          int64_t rows, int64_t width, int64_t row_stride_bytes, uint32_t box_w,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 }  // namespace mxfp8
