@@ -146,10 +146,20 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
  *  amax_dev   device fp32 scalar, written (overwritten: not accumulated).
  *  scale_dev  device fp32 scalar s, written.
  *  q          device, n bytes, 16-byte aligned.
+ *  workspace  NULL: two kernels (amax reduction, then the cast).  Otherwise
+ *             device scratch of mxfp8_tensor_workspace_bytes() bytes, 16-byte
+ *             aligned, owned by the caller: one cooperative kernel reduces the
+ *             amax, meets at a grid barrier kept in the workspace, and casts
+ *             (the library zeroes the workspace on the stream first).  Calls
+ *             sharing one workspace must not overlap on the GPU.
  * n == 0 writes amax = 0 and s = fmax / 1e-12.
  */
 mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
-                                 float* scale_dev, void* q, mxfp8_stream_t stream);
+                                 float* scale_dev, void* q, void* workspace,
+                                 mxfp8_stream_t stream);
+
+/* Bytes of device scratch fp8_quantize_tensor takes as its workspace. */
+size_t mxfp8_tensor_workspace_bytes(void);
 
 /*
  * fp8_scaled_gemm - C = A . B^T with FP32 accumulation and a BF16 epilogue

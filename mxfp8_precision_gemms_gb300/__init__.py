@@ -57,7 +57,8 @@ def lib() -> ctypes.CDLL:
                 "mxfp8_grouped_scale_bytes": (ctypes.c_size_t, [I64, I64, I32]),
                 "fp8_quantize_mx": (st, [P, I64, I64, I64, U, P, P, P, P, P]),
                 "fp8_quantize_mx_grouped": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
-                "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P]),
+                "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
+                "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
                 "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mxfp8_last_device_status": (st, [P]),
@@ -148,16 +149,23 @@ def fp8_quantize_mx_grouped(x: torch.Tensor, offsets: torch.Tensor, flags: int =
 
 
 def fp8_quantize_tensor(x: torch.Tensor, fmt: int = FP8_E4M3, q=None, amax=None, scale=None,
-                        stream=None):
-    """Per-tensor FP8 quantization; returns (q uint8, amax fp32[1], scale fp32[1])."""
+                        workspace=None, stream=None):
+    """Per-tensor FP8 quantization; returns (q uint8, amax fp32[1], scale fp32[1]).
+
+    ``workspace``: None for the two-kernel path, or a device uint8 tensor of
+    ``mxfp8_tensor_workspace_bytes()`` bytes for the single-launch path."""
     assert x.dtype == torch.bfloat16 and x.is_contiguous()
-    _need_cuda(x)
+    _need_cuda(x, workspace)
     q = q if q is not None else torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     amax = amax if amax is not None else torch.empty(1, dtype=torch.float32, device=x.device)
     scale = scale if scale is not None else torch.empty(1, dtype=torch.float32, device=x.device)
     _check(lib().fp8_quantize_tensor(_ptr(x), x.numel(), fmt, _ptr(amax), _ptr(scale), _ptr(q),
-                                     _stream(stream)))
+                                     _ptr(workspace), _stream(stream)))
     return q, amax, scale
+
+
+def mxfp8_tensor_workspace_bytes() -> int:
+    return int(lib().mxfp8_tensor_workspace_bytes())
 
 
 # --------------------------------------------------------------- GEMMs --

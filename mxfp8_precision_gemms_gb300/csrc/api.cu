@@ -176,18 +176,28 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
                        "fp8_quantize_mx_grouped launch");
 }
 
+size_t mxfp8_tensor_workspace_bytes(void) { return 256; }
+
 mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
-                                 float* scale_dev, void* q, mxfp8_stream_t stream) {
+                                 float* scale_dev, void* q, void* workspace,
+                                 mxfp8_stream_t stream) {
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
     if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
     if (!amax_dev || !scale_dev) return fail(MXFP8_ERR_INVALID_ARG, "amax/scale is NULL");
     if (n > 0 && (!x_bf16 || !q)) return fail(MXFP8_ERR_INVALID_ARG, "x or q is NULL");
     if ((n > 0 && (!aligned16(x_bf16) || !aligned16(q))) ||
-        (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u))
+        (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u) ||
+        (workspace && !aligned16(workspace)))
         return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
-    return cuda_result(launch_quantize_tensor(static_cast<const uint16_t*>(x_bf16), n, fmt, amax_dev,
-                                              scale_dev, static_cast<uint8_t*>(q),
-                                              reinterpret_cast<cudaStream_t>(stream)),
+    const auto s = reinterpret_cast<cudaStream_t>(stream);
+    const auto xs = static_cast<const uint16_t*>(x_bf16);
+    const auto qs = static_cast<uint8_t*>(q);
+    if (workspace) {
+        return cuda_result(launch_quantize_tensor_fused(xs, n, fmt, amax_dev, scale_dev, qs,
+                                                        static_cast<uint32_t*>(workspace), s),
+                           "fp8_quantize_tensor (fused) launch");
+    }
+    return cuda_result(launch_quantize_tensor(xs, n, fmt, amax_dev, scale_dev, qs, s),
                        "fp8_quantize_tensor launch");
 }
 

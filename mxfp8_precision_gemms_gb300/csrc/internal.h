@@ -29,6 +29,9 @@ cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
                                    float* scale, uint8_t* q, cudaStream_t s);
+// Single cooperative launch; ws: 2 uint32 of device scratch (zeroed here).
+cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
+                                         float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s);
 
 struct GemmArgs {
     int mode;          // GEMM_MX or GEMM_TENSOR

@@ -9,10 +9,12 @@
 // Per-tensor rule ("3.8 Mixed Precision, bf16 & FP8 Training", exercise 6):
 // s = fp32(fmax / max(amax, 1e-12)), q = FP8(fp32(x * s)).
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mxfp8 {
 
@@ -333,6 +335,91 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Single-launch per-tensor quantization: every CTA reduces its share of
+// |x| into ws[0] (atomicMax on the fp32 bit pattern), the CTAs meet at a
+// grid barrier (ws[1] counts arrivals; the launch is cooperative so all CTAs
+// are resident; the wait is bounded), then each CTA recomputes the scale and
+// casts its share, re-reading x (from L2 when the tensor fits there).
+// ws[0..1] must be zero at launch.
+constexpr int kFusedThreads = 512;
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kFusedThreads)
+    tensor_quant_fused_kernel(const uint16_t* __restrict__ x, int64_t n, float* amax_out,
+                              float* scale_out, uint8_t* __restrict__ q, uint32_t* ws,
+                              uint64_t limit_ns) {
+    __shared__ uint32_t red[kFusedThreads / 32];
+    __shared__ int s_ok;
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    uint32_t m = 0;
+    int64_t i = first;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+        const uint4 a0 = x8[i], a1 = x8[i + stride], a2 = x8[i + 2 * stride],
+                    a3 = x8[i + 3 * stride];
+        m = max(m, max(max(amax8(a0), amax8(a1)), max(amax8(a2), amax8(a3))));
+    }
+    for (; i < n8; i += stride) m = max(m, amax8(x8[i]));
+    for (int64_t t = n8 * 8 + first; t < n; t += stride) m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0u;
+        m = warp_max(m);
+        if (threadIdx.x == 0) {
+            if (m) atomicMax(ws, m << 16);
+            __threadfence();
+            atomicAdd(ws + 1, 1u);
+            bool ok = ld_acquire_gpu(ws + 1) >= gridDim.x;
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                for (uint32_t it = 1;; ++it) {
+                    if (ld_acquire_gpu(ws + 1) >= gridDim.x) {
+                        ok = true;
+                        break;
+                    }
+                    if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
+                }
+            }
+            s_ok = ok ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (!s_ok) {
+        if (threadIdx.x == 0) record_status(MXFP8_ERR_TIMEOUT);
+        return;
+    }
+    const float amax = __uint_as_float(ld_acquire_gpu(ws));
+    const float fmax = FMT == FP8_E4M3 ? 448.0f : 57344.0f;
+    const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *amax_out = amax;
+        *scale_out = s;
+    }
+    for (int64_t j = first; j < n8; j += stride) {
+        const uint4 v = x8[j];
+        uint2 o;
+        o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
+              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
+        o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
+              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
+        reinterpret_cast<uint2*>(q)[j] = o;
+    }
+    for (int64_t t = n8 * 8 + first; t < n; t += stride) {
+        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[t]) << 16), s);
+        q[t] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+    }
+}
+
 template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
 cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
     const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
@@ -384,6 +471,34 @@ cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float*
     } else {
         tensor_cast_kernel<FP8_E4M3><<<blocks, 256, 0, s>>>(x, n, bits, scale, q);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
+                                         float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    // resident blocks per SM, queried once per device and format
+    static std::atomic<int> per_sm[2][64];
+    const int f = fmt == FP8_E5M2 ? 1 : 0;
+    const void* k = f ? reinterpret_cast<const void*>(tensor_quant_fused_kernel<FP8_E5M2>)
+                      : reinterpret_cast<const void*>(tensor_quant_fused_kernel<FP8_E4M3>);
+    int bps = dev >= 0 && dev < 64 ? per_sm[f][dev].load() : 0;
+    if (bps <= 0) {
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, k, kFusedThreads, 0)) != cudaSuccess)
+            return e;
+        if (bps <= 0) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < 64) per_sm[f][dev].store(bps);
+    }
+    const int64_t chunks = n / 8 + 1;
+    const int64_t resident = static_cast<int64_t>(sm_count_current_device()) * bps;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((chunks + kFusedThreads - 1) / kFusedThreads, resident)));
+    uint64_t limit = wait_limit_ns();
+    void* args[] = {const_cast<uint16_t**>(&x), &n, &amax, &scale, &q, &ws, &limit};
+    e = cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kFusedThreads), args, 0, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

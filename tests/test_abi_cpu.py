@@ -65,9 +65,11 @@ def test_host_validation(lib):
     # empty input is a no-op
     assert lib.fp8_quantize_mx(None, 0, 64, 64, m.MX_ROWWISE, None, None, None, None, None) == m.MXFP8_OK
     # per-tensor
-    assert lib.fp8_quantize_tensor(P, 100, 7, P, P, P, None) == m.MXFP8_ERR_INVALID_ARG
-    assert lib.fp8_quantize_tensor(P, 100, 0, None, P, P, None) == m.MXFP8_ERR_INVALID_ARG
-    assert lib.fp8_quantize_tensor(P + 1, 100, 0, P, P, P, None) == m.MXFP8_ERR_MISALIGNED
+    assert lib.fp8_quantize_tensor(P, 100, 7, P, P, P, None, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_tensor(P, 100, 0, None, P, P, None, None) == m.MXFP8_ERR_INVALID_ARG
+    assert lib.fp8_quantize_tensor(P + 1, 100, 0, P, P, P, None, None) == m.MXFP8_ERR_MISALIGNED
+    assert lib.fp8_quantize_tensor(P, 100, 0, P, P, P, P + 8, None) == m.MXFP8_ERR_MISALIGNED
+    assert lib.mxfp8_tensor_workspace_bytes() >= 8
     # GEMM
     G = lib.fp8_scaled_gemm
     assert G(5, 0, 0, P, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG

@@ -48,8 +48,9 @@ def test_mx256():
 def test_tensor4096():
     w = workloads.tensor4096(seed=0, device=device())
     out = {}
+    ws = torch.zeros(m.mxfp8_tensor_workspace_bytes(), dtype=torch.uint8, device=device())
     for name in ("X", "W"):
-        q, amax, scale = m.fp8_quantize_tensor(w[name], m.FP8_E4M3)
+        q, amax, scale = m.fp8_quantize_tensor(w[name], m.FP8_E4M3, workspace=ws)
         assert_ok()
         ra, rs, rq = oracle.quantize_tensor(workloads.bits(w[name]), oracle.E4M3)
         assert np.array_equal(host(q), rq)

@@ -178,9 +178,10 @@ def test_quantize_grouped_bad_offsets_recorded(bad):
     assert (host(q) == 0x5A).all() and (host(s) == 0x5A).all()
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two_kernels", "single_launch"])
 @pytest.mark.parametrize("fmt", [m.FP8_E4M3, m.FP8_E5M2])
 @pytest.mark.parametrize("case", ["outliers", "loguniform", "tiny", "zeros", "odd", "empty"])
-def test_quantize_tensor_matches_oracle(fmt, case):
+def test_quantize_tensor_matches_oracle(fmt, case, fused):
     if case == "outliers":
         w = workloads.tensor4096(seed=1, device="cpu", m=512, n=8, k=1024)
         bits = workloads.bits(w["X"])
@@ -198,8 +199,10 @@ def test_quantize_tensor_matches_oracle(fmt, case):
     q = filled(bits.size, 0xA5)
     amax = filled(1, -1.0, torch.float32)
     scale = filled(1, -1.0, torch.float32)
-    m.fp8_quantize_tensor(x, fmt, q=q, amax=amax, scale=scale)
-    assert_ok()
+    ws = filled(m.mxfp8_tensor_workspace_bytes(), 0x77) if fused else None
+    for _ in range(2):  # twice: the workspace keeps the last call's contents
+        m.fp8_quantize_tensor(x, fmt, q=q, amax=amax, scale=scale, workspace=ws)
+        assert_ok()
     wa, ws, wq = oracle.quantize_tensor(bits.reshape(-1), fmt)
     assert np.array_equal(host(q), wq.reshape(-1))
     assert host(amax).view(np.uint32)[0] == np.float32(wa).view(np.uint32)
