@@ -162,6 +162,35 @@ mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* 
 size_t mxfp8_tensor_workspace_bytes(void);
 
 /*
+ * fp8_quantize_tensor_noalloc - fp8_quantize_tensor's single-launch path for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * to this entry point; it exists for the library's users.
+ *
+ * Some callers cannot call cudaMalloc (or any allocating routine) at the
+ * point where they quantize: code running inside a host application that
+ * owns every device allocation, or hot loops that are forbidden to allocate
+ * after start-up.  Those callers still pass x, q, amax_dev and scale_dev, but
+ * no workspace: the scratch comes from a static 256-byte device array inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.
+ *
+ * Results are identical to fp8_quantize_tensor (same kernel, same rule).
+ * The scratch this path needs does not grow with n (it is
+ * mxfp8_tensor_workspace_bytes()); a need larger than the static array would
+ * be rejected with MXFP8_ERR_UNSUPPORTED_SHAPE before anything runs.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array and each clears the words it needs
+ * on its stream first: calls that overlap on the GPU (e.g. on two streams)
+ * race and must not be issued.  Allocates nothing (no cudaMalloc, cudaFree
+ * or allocating library routine).
+ */
+mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt,
+                                         float* amax_dev, float* scale_dev, void* q,
+                                         mxfp8_stream_t stream);
+
+/*
+ * fp8_scaled_gemm - C = A . B^T/*
  * fp8_scaled_gemm - C = A . B^T with FP32 accumulation and a BF16 epilogue
  * (round to nearest even).
  * ("Olmo-core MoE report", Section 11.1.1: block-scaled tcgen05.mma with an

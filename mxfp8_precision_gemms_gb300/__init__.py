@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_mx_grouped": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
+                "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
                 "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
                 "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mxfp8_last_device_status": (st, [P]),

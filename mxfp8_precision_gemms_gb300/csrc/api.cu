@@ -201,6 +201,31 @@ mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* 
                        "fp8_quantize_tensor launch");
 }
 
+mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
+                                         float* scale_dev, void* q, mxfp8_stream_t stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (!amax_dev || !scale_dev) return fail(MXFP8_ERR_INVALID_ARG, "amax/scale is NULL");
+    if (n > 0 && (!x_bf16 || !q)) return fail(MXFP8_ERR_INVALID_ARG, "x or q is NULL");
+    if ((n > 0 && (!aligned16(x_bf16) || !aligned16(q))) ||
+        (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
+    // the scratch this path needs must fit the library's static array
+    const size_t need = mxfp8_tensor_workspace_bytes();
+    if (need > noalloc_scratch_bytes())
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE,
+                    "needs %zu bytes of scratch, the static device array holds %zu", need,
+                    noalloc_scratch_bytes());
+    uint32_t* ws = nullptr;
+    cudaError_t e = noalloc_scratch_address(&ws);
+    if (e != cudaSuccess)
+        return fail(MXFP8_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+    return cuda_result(launch_quantize_tensor_fused(static_cast<const uint16_t*>(x_bf16), n, fmt,
+                                                    amax_dev, scale_dev, static_cast<uint8_t*>(q), ws,
+                                                    reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_tensor_noalloc launch");
+}
+
 mxfp8_status fp8_scaled_gemm(int mode, int a_fmt, int b_fmt, const void* a, const void* a_scale,
                              const void* b, const void* b_scale, int64_t M, int64_t N, int64_t K,
                              void* c_bf16, int64_t ldc, mxfp8_stream_t stream) {

@@ -30,6 +30,7 @@ cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
                                    float* scale, uint8_t* q, cudaStream_t s);
 // Single cooperative launch; ws: 2 uint32 of device scratch (zeroed here).
+// The scratch it needs, whatever n is: mxfp8_tensor_workspace_bytes().
 cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
                                          float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s);
 
@@ -53,6 +54,11 @@ cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64
 
 // Per-translation-unit device status words: read (and clear) after a sync.
 cudaError_t take_status_quant(unsigned* out);
+
+// The allocation-free per-tensor path's static device scratch: its size and
+// its address on the current device (looked up once per device).
+size_t noalloc_scratch_bytes();
+cudaError_t noalloc_scratch_address(uint32_t** out);
 cudaError_t take_status_gemm(unsigned* out);
 
 // Time limit for device waits (ns) and the one-shot timeout-injection hook.

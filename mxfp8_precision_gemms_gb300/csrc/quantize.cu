@@ -10,6 +10,7 @@
 // s = fp32(fmax / max(amax, 1e-12)), q = FP8(fp32(x * s)).
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -500,6 +501,37 @@ cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, 
     e = cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kFusedThreads), args, 0, s);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Scratch of fp8_quantize_tensor_noalloc: a file-scope device array, so that
+// entry point needs no memory from its caller.  Every GPU that loads this
+// library holds these 256 bytes until the process exits; all calls on a
+// device share them.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / 4];
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol's name is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress, once per device, while that device is current.
+cudaError_t noalloc_scratch_address(uint32_t** out) {
+    constexpr int kDevices = 64;
+    static std::mutex mu;
+    static uint32_t* addr[kDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<uint32_t*>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t take_status_quant(unsigned* out) {
