@@ -137,6 +137,21 @@ def _num(s):
         return False
 
 
+def max_over_ranks(ms: float, pg, device=None) -> float:
+    """The slowest rank's time (the job's time); identity without a group."""
+    if pg is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job rate: the units all ranks processed per step over the
+    (max-over-ranks) step time, in units per second x 1e-12 (TFLOP/s for FLOPs)."""
+    return world * units_per_rank / (ms_per_step / 1e3) / 1e12
+
+
 # ----------------------------------------------------------- workloads --
 
 class Timer:
@@ -495,11 +510,7 @@ def e2e_pipelined(m, wl, dev, steps, pg):
     s_in.wait_stream(s_out)
     t1.record(s_in)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, pg, dev)
     out = {"value": None, "unit": UNIT, "ms_per_step": ms,
            "h2d_bytes_per_step": Xh.numel() * 2 + Wh.numel() * 2,
            "d2h_bytes_per_step": Ch[0].numel() * 2,
@@ -563,15 +574,11 @@ def main():
     ev1.record()
     barrier()
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     gemm_ms = timer.avg_ms("gemm")
     qx_ms, qw_ms = timer.avg_ms("quantize_x"), timer.avg_ms("quantize_w")
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
     ms_step = ms_total / args.steps
-    value = world * wl.flops / (ms_step / 1e3) / 1e12
+    value = job_throughput(wl.flops, world, ms_step)
 
     # ---- end to end through the C ABI with host buffers: every step copies
     # its X and W from pinned host memory and its C back to pinned host
@@ -579,7 +586,7 @@ def main():
     # double-buffered device tensors, so one step's copies overlap its
     # neighbours' compute.
     e2e = e2e_pipelined(m, wl, dev, args.e2e_steps, pg)
-    e2e["value"] = world * wl.flops / (e2e["ms_per_step"] / 1e3) / 1e12
+    e2e["value"] = job_throughput(wl.flops, world, e2e["ms_per_step"])
 
     rows = None
     if not args.no_rows:
