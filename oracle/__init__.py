@@ -64,6 +64,7 @@ def _load():
                                                 I64, I64, I64, P, I64, P]),
                 "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, I64, P]),
                 "orc_num_threads": (I, []),
+                "orc_dequantize_mx": (None, [P, P, I64, I64, P, I64]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -158,6 +159,16 @@ def quantize_mx(x_bits: np.ndarray, flags: int = ROWWISE) -> dict:
         out["q_row"], out["s_row"] = q_row, s_row
     if flags & COLWISE:
         out["q_col"], out["s_col"] = q_col, s_col
+    return out
+
+
+def dequantize_mx(q, s) -> np.ndarray:
+    """BF16 bit patterns of s * q for a rowwise MX operand (q: rows x cols)."""
+    q = np.ascontiguousarray(q, np.uint8)
+    s = np.ascontiguousarray(s, np.uint8)
+    rows, cols = q.shape
+    out = np.zeros((rows, cols), np.uint16)
+    _load().orc_dequantize_mx(_p(q), _p(s), rows, cols, _p(out), cols)
     return out
 
 

@@ -321,6 +321,24 @@ void orc_quantize_mx_grouped(const uint16_t* x, int64_t cols, int64_t ld,
     }
 }
 
+/* MX dequantization to BF16 ([OLMO] Eq. 58, x^ = s q; Section 11.4.3: a
+ * saved MXFP8 activation is dequantized when a BF16 consumer needs it).
+ * out[r, c] = bf16_RNE(E4M3(q[r, c]) * 2^(byte(r, c/32) - 127)), computed
+ * exactly in FP64 and rounded once (overflow to Inf, NaN codes / NaN scales
+ * give NaN).  q is rows x cols (row stride cols); s is the swizzled array of
+ * a rows x cols operand; out has row stride ldo. */
+void orc_dequantize_mx(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols,
+                       uint16_t* out, int64_t ldo) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            uint8_t sb = s[orc_swizzle_offset(r, c / 32, cols)];
+            double v = orc_e4m3_decode(q[r * cols + c]) * orc_e8m0_decode(sb);
+            out[r * ldo + c] = orc_bf16_round(v);
+        }
+    }
+}
+
 /* Dequantize one operand row ([OLMO] Eq. 58: x^ = s q). */
 static void deq_row(const uint8_t* q, const uint8_t* s, int64_t r, int64_t k,
                     int64_t s_row_base, double* out) {

@@ -565,3 +565,50 @@ def test_gemm_grouped_vs_numpy():
     want = [1, 150, 207]
     got_w = oracle.gemm_grouped(qa, sa, qw, sw, off, rows=want)
     assert np.array_equal(got_w, got[want])
+
+
+# ----------------------------------------------------------- dequantize --
+
+def test_dequantize_vs_torch_and_closed_form():
+    """s q rounded once to BF16: against torch's float8 decode times the
+    scale, rounded by torch (an independent path), and exact where the
+    product is a BF16 value."""
+    rng = np.random.default_rng(12)
+    rows, cols = 160, 256
+    q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x38  # no NaN codes in this part
+    bytes_ = rng.integers(90, 165, size=(rows, cols // 32))
+    s = np.zeros(oracle.scale_bytes(rows, cols), np.uint8)
+    pos = _blocked_swizzle_index(rows, cols // 32)
+    s[pos] = bytes_
+    got = oracle.dequantize_mx(q, s)
+    vals = torch_fp8_decode(q, E4M3) * np.repeat(np.ldexp(1.0, bytes_ - 127), 32, axis=1)
+    want = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)  # the products are exact in fp32 here
+    # every value here is exactly representable: decoding gives the product back
+    assert np.array_equal(oracle.bf16_decode(got), vals)
+
+
+def test_dequantize_roundtrip_and_specials():
+    rng = np.random.default_rng(13)
+    x = oracle.bf16_round(rng.standard_t(4, size=(96, 128)))
+    qd = oracle.quantize_mx(x)
+    back = oracle.bf16_decode(oracle.dequantize_mx(qd["q_row"], qd["s_row"]))
+    xv = oracle.bf16_decode(x)
+    # |x - x^| bounded by half an E4M3 spacing at the block scale (rceil: no clipping)
+    pos = _blocked_swizzle_index(96, 4)
+    sc = np.repeat(np.ldexp(1.0, qd["s_row"][pos].astype(int) - 127), 32, axis=1)
+    _, ex = np.frexp(np.abs(xv / sc))
+    spacing = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3) * sc
+    assert np.all(np.abs(xv - back) <= spacing / 2)
+    # NaN code, NaN scale, overflow to Inf, BF16-subnormal rounding
+    q = np.array([[0x7F] + [0x38] * 31, [0x7E] * 32, [0x01] * 32], np.uint8)
+    s = np.zeros(oracle.scale_bytes(3, 32), np.uint8)
+    s[oracle.swizzle_offset(0, 0, 32)] = 127
+    s[oracle.swizzle_offset(1, 0, 32)] = 254   # 448 * 2^127 overflows BF16
+    s[oracle.swizzle_offset(2, 0, 32)] = 3     # 2^-9 * 2^-124 = 2^-133: smallest BF16 subnormal
+    out = oracle.dequantize_mx(q, s)
+    assert np.isnan(oracle.bf16_decode(out[0, :1]))[0]
+    assert out[0, 1] == 0x3F80                  # 1.0
+    assert np.all(out[1] == 0x7F80)             # +Inf
+    assert np.all(out[2] == 0x0001)
