@@ -244,6 +244,83 @@ mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
                               void* c_bf16, int64_t ldc, mxfp8_stream_t stream);
 
 /*
+ * Routed-path kernels around the quantizer ("Olmo-core MoE report", Section
+ * 11.4.1 and Table 25).  Each takes optional group offsets: NULL with
+ * groups == 0 gives the plain rows x cols layout of fp8_quantize_mx's rowwise
+ * output; a device array of groups + 1 int32 (1 <= groups <= 1024, rows <
+ * 2^31, same rules and device check as fp8_quantize_mx_grouped) gives that
+ * entry point's group-padded scale layout.
+ */
+
+/*
+ * fp8_dequantize_mx - BF16 x^ = s q of a rowwise MXFP8 operand ("Olmo-core
+ * MoE report", Section 11.2.1 Eq. 58; used where a saved MXFP8 activation
+ * meets a BF16 consumer, Section 11.4.3, and for the routed Wgrad operands,
+ * Section 11.4.1).  A colwise output (q_col, s_col) is itself a rowwise
+ * operand of the transpose and dequantizes to X^T.
+ *
+ *  q        device, rows x cols E4M3 bytes (row stride cols).
+ *  s        device, its scales (mxfp8_scale_bytes(rows, cols), or the
+ *           group-padded array when offsets are given).
+ *  out_bf16 device, rows x cols BF16 with leading dimension ldo (>= cols).
+ * out[r][c] = bf16_RNE(E4M3(q[r][c]) * 2^(byte - 127)), the product being
+ * exact before that one rounding (overflow gives Inf; an E4M3 NaN code or
+ * scale byte 0xFF gives NaN).  Requirements: cols % 32 == 0, ldo % 8 == 0,
+ * every pointer 16-byte aligned.
+ */
+mxfp8_status fp8_dequantize_mx(const void* q, const void* s, int64_t rows, int64_t cols,
+                               const int32_t* group_offsets_dev, int32_t groups, void* out_bf16,
+                               int64_t ldo, mxfp8_stream_t stream);
+
+/*
+ * fp8_swiglu_quantize_mx - SwiGLU of the up/gate GEMM output, MXFP8-quantized
+ * rowwise in the same pass ("Olmo-core MoE report", Section 11.4.1: the fused
+ * SwiGLU-plus-quantization step that feeds the down projection; Table 25).
+ *
+ *  h_bf16  device, rows x 2f BF16 (leading dimension ld >= 2f): gate in
+ *          columns [0, f), up in columns [f, 2f).
+ *  q, s    outputs as fp8_quantize_mx's rowwise ones for a rows x f operand
+ *          (or the group-padded scale array).
+ * The hidden value a = bf16_RNE(g * sigma(g) * u), sigma(g) = 1/(1+e^-g), is
+ * what an unfused SwiGLU would store in BF16; it is formed in fp32 (double
+ * below g = -80) within 1.25 * 2^-21 relative of the exact value, so a is the
+ * correctly rounded BF16 value except within that distance of a rounding
+ * midpoint, where it may be the neighbour.  a is then quantized by the MX rule
+ * of fp8_quantize_mx (flags: MX_SCALE_FLOOR optional, rowwise implied) and
+ * never written.  Requirements: f % 32 == 0, ld % 8 == 0, pointers 16-byte
+ * aligned.
+ */
+mxfp8_status fp8_swiglu_quantize_mx(const void* h_bf16, int64_t rows, int64_t f, int64_t ld,
+                                    const int32_t* group_offsets_dev, int32_t groups,
+                                    unsigned flags, void* q, void* s, mxfp8_stream_t stream);
+
+/*
+ * fp8_route_weight_quantize_mx - combine backward: the route-weighted output
+ * gradient of every dispatched row, MXFP8-quantized rowwise in the same pass
+ * ("Olmo-core MoE report", Section 11.4.1: combine backward applies the route
+ * weights while quantizing the output gradient; Table 25).
+ *
+ *  dy_bf16         device, tokens x cols BF16 output gradient, leading
+ *                  dimension ld (>= cols).
+ *  row_token_dev   device, rows int32: the token each dispatched row came
+ *                  from.  An index outside [0, tokens) records
+ *                  MXFP8_ERR_DEVICE_CHECK; that row is quantized as zeros.
+ *  row_weight_dev  device, rows fp32 route weights.
+ *  q, s            rowwise outputs for the rows x cols dispatched gradient
+ *                  (or the group-padded scale array).
+ * Row i is g_i = bf16_RNE(w_i * dy[row_token[i]]), rounded once from the exact
+ * product, then quantized by the MX rule (MX_SCALE_FLOOR optional).  The
+ * route-expanded BF16 gradient is never written.  Requirements: cols % 32 ==
+ * 0, ld % 8 == 0, dy/q/s 16-byte aligned, row_token/row_weight 4-byte aligned.
+ */
+mxfp8_status fp8_route_weight_quantize_mx(const void* dy_bf16, int64_t tokens, int64_t ld,
+                                          const int32_t* row_token_dev,
+                                          const float* row_weight_dev, int64_t rows,
+                                          int64_t cols, const int32_t* group_offsets_dev,
+                                          int32_t groups, unsigned flags, void* q, void* s,
+                                          mxfp8_stream_t stream);
+
+/*
  * mxfp8_last_device_status - synchronize `stream`, then return and clear the
  * device status word of the current device: MXFP8_OK, MXFP8_ERR_DEVICE_CHECK
  * or MXFP8_ERR_TIMEOUT (the first one recorded since the last call), or

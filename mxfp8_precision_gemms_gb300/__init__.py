@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
+                "fp8_dequantize_mx": (st, [P, P, I64, I64, P, I32, P, I64, P]),
+                "fp8_swiglu_quantize_mx": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
+                "fp8_route_weight_quantize_mx": (st, [P, I64, I64, P, P, I64, I64, P, I32, U, P, P, P]),
                 "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
                 "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mxfp8_last_device_status": (st, [P]),
@@ -167,6 +170,70 @@ def fp8_quantize_tensor(x: torch.Tensor, fmt: int = FP8_E4M3, q=None, amax=None,
 
 def mxfp8_tensor_workspace_bytes() -> int:
     return int(lib().mxfp8_tensor_workspace_bytes())
+
+
+# ------------------------------------------- routed-path conversions --
+
+def _scales_for(rows: int, cols: int, offsets, device) -> torch.Tensor:
+    if offsets is None:
+        n = mxfp8_scale_bytes(rows, cols)
+    else:
+        n = mxfp8_grouped_scale_bytes(rows, cols, offsets.numel() - 1)
+    return torch.empty(max(1, n), dtype=torch.uint8, device=device)
+
+
+def _groups(offsets) -> int:
+    if offsets is None:
+        return 0
+    assert offsets.dtype == torch.int32
+    return offsets.numel() - 1
+
+
+def fp8_dequantize_mx(q: torch.Tensor, s: torch.Tensor, offsets=None, out=None,
+                      stream=None) -> torch.Tensor:
+    """BF16 s * q of a rowwise MX operand (q: rows x cols uint8); offsets: the
+    int32 group offsets of a group-padded scale array, or None."""
+    assert q.dtype == torch.uint8 and q.dim() == 2 and q.is_contiguous()
+    _need_cuda(q, s, offsets)
+    rows, cols = q.shape
+    out = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    assert out.dtype == torch.bfloat16 and out.stride(1) == 1
+    _check(lib().fp8_dequantize_mx(_ptr(q), _ptr(s), rows, cols, _ptr(offsets), _groups(offsets),
+                                   _ptr(out), out.stride(0), _stream(stream)))
+    return out
+
+
+def fp8_swiglu_quantize_mx(h: torch.Tensor, offsets=None, flags: int = 0, q=None, s=None,
+                           stream=None):
+    """Rowwise MXFP8 of SwiGLU(h): h is rows x 2f BF16 (gate | up); returns (q, s)."""
+    assert h.dtype == torch.bfloat16 and h.dim() == 2 and h.stride(1) == 1
+    _need_cuda(h, offsets)
+    rows, width = h.shape
+    f = width // 2
+    q = q if q is not None else torch.empty((rows, f), dtype=torch.uint8, device=h.device)
+    s = s if s is not None else _scales_for(rows, f, offsets, h.device)
+    _check(lib().fp8_swiglu_quantize_mx(_ptr(h), rows, f, h.stride(0), _ptr(offsets), _groups(offsets),
+                                        flags, _ptr(q), _ptr(s), _stream(stream)))
+    return q, s
+
+
+def fp8_route_weight_quantize_mx(dy: torch.Tensor, row_token: torch.Tensor, row_weight: torch.Tensor,
+                                 offsets=None, flags: int = 0, q=None, s=None, stream=None):
+    """Rowwise MXFP8 of w_i * dy[row_token[i]] for every dispatched row i;
+    row_token int32, row_weight fp32 (device).  Returns (q, s)."""
+    assert dy.dtype == torch.bfloat16 and dy.dim() == 2 and dy.stride(1) == 1
+    assert row_token.dtype == torch.int32 and row_weight.dtype == torch.float32
+    assert row_token.numel() == row_weight.numel()
+    _need_cuda(dy, row_token, row_weight, offsets)
+    tokens, cols = dy.shape
+    rows = row_token.numel()
+    q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=dy.device)
+    s = s if s is not None else _scales_for(rows, cols, offsets, dy.device)
+    _check(lib().fp8_route_weight_quantize_mx(_ptr(dy), tokens, dy.stride(0), _ptr(row_token),
+                                              _ptr(row_weight), rows, cols, _ptr(offsets),
+                                              _groups(offsets), flags, _ptr(q), _ptr(s),
+                                              _stream(stream)))
+    return q, s
 
 
 # --------------------------------------------------------------- GEMMs --

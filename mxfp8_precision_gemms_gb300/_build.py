@@ -15,8 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxfp8.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+SOURCES = ["api.cu", "quantize.cu", "fused.cu", "gemm.cu"]
+HEADERS = ["ptx.cuh", "mx_common.cuh", "internal.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -46,6 +46,19 @@ mxfp8_status cuda_result(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Optional group offsets of the routed entry points: NULL with groups == 0
+// selects the plain layout; otherwise 1 <= groups <= 1024 and rows < 2^31.
+mxfp8_status check_groups(const int32_t* offsets, int32_t groups, int64_t rows) {
+    if (!offsets) {
+        if (groups != 0) return fail(MXFP8_ERR_INVALID_ARG, "groups given without group_offsets");
+        return ok();
+    }
+    if (groups <= 0) return fail(MXFP8_ERR_INVALID_ARG, "groups must be >= 1 with group_offsets");
+    if (groups > 1024) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "groups > 1024");
+    if (rows > 0x7FFFFFFF) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "grouped rows >= 2^31");
+    return ok();
+}
+
 }  // namespace
 
 uint64_t wait_limit_ns() { return g_wait_limit.load(); }
@@ -177,6 +190,97 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
 }
 
 size_t mxfp8_tensor_workspace_bytes(void) { return 256; }
+
+mxfp8_status fp8_dequantize_mx(const void* q, const void* s, int64_t rows, int64_t cols,
+                               const int32_t* group_offsets_dev, int32_t groups, void* out_bf16,
+                               int64_t ldo, mxfp8_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    mxfp8_status st = check_groups(group_offsets_dev, groups, rows);
+    if (st != MXFP8_OK) return st;
+    if (rows == 0 || cols == 0) return ok();
+    if (!q || !s || !out_bf16) return fail(MXFP8_ERR_INVALID_ARG, "q, s or out is NULL");
+    if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (cols=%lld)", (long long)cols);
+    if (ldo < cols) return fail(MXFP8_ERR_INVALID_ARG, "ldo < cols");
+    if (ldo % 8 || !aligned16(q) || !aligned16(s) || !aligned16(out_bf16))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer or ldo not 16-byte aligned");
+    DequantArgs a{};
+    a.q = static_cast<const uint8_t*>(q);
+    a.s = static_cast<const uint8_t*>(s);
+    a.rows = rows;
+    a.cols = cols;
+    a.offsets = group_offsets_dev;
+    a.groups = groups;
+    a.out = static_cast<uint16_t*>(out_bf16);
+    a.ldo = ldo;
+    return cuda_result(launch_dequantize_mx(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_dequantize_mx launch");
+}
+
+mxfp8_status fp8_swiglu_quantize_mx(const void* h_bf16, int64_t rows, int64_t f, int64_t ld,
+                                    const int32_t* group_offsets_dev, int32_t groups,
+                                    unsigned flags, void* q, void* s, mxfp8_stream_t stream) {
+    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
+        return fail(MXFP8_ERR_INVALID_ARG, "SwiGLU quantization is rowwise only");
+    if (rows < 0 || f < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    mxfp8_status st = check_groups(group_offsets_dev, groups, rows);
+    if (st != MXFP8_OK) return st;
+    if (rows == 0 || f == 0) return ok();
+    if (!h_bf16 || !q || !s) return fail(MXFP8_ERR_INVALID_ARG, "h, q or s is NULL");
+    if (f % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "f %% 32 != 0 (f=%lld)", (long long)f);
+    if (ld < 2 * f) return fail(MXFP8_ERR_INVALID_ARG, "ld < 2 f");
+    if (ld % 8 || !aligned16(h_bf16) || !aligned16(q) || !aligned16(s))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer or ld not 16-byte aligned");
+    SwigluQuantArgs a{};
+    a.h = static_cast<const uint16_t*>(h_bf16);
+    a.rows = rows;
+    a.f = f;
+    a.ld = ld;
+    a.offsets = group_offsets_dev;
+    a.groups = groups;
+    a.flags = flags;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = static_cast<uint8_t*>(s);
+    return cuda_result(launch_swiglu_quantize_mx(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_swiglu_quantize_mx launch");
+}
+
+mxfp8_status fp8_route_weight_quantize_mx(const void* dy_bf16, int64_t tokens, int64_t ld,
+                                          const int32_t* row_token_dev,
+                                          const float* row_weight_dev, int64_t rows,
+                                          int64_t cols, const int32_t* group_offsets_dev,
+                                          int32_t groups, unsigned flags, void* q, void* s,
+                                          mxfp8_stream_t stream) {
+    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
+        return fail(MXFP8_ERR_INVALID_ARG, "route-weighted quantization is rowwise only");
+    if (rows < 0 || cols < 0 || tokens < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    mxfp8_status st = check_groups(group_offsets_dev, groups, rows);
+    if (st != MXFP8_OK) return st;
+    if (rows == 0 || cols == 0) return ok();
+    if (!dy_bf16 || !row_token_dev || !row_weight_dev || !q || !s)
+        return fail(MXFP8_ERR_INVALID_ARG, "dy, row_token, row_weight, q or s is NULL");
+    if (tokens == 0) return fail(MXFP8_ERR_INVALID_ARG, "rows to fill but no tokens");
+    if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (cols=%lld)", (long long)cols);
+    if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");
+    if (ld % 8 || !aligned16(dy_bf16) || !aligned16(q) || !aligned16(s))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer or ld not 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(row_token_dev) | reinterpret_cast<uintptr_t>(row_weight_dev)) & 3u)
+        return fail(MXFP8_ERR_MISALIGNED, "row_token or row_weight not 4-byte aligned");
+    WeightedQuantArgs a{};
+    a.dy = static_cast<const uint16_t*>(dy_bf16);
+    a.tokens = tokens;
+    a.ld = ld;
+    a.row_token = row_token_dev;
+    a.row_weight = row_weight_dev;
+    a.rows = rows;
+    a.cols = cols;
+    a.offsets = group_offsets_dev;
+    a.groups = groups;
+    a.flags = flags;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = static_cast<uint8_t*>(s);
+    return cuda_result(launch_weighted_quantize_mx(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_route_weight_quantize_mx launch");
+}
 
 mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
                                  float* scale_dev, void* q, void* workspace,
@@ -311,10 +415,11 @@ mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
 mxfp8_status mxfp8_last_device_status(mxfp8_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
-    unsigned q = 0, g = 0;
-    if ((e = take_status_quant(&q)) != cudaSuccess || (e = take_status_gemm(&g)) != cudaSuccess)
+    unsigned q = 0, g = 0, fu = 0;
+    if ((e = take_status_quant(&q)) != cudaSuccess || (e = take_status_gemm(&g)) != cudaSuccess ||
+        (e = take_status_fused(&fu)) != cudaSuccess)
         return fail(MXFP8_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-    const unsigned st = q ? q : g;
+    const unsigned st = q ? q : (g ? g : fu);
     if (st) return fail(static_cast<mxfp8_status>(st), "device reported %s",
                         mxfp8_status_string(static_cast<mxfp8_status>(st)));
     return ok();

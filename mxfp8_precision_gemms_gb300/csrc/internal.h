@@ -34,6 +34,47 @@ cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float*
 cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
                                          float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s);
 
+// The kernels around the quantizer (fused.cu).  offsets == nullptr selects
+// the plain layout; otherwise scales are group-padded as in the grouped
+// quantizer.
+struct DequantArgs {
+    const uint8_t* q;
+    const uint8_t* s;
+    int64_t rows, cols;
+    const int32_t* offsets;
+    int32_t groups;
+    uint16_t* out;
+    int64_t ldo;
+};
+
+struct SwigluQuantArgs {
+    const uint16_t* h;  // rows x 2f: gate columns [0, f), up columns [f, 2f)
+    int64_t rows, f, ld;
+    const int32_t* offsets;
+    int32_t groups;
+    unsigned flags;
+    uint8_t* q;
+    uint8_t* s;
+};
+
+struct WeightedQuantArgs {
+    const uint16_t* dy;  // tokens x cols, leading dimension ld
+    int64_t tokens, ld;
+    const int32_t* row_token;
+    const float* row_weight;
+    int64_t rows, cols;
+    const int32_t* offsets;
+    int32_t groups;
+    unsigned flags;
+    uint8_t* q;
+    uint8_t* s;
+};
+
+cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t s);
+cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t s);
+cudaError_t take_status_fused(unsigned* out);
+
 struct GemmArgs {
     int mode;          // GEMM_MX or GEMM_TENSOR
     int a_fmt, b_fmt;  // FP8_E4M3 / FP8_E5M2

@@ -1,0 +1,168 @@
+// Device helpers shared by the MX quantizer kernels (quantize.cu) and the
+// fused producers that quantize what they compute (fused.cu): the E8M0 rule
+// from a BF16 amax, saturating FP8 conversion, the swizzled scale-tile
+// position of a row, the row-tile lookup of group-padded (per-expert)
+// operands, and one rowwise quantization step of a 128 x 128 tile.
+//
+// MX rule ("Olmo-core MoE report, Section 11: MXFP8 Training", Eq. 58 and
+// Section 11.3.5): per 32-value block, amax -> E8M0 scale s = 2^e (rceil:
+// smallest e with amax <= 448 * 2^e; floor: e = floor(log2 amax) - 8),
+// clamped to [-127, 127]; payload q = E4M3(x / s), round to nearest even,
+// saturating.  Scale tiles: 128 rows x 4 blocks in 512 bytes (Section 11.3.2).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/mxfp8.h"
+
+namespace mxfp8 {
+
+constexpr int kTile = 128;     // rows and columns of one quantizer tile
+constexpr int kThreads = 256;  // 8 warps; each half-warp covers one tile row
+
+// E8M0 byte (e + 127) of a block from the bit pattern of its largest BF16
+// magnitude.  BF16 magnitude bits order like the magnitudes, with Inf and
+// NaN (>= 0x7F80) above every finite value.  For a normal amax with exponent
+// field f and mantissa field m: amax = (1 + m/128) 2^(f-127) and 448 = 1.75 2^8,
+// so rceil gives e = f - 135 + (m > 0x60) and floor gives e = f - 135.
+// Zero and subnormal amax fall below the clamp (byte 0).
+__device__ __forceinline__ uint32_t e8m0_byte(uint32_t amax_bits, bool floor_rule) {
+    if (amax_bits >= 0x7F80u) return 0xFFu;
+    const int f = static_cast<int>(amax_bits >> 7);
+    const int byte = f - 8 + ((!floor_rule && (amax_bits & 0x7Fu) > 0x60u) ? 1 : 0);
+    return byte < 0 ? 0u : static_cast<uint32_t>(byte);
+}
+
+// 1 / s = 2^(127 - byte) as an fp32 power of two (byte <= 247 for finite
+// BF16 input, so the exponent field 254 - byte stays normal).
+__device__ __forceinline__ float inv_scale(uint32_t byte) {
+    return __uint_as_float((254u - byte) << 23);
+}
+
+// Largest BF16 magnitude bits among the 8 values of a 16-byte vector.
+__device__ __forceinline__ uint32_t amax8(const uint4& v) {
+    uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Saturating RNE conversion of two fp32 values; `lo` lands in the low byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == FP8_E4M3) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
+// Four consecutive BF16 values (two words) times a factor -> four E4M3 bytes.
+// The product by a power of two is exact (no FTZ in this file).
+__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float f) {
+    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
+    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
+    return a | (b << 16);
+}
+
+// Same for four values held in the low (or high) halves of four words.
+template <bool HIGH>
+__device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                uint32_t w3, float f) {
+    auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
+    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
+    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
+    return a | (b << 16);
+}
+
+// Byte offset, inside its 512-byte tile, of the 4-byte group of scales of
+// tile row r (0..127): 32-row groups x 4 K-blocks per tile.
+__device__ __forceinline__ int swz_word(int r) { return (r & 31) * 16 + (r >> 5) * 4; }
+
+// Warp 0 of a CTA finds the rows [begin, end) of padded row tile rt of a
+// group-padded operand: group g owns ceil(m_g / 128) consecutive 128-row
+// tiles, m_g = offsets[g+1] - offsets[g].  It also validates the offsets
+// (offsets[0] == 0, non-decreasing, offsets[G] == total).  Results go to
+// shared memory: rows[0..1] (-1 past the last tile) and *ok.  The caller
+// synchronizes the CTA before reading them.
+__device__ __forceinline__ void locate_group_tile(const int32_t* off, int G, int64_t total,
+                                                  int64_t rt, int64_t* rows, int* ok_out) {
+    const int lane = threadIdx.x & 31;
+    bool ok = (off[0] == 0) && (static_cast<int64_t>(off[G]) == total);
+    int64_t base = 0, found_begin = -1, found_end = -1;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        int64_t tiles = 0, b = 0, e = 0;
+        if (g < G) {
+            b = off[g];
+            e = off[g + 1];
+            if (e < b) ok = false;
+            tiles = e > b ? (e - b + kTile - 1) / kTile : 0;
+        }
+        int64_t incl = tiles;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        const int64_t excl = base + incl - tiles;
+        if (g < G && rt >= excl && rt < excl + tiles) {
+            found_begin = b + (rt - excl) * kTile;
+            found_end = min(e, found_begin + kTile);
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    const unsigned who = __ballot_sync(0xffffffffu, found_begin >= 0);
+    if (lane == 0) {
+        *ok_out = ok ? 1 : 0;
+        rows[0] = -1;
+        rows[1] = -1;
+    }
+    __syncwarp();
+    if (who && lane == __ffs(who) - 1) {
+        rows[0] = found_begin;
+        rows[1] = found_end;
+    }
+}
+
+// One rowwise step of a 128 x 128 tile: the half-warp holding tile row r
+// (lane & 16 selects the half) has 8 BF16 values per lane in v, lanes
+// 4b..4b+3 of the half forming 32-value block b.  Writes the 8 E4M3 bytes to
+// q_dst (skipped when null) and, from the half's lane 0, the row's four
+// scale bytes into the 512-byte scale tile.  All 32 lanes must call it.
+template <bool FLOOR>
+__device__ __forceinline__ void mx_row_step(const uint4& v, int r, uint8_t* q_dst,
+                                            uint8_t* s_tile) {
+    const int lane = threadIdx.x & 31;
+    uint32_t m = amax8(v);
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const uint32_t byte = e8m0_byte(m, FLOOR);
+    uint2 q;
+    if (byte == 0xFFu) {
+        q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+        const float f = inv_scale(byte);
+        q.x = quant4_e4m3(v.x, v.y, f);
+        q.y = quant4_e4m3(v.z, v.w, f);
+    }
+    if (q_dst != nullptr) *reinterpret_cast<uint2*>(q_dst) = q;
+    const int hb = lane & 16;
+    const uint32_t b0 = __shfl_sync(0xffffffffu, byte, hb + 0);
+    const uint32_t b1 = __shfl_sync(0xffffffffu, byte, hb + 4);
+    const uint32_t b2 = __shfl_sync(0xffffffffu, byte, hb + 8);
+    const uint32_t b3 = __shfl_sync(0xffffffffu, byte, hb + 12);
+    if ((lane & 15) == 0) {
+        *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+}
+
+}  // namespace mxfp8

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "mx_common.cuh"
 #include "ptx.cuh"
 
 namespace mxfp8 {
@@ -23,76 +24,9 @@ __device__ unsigned int g_status_quant = 0;
 
 namespace {
 
-constexpr int kTile = 128;     // rows and columns of one quantizer tile
-constexpr int kThreads = 256;  // 8 warps; each half-warp covers one tile row
-
 __device__ __forceinline__ void record_status(unsigned code) {
     atomicCAS(&g_status_quant, 0u, code);
 }
-
-// E8M0 byte (e + 127) of a block from the bit pattern of its largest BF16
-// magnitude.  BF16 magnitude bits order like the magnitudes, with Inf and
-// NaN (>= 0x7F80) above every finite value.  For a normal amax with exponent
-// field f and mantissa field m: amax = (1 + m/128) 2^(f-127) and 448 = 1.75 2^8,
-// so rceil gives e = f - 135 + (m > 0x60) and floor gives e = f - 135.
-// Zero and subnormal amax fall below the clamp (byte 0).
-__device__ __forceinline__ uint32_t e8m0_byte(uint32_t amax_bits, bool floor_rule) {
-    if (amax_bits >= 0x7F80u) return 0xFFu;
-    const int f = static_cast<int>(amax_bits >> 7);
-    const int byte = f - 8 + ((!floor_rule && (amax_bits & 0x7Fu) > 0x60u) ? 1 : 0);
-    return byte < 0 ? 0u : static_cast<uint32_t>(byte);
-}
-
-// 1 / s = 2^(127 - byte) as an fp32 power of two (byte <= 247 for finite
-// BF16 input, so the exponent field 254 - byte stays normal).
-__device__ __forceinline__ float inv_scale(uint32_t byte) {
-    return __uint_as_float((254u - byte) << 23);
-}
-
-// Largest BF16 magnitude bits among the 8 values of a 16-byte vector.
-__device__ __forceinline__ uint32_t amax8(const uint4& v) {
-    uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
-    return max(m & 0xFFFFu, m >> 16);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Saturating RNE conversion of two fp32 values; `lo` lands in the low byte.
-template <int FMT>
-__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
-    uint16_t r;
-    if constexpr (FMT == FP8_E4M3) {
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    } else {
-        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    }
-    return r;
-}
-
-// Four consecutive BF16 values (two words) times a factor -> four E4M3 bytes.
-// The product by a power of two is exact (no FTZ in this file).
-__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float f) {
-    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
-    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
-    return a | (b << 16);
-}
-
-// Same for four values held in the low (or high) halves of four words.
-template <bool HIGH>
-__device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
-                                                uint32_t w3, float f) {
-    auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
-    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
-    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
-    return a | (b << 16);
-}
-
-// Byte offset, inside its 512-byte tile, of the 4-byte group of scales of
-// tile row r (0..127): 32-row groups x 4 K-blocks per tile.
-__device__ __forceinline__ int swz_word(int r) { return (r & 31) * 16 + (r >> 5) * 4; }
 
 // One CTA quantizes a 128 x 128 tile.  blockIdx.x = 128-row scale tile,
 // blockIdx.y = 128-column tile.  Rowwise: a half-warp owns one tile row per
@@ -115,46 +49,7 @@ __global__ void __launch_bounds__(kThreads)
 
     if constexpr (GROUPED) {
         // Find the group owning padded row tile rt; validate the offsets.
-        if (tid < 32) {
-            const int32_t* off = a.offsets;
-            const int G = a.groups;
-            bool ok = (off[0] == 0) && (static_cast<int64_t>(off[G]) == a.rows);
-            int64_t base = 0, found_begin = -1, found_end = -1;
-            for (int g0 = 0; g0 < G; g0 += 32) {
-                const int g = g0 + lane;
-                int64_t tiles = 0, b = 0, e = 0;
-                if (g < G) {
-                    b = off[g];
-                    e = off[g + 1];
-                    if (e < b) ok = false;
-                    tiles = e > b ? (e - b + kTile - 1) / kTile : 0;
-                }
-                int64_t incl = tiles;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += v;
-                }
-                const int64_t excl = base + incl - tiles;
-                if (g < G && rt >= excl && rt < excl + tiles) {
-                    found_begin = b + (rt - excl) * kTile;
-                    found_end = min(e, found_begin + kTile);
-                }
-                base += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            const unsigned who = __ballot_sync(0xffffffffu, found_begin >= 0);
-            if (lane == 0) {
-                s_ok = ok ? 1 : 0;
-                s_rows[0] = -1;
-                s_rows[1] = -1;
-            }
-            __syncwarp();
-            if (who && lane == __ffs(who) - 1) {
-                s_rows[0] = found_begin;
-                s_rows[1] = found_end;
-            }
-        }
+        if (tid < 32) locate_group_tile(a.offsets, a.groups, a.rows, rt, s_rows, &s_ok);
         __syncthreads();
         if (!s_ok) {
             if (rt == 0 && ct == 0 && tid == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
@@ -188,31 +83,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
             const int r = it * 16 + (tid >> 4);
-            uint32_t m = amax8(v[it]);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const uint32_t byte = e8m0_byte(m, FLOOR);
-            uint2 q;
-            if (byte == 0xFFu) {
-                q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            } else {
-                const float f = inv_scale(byte);
-                q.x = quant4_e4m3(v[it].x, v[it].y, f);
-                q.y = quant4_e4m3(v[it].z, v[it].w, f);
-            }
             const int64_t row = row_begin + r;
-            if (row < row_end && col < a.cols) {
-                *reinterpret_cast<uint2*>(a.q_row + row * a.cols + col) = q;
-            }
-            const int hb = lane & 16;
-            const uint32_t b0 = __shfl_sync(0xffffffffu, byte, hb + 0);
-            const uint32_t b1 = __shfl_sync(0xffffffffu, byte, hb + 4);
-            const uint32_t b2 = __shfl_sync(0xffffffffu, byte, hb + 8);
-            const uint32_t b3 = __shfl_sync(0xffffffffu, byte, hb + 12);
-            if (seg == 0) {
-                *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) =
-                    b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            }
+            const bool in = row < row_end && col < a.cols;
+            mx_row_step<FLOOR>(v[it], r, in ? a.q_row + row * a.cols + col : nullptr, s_tile);
         }
     }
 

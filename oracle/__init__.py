@@ -65,6 +65,9 @@ def _load():
                 "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, I64, P]),
                 "orc_num_threads": (I, []),
                 "orc_dequantize_mx": (None, [P, P, I64, I64, P, I64]),
+                "orc_dequantize_mx_grouped": (None, [P, P, P, I32, I64, P, I64]),
+                "orc_swiglu": (None, [P, I64, I64, I64, P]),
+                "orc_route_weight": (None, [P, I64, I64, P, P, I64, I64, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -169,6 +172,39 @@ def dequantize_mx(q, s) -> np.ndarray:
     rows, cols = q.shape
     out = np.zeros((rows, cols), np.uint16)
     _load().orc_dequantize_mx(_p(q), _p(s), rows, cols, _p(out), cols)
+    return out
+
+
+def dequantize_mx_grouped(q, s, offsets) -> np.ndarray:
+    """BF16 bit patterns of s * q for a group-padded rowwise operand."""
+    q = np.ascontiguousarray(q, np.uint8)
+    s = np.ascontiguousarray(s, np.uint8)
+    off = np.ascontiguousarray(offsets, np.int32)
+    rows, cols = q.shape
+    assert int(off[-1]) == rows
+    out = np.zeros((rows, cols), np.uint16)
+    _load().orc_dequantize_mx_grouped(_p(q), _p(s), _p(off), off.size - 1, cols, _p(out), cols)
+    return out
+
+
+def swiglu(h, f: int | None = None) -> np.ndarray:
+    """FP64 g * sigma(g) * u of BF16 bits h (rows x 2f: gate | up)."""
+    h = np.ascontiguousarray(h, np.uint16)
+    rows, width = h.shape
+    f = width // 2 if f is None else f
+    out = np.zeros((rows, f), np.float64)
+    _load().orc_swiglu(_p(h), rows, f, width, _p(out))
+    return out
+
+
+def route_weight(dy, row_token, row_weight) -> np.ndarray:
+    """BF16 bits of w_i * dy[tok_i], rounded once, for every dispatched row."""
+    dy = np.ascontiguousarray(dy, np.uint16)
+    tok = np.ascontiguousarray(row_token, np.int32)
+    w = np.ascontiguousarray(row_weight, np.float32)
+    tokens, cols = dy.shape
+    out = np.zeros((tok.size, cols), np.uint16)
+    _load().orc_route_weight(_p(dy), tokens, cols, _p(tok), _p(w), tok.size, cols, _p(out))
     return out
 
 

@@ -339,6 +339,67 @@ void orc_dequantize_mx(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t
     }
 }
 
+/* Grouped form of orc_dequantize_mx: q rows keep their positions; row r of
+ * group g reads its scales from padded row P_g + (r - off[g]) of the grouped
+ * array (layout of orc_quantize_mx_grouped). */
+void orc_dequantize_mx_grouped(const uint8_t* q, const uint8_t* s, const int32_t* off,
+                               int32_t groups, int64_t cols, uint16_t* out, int64_t ldo) {
+    int64_t padded = 0;
+    for (int32_t g = 0; g < groups; ++g) {
+        int64_t m = (int64_t)off[g + 1] - off[g];
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < m; ++i) {
+            int64_t r = off[g] + i;
+            for (int64_t c = 0; c < cols; ++c) {
+                uint8_t sb = s[orc_swizzle_offset(padded + i, c / 32, cols)];
+                double v = orc_e4m3_decode(q[r * cols + c]) * orc_e8m0_decode(sb);
+                out[r * ldo + c] = orc_bf16_round(v);
+            }
+        }
+        padded += (m + 127) / 128 * 128;
+    }
+}
+
+/* SwiGLU of an up/gate output row pair ([OLMO] Section 11.4.1: the hidden
+ * representation that feeds the down projection): y = g sigma(g) u with
+ * sigma(g) = 1 / (1 + e^-g), gate g = h[r, c] and up u = h[r, f + c] for
+ * c < f.  FP64; sigma is evaluated as e^g / (1 + e^g) for g < 0 so that no
+ * intermediate overflows.  out is rows x f (row stride f). */
+void orc_swiglu(const uint16_t* h, int64_t rows, int64_t f, int64_t ld, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < f; ++c) {
+            double g = orc_bf16_decode(h[r * ld + c]);
+            double u = orc_bf16_decode(h[r * ld + f + c]);
+            double sig;
+            if (g >= 0.0) {
+                sig = 1.0 / (1.0 + exp(-g));
+            } else {
+                double e = exp(g);
+                sig = e / (1.0 + e);
+            }
+            out[r * f + c] = g * sig * u;
+        }
+    }
+}
+
+/* Route-weighted gradient rows of combine backward ([OLMO] Section 11.4.1):
+ * row i = bf16_RNE(w_i * dy[tok_i]); the product of a BF16 value and an fp32
+ * weight is exact in FP64, so this is one rounding of the exact product.
+ * An index outside [0, tokens) gives a zero row.  out is rows x cols. */
+void orc_route_weight(const uint16_t* dy, int64_t tokens, int64_t ld, const int32_t* tok,
+                      const float* w, int64_t rows, int64_t cols, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t t = tok[i];
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = 0.0;
+            if (t >= 0 && t < tokens) v = (double)w[i] * orc_bf16_decode(dy[t * ld + c]);
+            out[i * cols + c] = orc_bf16_round(v);
+        }
+    }
+}
+
 /* Dequantize one operand row ([OLMO] Eq. 58: x^ = s q). */
 static void deq_row(const uint8_t* q, const uint8_t* s, int64_t r, int64_t k,
                     int64_t s_row_base, double* out) {

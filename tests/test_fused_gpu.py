@@ -1,0 +1,230 @@
+"""GPU parity of the routed-path conversions around the quantizer:
+dequantization (bit-exact), fused SwiGLU + MX quantization (exact outside
+BF16 rounding near-ties, see mx_check) and fused route weighting + MX
+gradient quantization (bit-exact), plain and group-padded, on small ragged
+shapes and at the workloads' full sizes."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_precision_gemms_gb300 as m
+import oracle
+import workloads
+from gpu_util import assert_ok, device, filled, host, to_dev_bf16, to_dev_u8
+from mx_check import bf16_candidates, check_set_quantization
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 32), (127, 96), (128, 128), (300, 416), (513, 1056)]
+GROUP_COUNTS = [[0, 130, 5, 0, 256, 1], [1], [0, 0, 700], [128, 128, 3]]
+
+
+def _offsets(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def _random_mx(rows, cols, seed, specials=True):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    if not specials:
+        q[(q & 0x7F) == 0x7F] = 0x3C
+    s = rng.integers(0, 256 if specials else 255, size=oracle.scale_bytes(rows, cols), dtype=np.uint8)
+    return q, s
+
+
+def _bits_equal_or_both_nan(got, want):
+    gn = np.isnan(oracle.bf16_decode(got))
+    wn = np.isnan(oracle.bf16_decode(want))
+    assert np.array_equal(gn, wn), "NaN positions differ"
+    d = (got != want) & ~wn
+    assert not d.any(), f"{int(d.sum())} BF16 values differ, first at {np.argwhere(d)[0]}"
+
+
+# ---------------------------------------------------------- dequantize --
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_dequantize_random_codes_and_scales(rows, cols):
+    """Every E4M3 code with every scale byte, including 0 (2^-127), 254
+    (overflow to Inf), 255 (NaN) and NaN payload codes."""
+    q, s = _random_mx(rows, cols, rows * 7 + cols)
+    out = filled((rows, cols + 8), 0x7777, torch.int16).view(torch.bfloat16)
+    m.fp8_dequantize_mx(to_dev_u8(q), to_dev_u8(s), out=out[:, :cols])
+    assert_ok()
+    got = host(out.view(torch.int16)).view(np.uint16)
+    _bits_equal_or_both_nan(got[:, :cols], oracle.dequantize_mx(q, s))
+    assert np.all(got[:, cols:] == 0x7777), "wrote past cols"
+
+
+def test_dequantize_roundtrip_of_gpu_quantization():
+    x = workloads.student_t((384, 640), 4, 3, 0, device())
+    qd = m.fp8_quantize_mx(x, m.MX_ROWWISE | m.MX_COLWISE)
+    back = m.fp8_dequantize_mx(qd["q_row"], qd["s_row"])
+    back_t = m.fp8_dequantize_mx(qd["q_col"], qd["s_col"])
+    assert_ok()
+    want = oracle.quantize_mx(workloads.bits(x), oracle.ROWWISE | oracle.COLWISE)
+    assert np.array_equal(host(back.view(torch.int16)).view(np.uint16),
+                          oracle.dequantize_mx(want["q_row"], want["s_row"]))
+    assert np.array_equal(host(back_t.view(torch.int16)).view(np.uint16),
+                          oracle.dequantize_mx(want["q_col"], want["s_col"]))
+
+
+@pytest.mark.parametrize("counts", GROUP_COUNTS)
+def test_dequantize_grouped(counts):
+    off = _offsets(counts)
+    rows, cols = int(off[-1]), 160
+    rng = np.random.default_rng(len(counts))
+    x = oracle.bf16_round(rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-20, 20, (rows, 1))))
+    q, s = oracle.quantize_mx_grouped(x, off)
+    s_full = np.zeros(oracle.grouped_scale_bytes(off, cols) + 512, np.uint8)
+    s_full[: s.size] = s
+    out = m.fp8_dequantize_mx(to_dev_u8(q), to_dev_u8(s_full),
+                              offsets=torch.from_numpy(off).to(device()))
+    assert_ok()
+    assert np.array_equal(host(out.view(torch.int16)).view(np.uint16),
+                          oracle.dequantize_mx_grouped(q, s, off))
+
+
+def test_dequantize_grouped_bad_offsets_recorded():
+    off = np.array([0, 50, 40, 100], np.int32)  # decreasing
+    q = torch.zeros((100, 32), dtype=torch.uint8, device=device())
+    s = torch.zeros(8192, dtype=torch.uint8, device=device())
+    m.fp8_dequantize_mx(q, s, offsets=torch.from_numpy(off).to(device()))
+    assert m.mxfp8_last_device_status() == m.MXFP8_ERR_DEVICE_CHECK
+    assert_ok()  # cleared
+
+
+def test_dequantize_full_size_mlp_up_activation():
+    """Save/restore of the mlp_up activation X (8192 x 4096): GPU quantize,
+    GPU dequantize, every BF16 value against the oracle."""
+    x = workloads.mlp_up(seed=0, device=device())["X"]
+    qd = m.fp8_quantize_mx(x, m.MX_ROWWISE)
+    back = m.fp8_dequantize_mx(qd["q_row"], qd["s_row"])
+    back2 = m.fp8_dequantize_mx(qd["q_row"], qd["s_row"])
+    assert_ok()
+    want = oracle.quantize_mx(workloads.bits(x), oracle.ROWWISE)
+    ref = oracle.dequantize_mx(want["q_row"], want["s_row"])
+    assert np.array_equal(host(back.view(torch.int16)).view(np.uint16), ref)
+    assert torch.equal(back.view(torch.int16), back2.view(torch.int16))
+
+
+# ----------------------------------------------------- SwiGLU + quantize --
+
+def _swiglu_check(h_dev, offsets=None, floor=False):
+    flags = m.MX_SCALE_FLOOR if floor else 0
+    off_d = None if offsets is None else torch.from_numpy(offsets).to(device())
+    q, s = m.fp8_swiglu_quantize_mx(h_dev, offsets=off_d, flags=flags)
+    assert_ok()
+    hb = workloads.bits(h_dev)
+    c, lo, hi = bf16_candidates(oracle.swiglu(hb))
+    fl = oracle.SCALE_FLOOR if floor else 0
+    if offsets is None:
+        want = oracle.quantize_mx(c, oracle.ROWWISE | fl)
+        q_exp, s_exp = want["q_row"], want["s_row"]
+    else:
+        q_exp, s_exp = oracle.quantize_mx_grouped(c, offsets, oracle.ROWWISE | fl)
+    return check_set_quantization(host(q), host(s), lo, hi, q_exp, s_exp, offsets, floor)
+
+
+@pytest.mark.parametrize("rows,f", SHAPES)
+@pytest.mark.parametrize("floor", [False, True])
+def test_swiglu_quantize_plain(rows, f, floor):
+    rng = np.random.default_rng(rows + f)
+    h = oracle.bf16_round(rng.standard_normal((rows, 2 * f)) * 3)
+    _swiglu_check(to_dev_bf16(h), floor=floor)
+
+
+def test_swiglu_quantize_extremes():
+    """Gates far below -80 (double branch), tiny gates (the (g u) sigma
+    order), huge ups, zeros of both signs and values that underflow BF16."""
+    rng = np.random.default_rng(21)
+    rows, f = 256, 128
+    g = rng.standard_normal((rows, f)) * np.exp(rng.uniform(-100, 6, (rows, 1)))
+    u = rng.standard_normal((rows, f)) * np.exp(rng.uniform(-60, 60, (rows, 1)))
+    g[:8] = -rng.uniform(80, 300, (8, f))
+    g[8, :16] = 0.0
+    u[9, :16] = -0.0
+    g[10] = np.ldexp(rng.uniform(1, 2, f), rng.integers(-133, -100, f))
+    h = oracle.bf16_round(np.concatenate([g, u], axis=1))
+    _swiglu_check(to_dev_bf16(h))
+
+
+@pytest.mark.parametrize("counts", GROUP_COUNTS)
+def test_swiglu_quantize_grouped(counts):
+    off = _offsets(counts)
+    rng = np.random.default_rng(sum(counts))
+    h = oracle.bf16_round(rng.standard_normal((int(off[-1]), 2 * 96)) * 2)
+    _swiglu_check(to_dev_bf16(h), offsets=off)
+
+
+def test_swiglu_quantize_full_size():
+    """The grouped workload's up/gate output (262144 x 1024, 64 experts)."""
+    w = workloads.swiglu_hidden(seed=0, device=device())
+    amb = _swiglu_check(w["H"], offsets=w["offsets"])
+    assert amb < 0.05 * (w["H"].shape[0] * 512 // 32)  # near-ties are rare
+
+
+# ------------------------------------------- route weighting + quantize --
+
+def _weighted_check(dy, tok, wt, offsets=None, floor=False):
+    off_d = None if offsets is None else torch.from_numpy(offsets).to(device())
+    q, s = m.fp8_route_weight_quantize_mx(dy, torch.from_numpy(tok).to(device()),
+                                          torch.from_numpy(wt).to(device()), offsets=off_d,
+                                          flags=m.MX_SCALE_FLOOR if floor else 0)
+    st = m.mxfp8_last_device_status()
+    g = oracle.route_weight(workloads.bits(dy), tok, wt)
+    fl = oracle.SCALE_FLOOR if floor else 0
+    if offsets is None:
+        want = oracle.quantize_mx(g, oracle.ROWWISE | fl)
+        q_exp, s_exp = want["q_row"], want["s_row"]
+    else:
+        q_exp, s_exp = oracle.quantize_mx_grouped(g, offsets, oracle.ROWWISE | fl)
+    assert np.array_equal(host(q), q_exp)
+    assert np.array_equal(host(s)[: s_exp.size], s_exp)
+    return st
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("floor", [False, True])
+def test_route_weight_quantize_plain(rows, cols, floor):
+    rng = np.random.default_rng(rows * 3 + cols)
+    tokens = max(1, rows // 3)
+    dy = to_dev_bf16(oracle.bf16_round(rng.standard_normal((tokens, cols)) *
+                                       np.exp(rng.uniform(-25, 5, (tokens, 1)))))
+    tok = rng.integers(0, tokens, rows).astype(np.int32)
+    wt = rng.uniform(0, 1, rows).astype(np.float32)
+    assert _weighted_check(dy, tok, wt, floor=floor) == m.MXFP8_OK
+
+
+def test_route_weight_quantize_extremes():
+    """Exact-product ties, products below fp32's normal range (the double
+    branch), overflow to Inf, zero weights, and an out-of-range token index
+    (recorded; that row quantizes as zeros)."""
+    rng = np.random.default_rng(22)
+    tokens, cols, rows = 8, 64, 40
+    dy = oracle.bf16_round(rng.standard_normal((tokens, cols)) * np.exp(rng.uniform(-80, 80, (tokens, 1))))
+    dy[0, :8] = [0x3F80, 0xBF80, 0x0001, 0x8001, 0x7F7F, 0x0080, 0x3F81, 0x0000]
+    tok = rng.integers(0, tokens, rows).astype(np.int32)
+    tok[:6] = 0
+    wt = rng.uniform(0, 1, rows).astype(np.float32)
+    wt[:6] = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2.0 ** -30, 1.5, 0.0, 2.0 ** -126], np.float32)
+    tok[7] = tokens  # out of range
+    st = _weighted_check(to_dev_bf16(dy), tok, wt)
+    assert st == m.MXFP8_ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("counts", GROUP_COUNTS)
+def test_route_weight_quantize_grouped(counts):
+    off = _offsets(counts)
+    rows = int(off[-1])
+    rng = np.random.default_rng(rows)
+    tokens = max(1, rows // 4)
+    dy = to_dev_bf16(oracle.bf16_round(rng.standard_normal((tokens, 224)) * 1e-3))
+    tok = rng.integers(0, tokens, rows).astype(np.int32)
+    wt = rng.uniform(0, 1, rows).astype(np.float32)
+    assert _weighted_check(dy, tok, wt, offsets=off) == m.MXFP8_OK
+
+
+def test_route_weight_quantize_full_size():
+    """Combine backward of 32768 tokens x 2048, top-8 of 64 experts."""
+    w = workloads.combine_backward(seed=0, device=device())
+    assert _weighted_check(w["dY"], w["row_token"], w["row_weight"], offsets=w["offsets"]) == m.MXFP8_OK

@@ -7,6 +7,7 @@ all BF16 bit patterns, closed forms and invariants of the method, and numpy
 matmuls of operands dequantized without the oracle.
 """
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -612,3 +613,104 @@ def test_dequantize_roundtrip_and_specials():
     assert out[0, 1] == 0x3F80                  # 1.0
     assert np.all(out[1] == 0x7F80)             # +Inf
     assert np.all(out[2] == 0x0001)
+
+
+def test_dequantize_grouped_is_plain_per_group():
+    """Each group's scale rows are whole 128-row tiles of the grouped array,
+    so the grouped dequantization of group g equals the plain one of its rows
+    with that slice of tiles."""
+    rng = np.random.default_rng(14)
+    counts = np.array([0, 130, 5, 0, 256, 1])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows, cols = int(off[-1]), 96
+    x = oracle.bf16_round(rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-8, 8, (rows, 1))))
+    q, s = oracle.quantize_mx_grouped(x, off)
+    got = oracle.dequantize_mx_grouped(q, s, off)
+    nkc = (cols + 127) // 128
+    padded = 0
+    for g in range(counts.size):
+        m = int(counts[g])
+        if m:
+            tiles = (m + 127) // 128
+            sl = s[padded // 128 * nkc * 512:(padded // 128 + tiles) * nkc * 512]
+            want = oracle.dequantize_mx(q[off[g]:off[g + 1]], sl)
+            assert np.array_equal(got[off[g]:off[g + 1]], want)
+        padded += (m + 127) // 128 * 128
+
+
+# -------------------------------------------------------------- SwiGLU --
+
+def test_swiglu_vs_torch_silu():
+    """FP64 g sigma(g) u against torch's float64 SiLU times u, plus the
+    identity silu(g) - silu(-g) = g and sigma(g) = 1 in FP64 for g >= 40."""
+    rng = np.random.default_rng(15)
+    rows, f = 64, 96
+    h = oracle.bf16_round(rng.standard_normal((rows, 2 * f)) * 4)
+    y = oracle.swiglu(h)
+    hv = oracle.bf16_decode(h)
+    g, u = torch.from_numpy(hv[:, :f]), torch.from_numpy(hv[:, f:])
+    want = (torch.nn.functional.silu(g) * u).numpy()
+    np.testing.assert_allclose(y, want, rtol=1e-15, atol=0)  # a few FP64 ulps
+    # odd part of SiLU: silu(g) - silu(-g) = g
+    gg = hv[:, :f]
+    ones = oracle.bf16_round(np.ones_like(gg))
+    pos = oracle.swiglu(np.concatenate([h[:, :f], ones], axis=1))
+    neg = oracle.swiglu(np.concatenate([h[:, :f] ^ np.uint16(0x8000), ones], axis=1))
+    np.testing.assert_allclose(pos - neg, gg, rtol=1e-15, atol=1e-300)
+    # saturated gate: y = g u exactly; far negative gate: |y| below every BF16 value
+    big = oracle.bf16_round(np.array([[40.0, -3.5], [100.0, 7.0], [-200.0, 1e30]]))
+    hb = np.stack([big[:, 0], big[:, 1]], axis=1)
+    yb = oracle.swiglu(hb)[:, 0]
+    assert yb[0] == 40.0 * -3.5 and yb[1] == 700.0
+    assert yb[2] < 0 and abs(yb[2]) < 2.0 ** -134
+
+
+# ------------------------------------------------------- route weighting --
+
+def _bf16_neighbours_table():
+    bits = all_bf16_bits()
+    vals = oracle.bf16_decode(bits)
+    keep = np.isfinite(vals) & ~((bits == 0x8000))
+    order = np.argsort(vals[keep], kind="stable")
+    return vals[keep][order], bits[keep][order]
+
+
+def _correctly_rounded_bf16(v: Fraction, table) -> int:
+    """RNE of an exact rational to BF16 by comparing the two neighbours."""
+    vals, bits = table
+    top = Fraction(2) ** 128 - Fraction(2) ** 119  # halfway to the next binade: rounds to Inf
+    if v >= top:
+        return 0x7F80
+    if v <= -top:
+        return 0xFF80
+    i = int(np.searchsorted(vals, float(v), side="left"))
+    cands = [j for j in (i - 1, i, i + 1) if 0 <= j < vals.size]
+    best = min(cands, key=lambda j: (abs(Fraction(vals[j]) - v), int(bits[j]) & 1))
+    b = int(bits[best])
+    if vals[best] == 0.0:
+        b = 0x8000 if v < 0 else 0x0000
+    return b
+
+
+def test_route_weight_is_one_rounding_of_the_exact_product():
+    rng = np.random.default_rng(16)
+    table = _bf16_neighbours_table()
+    tokens, cols, rows = 12, 64, 40
+    dy = oracle.bf16_round(rng.standard_normal((tokens, cols)) * np.exp(rng.uniform(-30, 30, (tokens, 1))))
+    # exact midpoints: 1 * (1 + 2^-8) and 1 * (1 + 3 * 2^-8) tie to the even neighbour
+    dy[0, :4] = [0x3F80, 0x3F80, 0xBF80, 0x0001]
+    tok = rng.integers(0, tokens, rows).astype(np.int32)
+    tok[:3] = 0
+    w = rng.uniform(0, 1, rows).astype(np.float32)
+    w[:3] = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2.0 ** -20], np.float32)
+    tok[3] = -1  # out of range: zero row
+    got = oracle.route_weight(dy, tok, w)
+    assert list(got[0, :4]) == [0x3F80, 0x3F80, 0xBF80, 0x0001] and got[1, 0] == 0x3F82
+    assert np.all(got[3] == 0)
+    dyv = oracle.bf16_decode(dy)
+    for i in range(rows):
+        if tok[i] < 0:
+            continue
+        for c in range(0, cols, 7):
+            v = Fraction(float(w[i])) * Fraction(float(dyv[tok[i], c]))
+            assert got[i, c] == _correctly_rounded_bf16(v, table), (i, c)

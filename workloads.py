@@ -20,6 +20,16 @@ Workloads (one GB300; shapes from the benchmark definition):
              W 4096 x 4096 N(0, 0.02); X 8192 x 4096 N(0, 1)
   grouped    64 experts, counts ~ Multinomial(32768 * 8, p_e ~ e^-1.1);
              dispatched X (262144 x 2048) N(0, 1); W 64 x 1024 x 2048 N(0, 0.02)
+
+Routed-path conversions (the grouped workload's surroundings):
+  swiglu_hidden     the up/gate output of the grouped workload, H 262144 x 1024
+                    N(0, 1) read as gate | up halves of 512, with the grouped
+                    workload's expert offsets
+  combine_backward  dY 32768 x 2048 with |v| = 10^U(-8, -2) and a random sign;
+                    every token routed to 8 distinct experts of 64 drawn with
+                    p_e ~ e^-1.1 (Gumbel top-k, without replacement), rows
+                    sorted by expert then token; route weights = softmax of
+                    8 N(0, 1) logits per token, fp32
 """
 from __future__ import annotations
 
@@ -130,10 +140,45 @@ def grouped(seed=0, device="cpu", tokens=32768, top_k=8, experts=64, hidden=2048
             "offsets": offsets_from_counts(counts)}
 
 
+def swiglu_hidden(seed=0, device="cpu", tokens=32768, top_k=8, experts=64, ffn=1024,
+                  zipf_s=1.1):
+    counts = zipf_counts(tokens * top_k, experts, zipf_s, seed, 3)  # the grouped workload's
+    total = int(counts.sum())
+    return {"H": normal((total, ffn), 1.0, seed, 4, device),
+            "counts": counts, "offsets": offsets_from_counts(counts)}
+
+
+def routing(seed=0, tokens=32768, top_k=8, experts=64, zipf_s=1.1):
+    """Token -> expert assignments (top_k distinct experts per token, Gumbel
+    top-k on log p_e) sorted by expert then token, with softmax route weights."""
+    rng = np.random.Generator(np.random.PCG64(_stream(seed, 5)))
+    logp = -zipf_s * np.log(np.arange(1, experts + 1, dtype=np.float64))
+    keys = logp[None, :] + rng.gumbel(size=(tokens, experts))
+    chosen = np.argpartition(-keys, top_k - 1, axis=1)[:, :top_k]
+    logits = rng.standard_normal((tokens, top_k))
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w /= w.sum(axis=1, keepdims=True)
+    tok = np.repeat(np.arange(tokens, dtype=np.int64), top_k)
+    exp_ = chosen.reshape(-1)
+    order = np.lexsort((tok, exp_))
+    counts = np.bincount(exp_, minlength=experts).astype(np.int64)
+    return {"row_token": tok[order].astype(np.int32),
+            "row_weight": w.reshape(-1)[order].astype(np.float32),
+            "counts": counts, "offsets": offsets_from_counts(counts)}
+
+
+def combine_backward(seed=0, device="cpu", tokens=32768, d_model=2048, **kw):
+    r = routing(seed=seed, tokens=tokens, **kw)
+    r["dY"] = log_uniform_signed((tokens, d_model), 1e-8, 1e-2, seed, 6, device)
+    return r
+
+
 WORKLOADS = {
     "mx256": (mx256, "MXFP8 quantize+GEMM M=N=K=256"),
     "tensor4096": (tensor4096, "per-tensor FP8 forward GEMM M=N=K=4096, 1% outlier columns"),
     "mlp_up": (mlp_up, "MXFP8 MLP up-projection X[8192x4096] . W[16384x4096]^T"),
     "backward": (backward, "MXFP8 dgrad + wgrad of a 4096->4096 linear over 8192 tokens"),
     "grouped": (grouped, "MXFP8 grouped expert GEMM, 64 experts top-8 Zipf(1.1), 2048->1024"),
+    "swiglu_hidden": (swiglu_hidden, "fused SwiGLU + MX quantize of the grouped up/gate output"),
+    "combine_backward": (combine_backward, "fused route weighting + MX gradient quantize"),
 }
