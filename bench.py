@@ -45,6 +45,7 @@ import torch  # noqa: E402
 METRIC = "MXFP8 GEMM TFLOP/s incl. quantize (vs 4500 FP8 peak); quantize GB/s vs HBM"
 UNIT = "TFLOP/s"
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+SWIGLU_Q_BYTES = 4 + 1 + 1 / 32     # read gate and up (BF16), write E4M3 + scale per output
 MX_ROW_BYTES = 2 + 1 + 1 / 32  # algorithmic bytes per value: read BF16, write E4M3 + E8M0/32
 MX_BOTH_BYTES = 2 + 2 * (1 + 1 / 32)
 TENSOR_Q_BYTES = 3.0
@@ -338,6 +339,8 @@ def hot_path_rows(m, dev, steps, warmup):
         "largest_group_rows": int(np.max(w["counts"])), "launches_per_step": 3}
     del Xg, Wg, qa, qwg, Cg, w
 
+    rows.update(routed_conversion_rows(m, dev, steps, warmup))
+
     # 256^3, launch-bound
     w = workloads.mx256(seed=0, device=dev)
     A, B = w["A"], w["B"]
@@ -353,6 +356,78 @@ def hot_path_rows(m, dev, steps, warmup):
     ms, _ = _time_steps(small, max(steps, 50), warmup)
     rows["mx_256"] = {"ms_per_step": ms, "tflops_incl_quantize": 2.0 * 256 ** 3 / ms / 1e9,
                       "note": "launch-bound; not graded against a roofline", "launches_per_step": 3}
+    return rows
+
+
+def routed_conversion_rows(m, dev, steps, warmup):
+    """The conversions around the grouped GEMM, each one launch on inputs
+    larger than L2: global dequantization of the dispatched activation (the
+    routed Wgrad operand), the fused SwiGLU + quantize of the up/gate output,
+    and the fused route-weight + gradient quantize of combine backward."""
+    import workloads
+    u8 = dict(dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    L = m.lib()
+    rows = {}
+
+    w = workloads.grouped(seed=0, device=dev)
+    off = torch.from_numpy(w["offsets"]).to(dev)
+    X = w["X"]
+    del w
+    total, K, G = X.shape[0], X.shape[1], 64
+    qa = torch.empty((total, K), **u8)
+    sa = torch.empty(m.mxfp8_grouped_scale_bytes(total, K, G), **u8)
+    _ok(L.fp8_quantize_mx_grouped(X.data_ptr(), total, K, K, off.data_ptr(), G, 0,
+                                  qa.data_ptr(), sa.data_ptr(), st))
+
+    def dq(timer):
+        e = timer.mark("k") if timer else None
+        _ok(L.fp8_dequantize_mx(qa.data_ptr(), sa.data_ptr(), total, K, off.data_ptr(), G,
+                                X.data_ptr(), K, st))
+        if e: e.record()
+    ms, _ = _time_steps(dq, steps, warmup)
+    rows["dequantize_grouped_262144x2048"] = {
+        "ms_per_step": ms, "gbs": total * K * MX_ROW_BYTES / ms / 1e6,
+        "bytes_per_value": MX_ROW_BYTES, "launches_per_step": 1}
+    del qa, sa, X
+
+    w = workloads.swiglu_hidden(seed=0, device=dev)
+    H = w["H"]
+    off = torch.from_numpy(w["offsets"]).to(dev)
+    total, F = H.shape[0], H.shape[1] // 2
+    qh = torch.empty((total, F), **u8)
+    sh = torch.empty(m.mxfp8_grouped_scale_bytes(total, F, G), **u8)
+
+    def sw(timer):
+        _ok(L.fp8_swiglu_quantize_mx(H.data_ptr(), total, F, 2 * F, off.data_ptr(), G, 0,
+                                     qh.data_ptr(), sh.data_ptr(), st))
+    ms, _ = _time_steps(sw, steps, warmup)
+    rows["swiglu_quantize_262144x512"] = {
+        "ms_per_step": ms, "gbs": total * F * SWIGLU_Q_BYTES / ms / 1e6,
+        "bytes_per_value": SWIGLU_Q_BYTES, "launches_per_step": 1}
+    del H, qh, sh, w
+
+    w = workloads.combine_backward(seed=0, device=dev)
+    dY = w["dY"]
+    tok = torch.from_numpy(w["row_token"]).to(dev)
+    wt = torch.from_numpy(w["row_weight"]).to(dev)
+    off = torch.from_numpy(w["offsets"]).to(dev)
+    T, D = dY.shape
+    R = tok.numel()
+    qg = torch.empty((R, D), **u8)
+    sg = torch.empty(m.mxfp8_grouped_scale_bytes(R, D, G), **u8)
+
+    def rw(timer):
+        _ok(L.fp8_route_weight_quantize_mx(dY.data_ptr(), T, D, tok.data_ptr(), wt.data_ptr(), R, D,
+                                           off.data_ptr(), G, 0, qg.data_ptr(), sg.data_ptr(), st))
+    ms, _ = _time_steps(rw, steps, warmup)
+    unique = T * D * 2 + R * D * (1 + 1 / 32) + R * 8
+    rows["route_weight_quantize_262144x2048"] = {
+        "ms_per_step": ms, "gbs": unique / ms / 1e6,
+        "bytes": "dY read once + payload and scales written + token/weight per row",
+        "gbs_if_gathered_rows_counted": (R * D * (2 + 1 + 1 / 32) + R * 8) / ms / 1e6,
+        "launches_per_step": 1}
+    del dY, qg, sg, w
     return rows
 
 

@@ -282,10 +282,10 @@ mxfp8_status fp8_dequantize_mx(const void* q, const void* s, int64_t rows, int64
  *  q, s    outputs as fp8_quantize_mx's rowwise ones for a rows x f operand
  *          (or the group-padded scale array).
  * The hidden value a = bf16_RNE(g * sigma(g) * u), sigma(g) = 1/(1+e^-g), is
- * what an unfused SwiGLU would store in BF16; it is formed in fp32 (double
- * below g = -80) within 1.25 * 2^-21 relative of the exact value, so a is the
- * correctly rounded BF16 value except within that distance of a rounding
- * midpoint, where it may be the neighbour.  a is then quantized by the MX rule
+ * what an unfused SwiGLU would store in BF16; it is formed in fp32 within
+ * 14 * 2^-24 relative of the exact value (in double, rounded once, for
+ * g < -80), so a is the correctly rounded BF16 value except within that
+ * distance of a rounding midpoint, where it may be the neighbour.  a is then quantized by the MX rule
  * of fp8_quantize_mx (flags: MX_SCALE_FLOOR optional, rowwise implied) and
  * never written.  Requirements: f % 32 == 0, ld % 8 == 0, pointers 16-byte
  * aligned.

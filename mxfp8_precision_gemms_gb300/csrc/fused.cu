@@ -120,45 +120,73 @@ __global__ void __launch_bounds__(kThreads)
 
 // ------------------------------------------------------ SwiGLU + Q ------
 
-__device__ __forceinline__ uint32_t bf16_bits_rn(float v) {
-    uint16_t r;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t bf16_bits_rn(double v) {
     return __bfloat16_as_ushort(__double2bfloat16(v));
 }
 
-// bf16_RNE(g sigma(g) u), sigma(g) = 1 / (1 + e^-g).  For g >= -80 the value
-// is formed in fp32 from e^-|g| (never overflows; a normal number), with
-// sigma = 1/(1+t) for g >= 0 and t/(1+t) below 0; with CUDA's expf error of
-// at most 2 ulp the fp32 value is within 1.25 * 2^-21 relative of the exact
-// one (plus an absolute 2^-149 where the product underflows), so the BF16
-// result is the correctly rounded one unless the exact value lies that close
-// to a rounding midpoint, where it may be the neighbour.  The product is
-// taken as (g sigma) u, or (g u) sigma when |g| < 2^-100 so that g sigma never
-// loses bits to fp32 underflow.  Below -80, where e^g leaves fp32's normal
-// range, the value is formed in double and rounded once.
-__device__ __forceinline__ uint32_t swiglu_bf16(float g, float u) {
-    if (!(g >= -80.f)) {  // also NaN
-        const double gd = g;
-        const double e = exp(gd);
-        return bf16_bits_rn(gd * (e / (1.0 + e)) * static_cast<double>(u));
-    }
+// Two fp32 values rounded to BF16 (RNE), `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// g sigma(g) u in fp32, sigma(g) = 1 / (1 + e^-g), branch free, for
+// g >= -80.  t = e^-|g| (CUDA's expf, 2 ulp) is a normal number there;
+// r = 1/(1+t) (__fdividef, 2 ulp for divisors in [1, 2]); n = max(g, g t)
+// is g for g >= 0 (exact) and g e^g below; y = (n u) r.  The error is at most
+// 14 * 2^-24 = 1.75 * 2^-21 relative, plus an absolute 2^-149 where n u
+// underflows (for g >= 0, n u = g u is exact unless it underflows, which
+// also covers BF16-subnormal gates; n u cannot overflow for g < 0).  The
+// BF16 rounding of y is therefore the correctly rounded value unless the
+// exact value lies that close to a rounding midpoint, where it may be the
+// neighbour.  NaN propagates; g < -80 (e^g leaves fp32's normal range,
+// including -Inf) takes the exact path below.
+__device__ __forceinline__ float swiglu_fast(float g, float u) {
     const float t = expf(-fabsf(g));
-    const float sig = __fdiv_rn(g >= 0.f ? 1.f : t, __fadd_rn(1.f, t));
-    const float y = fabsf(g) < 0x1p-100f ? __fmul_rn(__fmul_rn(g, u), sig)
-                                         : __fmul_rn(__fmul_rn(g, sig), u);
-    return bf16_bits_rn(y);
+    const float r = __fdividef(1.f, __fadd_rn(1.f, t));
+    const float n = fmaxf(g, __fmul_rn(g, t));
+    return __fmul_rn(__fmul_rn(n, u), r);
+}
+
+// Any of 8 packed BF16 gates below -80 (bits above 0xC2A0 as unsigned:
+// negative with magnitude above 80, -Inf, negative NaN).
+__device__ __forceinline__ bool swiglu_rare8(const uint4& g8) {
+    const uint32_t m = max_u16x2(max_u16x2(g8.x, g8.y), max_u16x2(g8.z, g8.w));
+    return max(m & 0xFFFFu, m >> 16) > 0xC2A0u;
+}
+
+// The same value formed in double and rounded once to BF16.
+__device__ __noinline__ uint32_t swiglu_bf16_exact(float g, float u) {
+    const double gd = g;
+    const double e = exp(gd < 0.0 ? gd : -gd);
+    const double sig = gd < 0.0 ? e / (1.0 + e) : 1.0 / (1.0 + e);
+    return bf16_bits_rn(gd * sig * static_cast<double>(u));
+}
+
+// All 8 values of a chunk with a gate off the fast path, in double.
+__device__ __noinline__ uint4 swiglu8_exact(uint4 g8, uint4 u8) {
+    uint4 v;
+    uint32_t* vv = reinterpret_cast<uint32_t*>(&v);
+    const uint32_t* gg = reinterpret_cast<const uint32_t*>(&g8);
+    const uint32_t* uu = reinterpret_cast<const uint32_t*>(&u8);
+    for (int i = 0; i < 4; ++i) {
+        vv[i] = swiglu_bf16_exact(bf16_lo(gg[i]), bf16_lo(uu[i])) |
+                (swiglu_bf16_exact(bf16_hi(gg[i]), bf16_hi(uu[i])) << 16);
+    }
+    return v;
 }
 
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2) {
-    return swiglu_bf16(bf16_lo(g2), bf16_lo(u2)) | (swiglu_bf16(bf16_hi(g2), bf16_hi(u2)) << 16);
+    return bf16x2_rn(swiglu_fast(bf16_lo(g2), bf16_lo(u2)), swiglu_fast(bf16_hi(g2), bf16_hi(u2)));
 }
 
+// Column tiles per CTA of the fused row producers: the tile-row lookup (and,
+// for gathers, the row indices) are paid once per CTA.
+constexpr int kColTilesPerCta = 4;
+
 template <bool FLOOR, bool GROUPED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     swiglu_quant_kernel(const uint16_t* __restrict__ h, int64_t rows, int64_t f, int64_t ld,
                         const int32_t* offsets, int groups, uint8_t* __restrict__ q,
                         uint8_t* __restrict__ s, int64_t nkc) {
@@ -166,55 +194,71 @@ __global__ void __launch_bounds__(kThreads)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int seg = tid & 15;
-    const int64_t col = static_cast<int64_t>(blockIdx.y) * kTile + seg * 8;
-    uint4 gv[8], uv[8];
+    for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
+        const int64_t col = ct * kTile + seg * 8;
+        uint4 gv[8], uv[8];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int64_t row = row_begin + it * 16 + (tid >> 4);
-        if (row < row_end && col < f) {
-            gv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + col));
-            uv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + f + col));
-        } else {
-            gv[it] = make_uint4(0u, 0u, 0u, 0u);
-            uv[it] = make_uint4(0u, 0u, 0u, 0u);
+        for (int it = 0; it < 8; ++it) {
+            const int64_t row = row_begin + it * 16 + (tid >> 4);
+            if (row < row_end && col < f) {
+                gv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + col));
+                uv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + f + col));
+            } else {
+                gv[it] = make_uint4(0u, 0u, 0u, 0u);
+                uv[it] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
-    }
-    uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + blockIdx.y) * 512;
+        uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = it * 16 + (tid >> 4);
-        const int64_t row = row_begin + r;
-        const bool in = row < row_end && col < f;
-        uint4 v;
-        v.x = swiglu2(gv[it].x, uv[it].x);
-        v.y = swiglu2(gv[it].y, uv[it].y);
-        v.z = swiglu2(gv[it].z, uv[it].z);
-        v.w = swiglu2(gv[it].w, uv[it].w);
-        mx_row_step<FLOOR>(v, r, in ? q + row * f + col : nullptr, s_tile);
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 16 + (tid >> 4);
+            const int64_t row = row_begin + r;
+            const bool in = row < row_end && col < f;
+            uint4 v;
+            if (in && swiglu_rare8(gv[it])) {
+                v = swiglu8_exact(gv[it], uv[it]);
+            } else {
+                v.x = swiglu2(gv[it].x, uv[it].x);
+                v.y = swiglu2(gv[it].y, uv[it].y);
+                v.z = swiglu2(gv[it].z, uv[it].z);
+                v.w = swiglu2(gv[it].w, uv[it].w);
+            }
+            mx_row_step<FLOOR>(v, r, in ? q + row * f + col : nullptr, s_tile);
+        }
     }
 }
 
 // ------------------------------------------- route weighting + Q --------
 
-// bf16_RNE(x w) of a BF16 x and an fp32 w, rounded once from the exact
-// product.  The product has at most 32 significant bits, so it is first
-// rounded to fp32 toward zero with the lowest bit forced to 1 when inexact
-// (round-to-odd; the FMA residual is exact for normal products), and the
-// RNE rounding of that to BF16, 16 bits shorter, equals the RNE rounding of
-// the exact product.  Products below fp32's normal range are formed in
-// double (exact there) and rounded once.
-__device__ __forceinline__ uint32_t weighted_bf16(float x, float w) {
-    const float p = __fmul_rz(x, w);
-    if (fabsf(p) < 0x1p-126f) {
-        return bf16_bits_rn(static_cast<double>(x) * static_cast<double>(w));
-    }
-    uint32_t b = __float_as_uint(p);
-    if (isfinite(p) && __fmaf_rn(x, w, -p) != 0.f) b |= 1u;
-    return bf16_bits_rn(__uint_as_float(b));
+// bf16_RNE(x w) of a BF16 x and an fp32 w, equal to one rounding of the
+// exact product: p = fp32_RN(x w) is monotone in the exact value and every
+// BF16 rounding midpoint is an fp32 number, so the BF16 rounding of p agrees
+// with that of the exact product unless p lands exactly on a midpoint (its
+// low 16 bits are 0x8000; this covers the fp32-subnormal range too, where
+// fp32 still has 16 more fraction bits than BF16).  `mid` (a running
+// minimum) becomes 0 for such a product, and the chunk is redone exactly in
+// double.  Overflow, Inf and NaN follow the
+// fp32 product, which agrees with the exact one in BF16.
+__device__ __forceinline__ uint32_t weighted2(uint32_t x2, float w, uint32_t& mid) {
+    const float p0 = __fmul_rn(bf16_lo(x2), w);
+    const float p1 = __fmul_rn(bf16_hi(x2), w);
+    // (bits << 16) + 2^31 is zero exactly when the low half is 0x8000
+    mid = min(mid, min(__float_as_uint(p0) * 65536u + 0x80000000u,
+                       __float_as_uint(p1) * 65536u + 0x80000000u));
+    return bf16x2_rn(p0, p1);
 }
 
-__device__ __forceinline__ uint32_t weighted2(uint32_t x2, float w) {
-    return weighted_bf16(bf16_lo(x2), w) | (weighted_bf16(bf16_hi(x2), w) << 16);
+// 8 products formed exactly in double and rounded once.
+__device__ __noinline__ uint4 weighted8_exact(uint4 x8, float w) {
+    uint4 v;
+    uint32_t* vv = reinterpret_cast<uint32_t*>(&v);
+    const uint32_t* xx = reinterpret_cast<const uint32_t*>(&x8);
+    const double wd = w;
+    for (int i = 0; i < 4; ++i) {
+        vv[i] = bf16_bits_rn(static_cast<double>(bf16_lo(xx[i])) * wd) |
+                (bf16_bits_rn(static_cast<double>(bf16_hi(xx[i])) * wd) << 16);
+    }
+    return v;
 }
 
 template <bool FLOOR, bool GROUPED>
@@ -227,48 +271,59 @@ __global__ void __launch_bounds__(kThreads)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int seg = tid & 15;
-    const int64_t col = static_cast<int64_t>(blockIdx.y) * kTile + seg * 8;
-    uint4 xv[8];
+    // token and weight of each of this thread's rows, once for all column tiles
+    const int32_t* tk_base = row_token + row_begin;
+    int32_t tk[8];
     float wv[8];
     bool bad = false;
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
-        const int64_t row = row_begin + it * 16 + (tid >> 4);
-        xv[it] = make_uint4(0u, 0u, 0u, 0u);
-        wv[it] = 0.f;
-        if (row < row_end && col < cols) {
-            const int64_t t = __ldg(row_token + row);
-            if (t >= 0 && t < tokens) {
-                xv[it] = __ldcs(reinterpret_cast<const uint4*>(dy + t * ld + col));
-                wv[it] = __ldg(row_weight + row);
-            } else {
-                bad = true;
-            }
-        }
-    }
-    if (bad) record_status(MXFP8_ERR_DEVICE_CHECK);
-    uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + blockIdx.y) * 512;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
         const int r = it * 16 + (tid >> 4);
-        const int64_t row = row_begin + r;
-        const bool in = row < row_end && col < cols;
-        uint4 v;
-        v.x = weighted2(xv[it].x, wv[it]);
-        v.y = weighted2(xv[it].y, wv[it]);
-        v.z = weighted2(xv[it].z, wv[it]);
-        v.w = weighted2(xv[it].w, wv[it]);
-        mx_row_step<FLOOR>(v, r, in ? q + row * cols + col : nullptr, s_tile);
+        const bool in = row_begin + r < row_end;
+        const int32_t t = in ? __ldg(tk_base + r) : -1;
+        const bool valid = t >= 0 && t < tokens;
+        bad |= in && !valid;
+        tk[it] = valid ? t : -1;
+        wv[it] = valid ? __ldg(row_weight + row_begin + r) : 0.f;
+    }
+    if (bad && blockIdx.y == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
+    for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
+        const int64_t col = ct * kTile + seg * 8;
+        uint4 xv[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            // cached load: each token row is gathered by several dispatched rows
+            xv[it] = (tk[it] >= 0 && col < cols)
+                         ? __ldg(reinterpret_cast<const uint4*>(dy + static_cast<int64_t>(tk[it]) * ld + col))
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 16 + (tid >> 4);
+            const int64_t row = row_begin + r;
+            const bool in = row < row_end && col < cols;
+            uint4 v;
+            uint32_t mid = 0xFFFFFFFFu;
+            v.x = weighted2(xv[it].x, wv[it], mid);
+            v.y = weighted2(xv[it].y, wv[it], mid);
+            v.z = weighted2(xv[it].z, wv[it], mid);
+            v.w = weighted2(xv[it].w, wv[it], mid);
+            if (mid == 0u) v = weighted8_exact(xv[it], wv[it]);
+            mx_row_step<FLOOR>(v, r, in ? q + row * cols + col : nullptr, s_tile);
+        }
     }
 }
 
 // Grid of a tile walk: plain operands have ceil(rows/128) row tiles; a
 // group-padded one at most floor(rows/128) + groups.
-bool tile_grid(int64_t rows, int64_t cols, bool grouped, int groups, dim3* grid) {
+bool tile_grid(int64_t rows, int64_t cols, bool grouped, int groups, dim3* grid,
+               int col_tiles_per_cta = 1) {
     const int64_t row_tiles = grouped ? rows / kTile + groups : (rows + kTile - 1) / kTile;
     const int64_t col_tiles = (cols + kTile - 1) / kTile;
-    if (row_tiles > 0x7FFFFFFF || col_tiles > 65535) return false;
-    *grid = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
+    const int64_t col_ctas = (col_tiles + col_tiles_per_cta - 1) / col_tiles_per_cta;
+    if (row_tiles > 0x7FFFFFFF || col_ctas > 65535) return false;
+    *grid = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_ctas));
     return true;
 }
 
@@ -294,7 +349,8 @@ cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t st)
     dim3 grid;
     const bool grouped = a.offsets != nullptr;
     const bool fl = a.flags & MX_SCALE_FLOOR;
-    if (!tile_grid(a.rows, a.f, grouped, a.groups, &grid)) return cudaErrorInvalidValue;
+    if (!tile_grid(a.rows, a.f, grouped, a.groups, &grid, kColTilesPerCta))
+        return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.f + kTile - 1) / kTile;
 #define MXFP8_SWIGLU(FL, GR) \
@@ -313,7 +369,8 @@ cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t
     dim3 grid;
     const bool grouped = a.offsets != nullptr;
     const bool fl = a.flags & MX_SCALE_FLOOR;
-    if (!tile_grid(a.rows, a.cols, grouped, a.groups, &grid)) return cudaErrorInvalidValue;
+    if (!tile_grid(a.rows, a.cols, grouped, a.groups, &grid, kColTilesPerCta))
+        return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
 #define MXFP8_WEIGHTED(FL, GR)                                                               \

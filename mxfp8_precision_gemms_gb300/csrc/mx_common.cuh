@@ -41,11 +41,18 @@ __device__ __forceinline__ float inv_scale(uint32_t byte) {
     return __uint_as_float((254u - byte) << 23);
 }
 
+// Per-half unsigned 16-bit maximum (native on sm_90 and later).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Largest BF16 magnitude bits among the 8 values of a 16-byte vector.
 __device__ __forceinline__ uint32_t amax8(const uint4& v) {
-    uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    uint32_t m = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.z & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.w & 0x7FFF7FFFu);
     return max(m & 0xFFFFu, m >> 16);
 }
 

@@ -1,12 +1,13 @@
 """Comparison of a GPU MX quantization with the oracle's when the BF16 values
 being quantized are only known to lie in a small set.
 
-The fused SwiGLU quantizer forms g sigma(g) u in fp32 (error below 1.25 *
-2^-21 relative, plus an absolute 2^-149 where fp32 underflows) before the
+The fused SwiGLU quantizer forms g sigma(g) u in fp32 (error below 14 *
+2^-24 relative from the documented 2-ulp bounds of expf and __fdividef plus
+three roundings, plus an absolute 2^-149 where fp32 underflows) before the
 BF16 rounding.  Where the exact value lies within that distance of a BF16
 rounding midpoint either neighbour is a correct result, so the check takes,
 per element, the set {bf16(y - band), bf16(y + band)} around the oracle's
-FP64 value y, band = 2^-20 |y| + 2^-140 (both bounds with margin).  Blocks
+FP64 value y, band = 2^-19 |y| + 2^-140 (both bounds with margin).  Blocks
 whose 32 values are all unambiguous must match the oracle's bytes exactly;
 an ambiguous block's scale byte must lie between the E8M0 bytes of the
 smallest and the largest admissible block maximum, and each of its payload
@@ -16,7 +17,7 @@ import numpy as np
 
 import oracle
 
-BAND_REL = 2.0 ** -20
+BAND_REL = 2.0 ** -19
 BAND_ABS = 2.0 ** -140
 
 

@@ -134,8 +134,8 @@ def test_swiglu_quantize_plain(rows, f, floor):
 
 
 def test_swiglu_quantize_extremes():
-    """Gates far below -80 (double branch), tiny gates (the (g u) sigma
-    order), huge ups, zeros of both signs and values that underflow BF16."""
+    """Gates far below -80 (the double path), BF16-subnormal gates, gates
+    beyond 64, huge ups, zeros of both signs and values that underflow BF16."""
     rng = np.random.default_rng(21)
     rows, f = 256, 128
     g = rng.standard_normal((rows, f)) * np.exp(rng.uniform(-100, 6, (rows, 1)))
@@ -144,6 +144,7 @@ def test_swiglu_quantize_extremes():
     g[8, :16] = 0.0
     u[9, :16] = -0.0
     g[10] = np.ldexp(rng.uniform(1, 2, f), rng.integers(-133, -100, f))
+    g[11] = rng.uniform(60, 3000, f) * rng.choice([-1, 1], f)
     h = oracle.bf16_round(np.concatenate([g, u], axis=1))
     _swiglu_check(to_dev_bf16(h))
 
@@ -210,6 +211,42 @@ def test_route_weight_quantize_extremes():
     tok[7] = tokens  # out of range
     st = _weighted_check(to_dev_bf16(dy), tok, wt)
     assert st == m.MXFP8_ERR_DEVICE_CHECK
+
+
+def _fp32_midpoint_pairs(n, seed):
+    """(x, w) pairs whose fp32 product lands exactly on a BF16 rounding
+    midpoint while the exact product does not: the double-rounding cases."""
+    rng = np.random.default_rng(seed)
+    xs_bits = np.arange(0x0080, 0x7F80, dtype=np.uint16)  # positive normal BF16
+    xs = oracle.bf16_decode(xs_bits)
+    found = []
+    while len(found) < n:
+        w = np.float32(rng.uniform(0.25, 1.0))
+        p32 = (xs.astype(np.float32) * w).astype(np.float32)
+        hit = ((p32.view(np.uint32) & 0xFFFF) == 0x8000) & (p32.astype(np.float64) != xs * np.float64(w))
+        for i in np.nonzero(hit)[0][:2]:
+            found.append((int(xs_bits[i]), w))
+    return found[:n]
+
+
+def test_route_weight_quantize_double_rounding_cases():
+    """Products whose fp32 rounding sits on a BF16 midpoint take the exact
+    path; one fp32 rounding followed by the BF16 rounding would be off by one
+    unit in the last place there."""
+    pairs = _fp32_midpoint_pairs(32, 23)
+    cols = 64
+    dy = np.zeros((len(pairs), cols), np.uint16)
+    rng = np.random.default_rng(24)
+    for i, (xb, _) in enumerate(pairs):
+        dy[i] = oracle.bf16_round(rng.uniform(0.5, 1.0, cols))
+        dy[i, i % cols] = xb
+    tok = np.arange(len(pairs), dtype=np.int32)
+    wt = np.array([w for _, w in pairs], np.float32)
+    g = oracle.route_weight(dy, tok, wt)
+    naive = (oracle.bf16_decode(dy).astype(np.float32) * wt[:, None]).astype(np.float32)
+    naive_bits = oracle.bf16_round(naive.astype(np.float64))
+    assert (naive_bits != g).sum() >= len(pairs) // 4  # the cases are real
+    assert _weighted_check(to_dev_bf16(dy), tok, wt) == m.MXFP8_OK
 
 
 @pytest.mark.parametrize("counts", GROUP_COUNTS)
