@@ -11,9 +11,10 @@
 //    and MX-quantized rowwise in the same pass (the "route weighting +
 //    gradient Q" fusion).
 //
-// All three share the quantizer's 128 x 128 tile walk: blockIdx.x is a
+// All three share the row quantizer's 128 x 128 tile walk: blockIdx.x is a
 // 128-row scale tile (group-padded when offsets are given), blockIdx.y a
-// 128-column tile; a half-warp covers one tile row, 8 columns per lane.
+// 128-column tile (or the first of several); each thread owns whole 32-value
+// blocks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -81,39 +82,48 @@ __device__ __forceinline__ uint32_t dq2(uint32_t codes, float s) {
     return r;
 }
 
+// One thread per 32-value block: thread t of a 128 x 128 tile owns block
+// (t & 3) of tile rows t/4 and t/4 + 64.
 template <bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     dequantize_mx_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                          int64_t rows, int64_t cols, const int32_t* offsets, int groups,
-                         uint16_t* __restrict__ out, int64_t ldo, int64_t nkc) {
+                         uint16_t* __restrict__ out, int64_t ldo, int64_t nkc, bool v8) {
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
-    const int seg = tid & 15;
-    const int64_t col = static_cast<int64_t>(blockIdx.y) * kTile + seg * 8;
+    const int j = tid & 3;
+    const int64_t col = static_cast<int64_t>(blockIdx.y) * kTile + j * 32;
     const uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + blockIdx.y) * 512;
-    uint2 qv[8];
-    uint32_t sw[8];
+    uint32_t qw[2][8];
+    uint32_t sb[2];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = it * 16 + (tid >> 4);
-        const int64_t row = row_begin + r;
-        const bool in = row < row_end && col < cols;
-        qv[it] = in ? __ldcs(reinterpret_cast<const uint2*>(q + row * cols + col)) : make_uint2(0u, 0u);
-        sw[it] = in ? __ldg(reinterpret_cast<const uint32_t*>(s_tile + swz_word(r))) : 0u;
-    }
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = it * 16 + (tid >> 4);
+    for (int i = 0; i < 2; ++i) {
+        const int r = (tid >> 2) + 64 * i;
         const int64_t row = row_begin + r;
         if (row < row_end && col < cols) {
-            const float sc = e8m0_value((sw[it] >> (8 * (seg >> 2))) & 0xFFu);
-            uint4 o;
-            o.x = dq2(qv[it].x & 0xFFFFu, sc);
-            o.y = dq2(qv[it].x >> 16, sc);
-            o.z = dq2(qv[it].y & 0xFFFFu, sc);
-            o.w = dq2(qv[it].y >> 16, sc);
-            *reinterpret_cast<uint4*>(out + row * ldo + col) = o;
+            ld32_stream(q + row * cols + col, qw[i], v8);
+            sb[i] = __ldg(s_tile + swz_word(r) + j);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qw[i][k] = 0u;
+            sb[i] = 0u;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int64_t row = row_begin + (tid >> 2) + 64 * i;
+        if (row < row_end && col < cols) {
+            const float sc = e8m0_value(sb[i]);
+            uint32_t o[16];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                o[2 * k] = dq2(qw[i][k] & 0xFFFFu, sc);
+                o[2 * k + 1] = dq2(qw[i][k] >> 16, sc);
+            }
+            uint16_t* dst = out + row * ldo + col;
+            st32(dst, o, v8);
+            st32(dst + 16, o + 8, v8);
         }
     }
 }
@@ -185,45 +195,63 @@ __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2) {
 // for gathers, the row indices) are paid once per CTA.
 constexpr int kColTilesPerCta = 4;
 
+// Any of 32 packed BF16 gates (16 words) below -80.
+__device__ __forceinline__ bool swiglu_rare32(const uint32_t* g) {
+    uint32_t m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = max_u16x2(max_u16x2(g[4 * k], g[4 * k + 1]), max_u16x2(g[4 * k + 2], g[4 * k + 3]));
+    const uint32_t t = max_u16x2(max_u16x2(m[0], m[1]), max_u16x2(m[2], m[3]));
+    return max(t & 0xFFFFu, t >> 16) > 0xC2A0u;
+}
+
+// One thread per 32-value output block (thread t of a 128 x 128 tile owns
+// block t & 3 of tile rows t/4 and t/4 + 64), several column tiles per CTA.
 template <bool FLOOR, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads)
     swiglu_quant_kernel(const uint16_t* __restrict__ h, int64_t rows, int64_t f, int64_t ld,
                         const int32_t* offsets, int groups, uint8_t* __restrict__ q,
-                        uint8_t* __restrict__ s, int64_t nkc) {
+                        uint8_t* __restrict__ s, int64_t nkc, bool v8) {
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
-    const int seg = tid & 15;
+    const int j = tid & 3;
     for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
-        const int64_t col = ct * kTile + seg * 8;
-        uint4 gv[8], uv[8];
+        const int64_t col = ct * kTile + j * 32;
+        uint32_t gw[2][16], uw[2][16];
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int64_t row = row_begin + it * 16 + (tid >> 4);
+        for (int i = 0; i < 2; ++i) {
+            const int64_t row = row_begin + (tid >> 2) + 64 * i;
             if (row < row_end && col < f) {
-                gv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + col));
-                uv[it] = __ldcs(reinterpret_cast<const uint4*>(h + row * ld + f + col));
+                const uint16_t* src = h + row * ld + col;
+                ld32_stream(src, gw[i], v8);
+                ld32_stream(src + 16, gw[i] + 8, v8);
+                ld32_stream(src + f, uw[i], v8);
+                ld32_stream(src + f + 16, uw[i] + 8, v8);
             } else {
-                gv[it] = make_uint4(0u, 0u, 0u, 0u);
-                uv[it] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) gw[i][k] = uw[i][k] = 0u;
             }
         }
         uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int r = it * 16 + (tid >> 4);
+        for (int i = 0; i < 2; ++i) {
+            const int r = (tid >> 2) + 64 * i;
             const int64_t row = row_begin + r;
             const bool in = row < row_end && col < f;
-            uint4 v;
-            if (in && swiglu_rare8(gv[it])) {
-                v = swiglu8_exact(gv[it], uv[it]);
+            uint32_t v[16];
+            if (in && swiglu_rare32(gw[i])) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 e = swiglu8_exact(
+                        make_uint4(gw[i][4 * k], gw[i][4 * k + 1], gw[i][4 * k + 2], gw[i][4 * k + 3]),
+                        make_uint4(uw[i][4 * k], uw[i][4 * k + 1], uw[i][4 * k + 2], uw[i][4 * k + 3]));
+                    v[4 * k] = e.x; v[4 * k + 1] = e.y; v[4 * k + 2] = e.z; v[4 * k + 3] = e.w;
+                }
             } else {
-                v.x = swiglu2(gv[it].x, uv[it].x);
-                v.y = swiglu2(gv[it].y, uv[it].y);
-                v.z = swiglu2(gv[it].z, uv[it].z);
-                v.w = swiglu2(gv[it].w, uv[it].w);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = swiglu2(gw[i][k], uw[i][k]);
             }
-            mx_row_step<FLOOR>(v, r, in ? q + row * f + col : nullptr, s_tile);
+            mx_block32<FLOOR>(v, in ? q + row * f + col : nullptr, s_tile + swz_word(r) + j, v8);
         }
     }
 }
@@ -266,54 +294,66 @@ __global__ void __launch_bounds__(kThreads)
     weighted_quant_kernel(const uint16_t* __restrict__ dy, int64_t tokens, int64_t ld,
                           const int32_t* __restrict__ row_token, const float* __restrict__ row_weight,
                           int64_t rows, int64_t cols, const int32_t* offsets, int groups,
-                          uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc) {
+                          uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
+                          bool v8) {
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
-    const int seg = tid & 15;
-    // token and weight of each of this thread's rows, once for all column tiles
-    const int32_t* tk_base = row_token + row_begin;
-    int32_t tk[8];
-    float wv[8];
+    const int j = tid & 3;
+    // token and weight of this thread's two rows, once for all column tiles
+    int32_t tk[2];
+    float wv[2];
     bool bad = false;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = it * 16 + (tid >> 4);
-        const bool in = row_begin + r < row_end;
-        const int32_t t = in ? __ldg(tk_base + r) : -1;
+    for (int i = 0; i < 2; ++i) {
+        const int64_t row = row_begin + (tid >> 2) + 64 * i;
+        const bool in = row < row_end;
+        const int32_t t = in ? __ldg(row_token + row) : -1;
         const bool valid = t >= 0 && t < tokens;
         bad |= in && !valid;
-        tk[it] = valid ? t : -1;
-        wv[it] = valid ? __ldg(row_weight + row_begin + r) : 0.f;
+        tk[i] = valid ? t : -1;
+        wv[i] = valid ? __ldg(row_weight + row) : 0.f;
     }
     if (bad && blockIdx.y == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
     for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
-        const int64_t col = ct * kTile + seg * 8;
-        uint4 xv[8];
+        const int64_t col = ct * kTile + j * 32;
+        uint32_t xw[2][16];
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            // cached load: each token row is gathered by several dispatched rows
-            xv[it] = (tk[it] >= 0 && col < cols)
-                         ? __ldg(reinterpret_cast<const uint4*>(dy + static_cast<int64_t>(tk[it]) * ld + col))
-                         : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 2; ++i) {
+            if (tk[i] >= 0 && col < cols) {
+                // cached: each token row is gathered by several dispatched rows
+                const uint16_t* src = dy + static_cast<int64_t>(tk[i]) * ld + col;
+                ld32_cached(src, xw[i], v8);
+                ld32_cached(src + 16, xw[i] + 8, v8);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) xw[i][k] = 0u;
+            }
         }
         uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int r = it * 16 + (tid >> 4);
+        for (int i = 0; i < 2; ++i) {
+            const int r = (tid >> 2) + 64 * i;
             const int64_t row = row_begin + r;
             const bool in = row < row_end && col < cols;
-            uint4 v;
+            uint32_t v[16];
             uint32_t mid = 0xFFFFFFFFu;
-            v.x = weighted2(xv[it].x, wv[it], mid);
-            v.y = weighted2(xv[it].y, wv[it], mid);
-            v.z = weighted2(xv[it].z, wv[it], mid);
-            v.w = weighted2(xv[it].w, wv[it], mid);
-            if (mid == 0u) v = weighted8_exact(xv[it], wv[it]);
-            mx_row_step<FLOOR>(v, r, in ? q + row * cols + col : nullptr, s_tile);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = weighted2(xw[i][k], wv[i], mid);
+            if (mid == 0u) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 e = weighted8_exact(
+                        make_uint4(xw[i][4 * k], xw[i][4 * k + 1], xw[i][4 * k + 2], xw[i][4 * k + 3]), wv[i]);
+                    v[4 * k] = e.x; v[4 * k + 1] = e.y; v[4 * k + 2] = e.z; v[4 * k + 3] = e.w;
+                }
+            }
+            mx_block32<FLOOR>(v, in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
         }
     }
 }
+
+bool aligned32_host(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Grid of a tile walk: plain operands have ceil(rows/128) row tiles; a
 // group-padded one at most floor(rows/128) + groups.
@@ -335,12 +375,13 @@ cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t st) {
     if (!tile_grid(a.rows, a.cols, grouped, a.groups, &grid)) return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
+    const bool v8 = aligned32_host(a.q) && aligned32_host(a.out) && a.ldo % 16 == 0;
     if (grouped) {
         dequantize_mx_kernel<true><<<grid, kThreads, 0, st>>>(a.q, a.s, a.rows, a.cols, a.offsets,
-                                                             a.groups, a.out, a.ldo, nkc);
+                                                             a.groups, a.out, a.ldo, nkc, v8);
     } else {
         dequantize_mx_kernel<false><<<grid, kThreads, 0, st>>>(a.q, a.s, a.rows, a.cols, nullptr, 0,
-                                                              a.out, a.ldo, nkc);
+                                                              a.out, a.ldo, nkc, v8);
     }
     return cudaGetLastError();
 }
@@ -353,9 +394,10 @@ cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t st)
         return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.f + kTile - 1) / kTile;
+    const bool v8 = aligned32_host(a.h) && a.ld % 16 == 0 && a.f % 16 == 0 && aligned32_host(a.q);
 #define MXFP8_SWIGLU(FL, GR) \
     swiglu_quant_kernel<FL, GR><<<grid, kThreads, 0, st>>>(a.h, a.rows, a.f, a.ld, a.offsets, \
-                                                            a.groups, a.q, a.s, nkc)
+                                                            a.groups, a.q, a.s, nkc, v8)
     if (grouped) {
         if (fl) MXFP8_SWIGLU(true, true); else MXFP8_SWIGLU(false, true);
     } else {
@@ -373,10 +415,11 @@ cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t
         return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
+    const bool v8 = aligned32_host(a.dy) && a.ld % 16 == 0 && aligned32_host(a.q);
 #define MXFP8_WEIGHTED(FL, GR)                                                               \
     weighted_quant_kernel<FL, GR><<<grid, kThreads, 0, st>>>(                                \
         a.dy, a.tokens, a.ld, a.row_token, a.row_weight, a.rows, a.cols, a.offsets, a.groups, \
-        a.q, a.s, nkc)
+        a.q, a.s, nkc, v8)
     if (grouped) {
         if (fl) MXFP8_WEIGHTED(true, true); else MXFP8_WEIGHTED(false, true);
     } else {

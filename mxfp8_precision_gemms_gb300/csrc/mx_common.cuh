@@ -140,11 +140,88 @@ __device__ __forceinline__ void locate_group_tile(const int32_t* off, int G, int
     }
 }
 
+// 32-byte global accesses: one 256-bit instruction when `v8` (the caller
+// has checked 32-byte alignment of every address it will use), else two
+// 16-byte ones (the library's documented alignment is 16 bytes).  A thread
+// owning a whole 32-value block touches whole 32-byte sectors either way,
+// but a 256-bit access fetches each sector once per warp instruction.
+// ld32_stream: data read once (evict-first); ld32_cached: data that other
+// threads read again (gathers); st32: plain store.
+__device__ __forceinline__ void ld32_stream(const void* p, uint32_t* r, bool v8) {
+    if (v8) {
+        asm("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7])
+            : "l"(p));
+    } else {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
+        r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
+        r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ void ld32_cached(const void* p, uint32_t* r, bool v8) {
+    if (v8) {
+        asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7])
+            : "l"(p));
+    } else {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+        r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
+        r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ void st32(void* p, const uint32_t* r, bool v8) {
+    if (v8) {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]),
+                     "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else {
+        reinterpret_cast<uint4*>(p)[0] = make_uint4(r[0], r[1], r[2], r[3]);
+        reinterpret_cast<uint4*>(p)[1] = make_uint4(r[4], r[5], r[6], r[7]);
+    }
+}
+
+__device__ __forceinline__ bool aligned32(const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
+}
+
+// MX quantization of one 32-value block held by one thread as 16 words of
+// packed BF16 (value 2i in the low half of w[i]).  Writes the 32 E4M3 bytes
+// to q_dst (skipped when null; 32-byte aligned when v8) and the E8M0 byte to
+// *s_dst.
+template <bool FLOOR>
+__device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, uint8_t* s_dst,
+                                           bool v8) {
+    uint32_t m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = max_u16x2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m8[i] = max_u16x2(m8[i], m8[i + 4]);
+    const uint32_t m2 = max_u16x2(max_u16x2(m8[0], m8[1]), max_u16x2(m8[2], m8[3]));
+    const uint32_t byte = e8m0_byte(max(m2 & 0xFFFFu, m2 >> 16), FLOOR);
+    uint32_t q[8];
+    if (byte == 0xFFu) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = 0x7F7F7F7Fu;
+    } else {
+        const float f = inv_scale(byte);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = quant4_e4m3(w[2 * k], w[2 * k + 1], f);
+    }
+    if (q_dst != nullptr) st32(q_dst, q, v8);
+    *s_dst = static_cast<uint8_t>(byte);
+}
+
 // One rowwise step of a 128 x 128 tile: the half-warp holding tile row r
 // (lane & 16 selects the half) has 8 BF16 values per lane in v, lanes
 // 4b..4b+3 of the half forming 32-value block b.  Writes the 8 E4M3 bytes to
-// q_dst (skipped when null) and, from the half's lane 0, the row's four
-// scale bytes into the 512-byte scale tile.  All 32 lanes must call it.
+// q_dst (skipped when null) and, from lane 4b, block b's scale byte into the
+// 512-byte scale tile.  All 32 lanes must call it.
 template <bool FLOOR>
 __device__ __forceinline__ void mx_row_step(const uint4& v, int r, uint8_t* q_dst,
                                             uint8_t* s_tile) {
@@ -162,14 +239,7 @@ __device__ __forceinline__ void mx_row_step(const uint4& v, int r, uint8_t* q_ds
         q.y = quant4_e4m3(v.z, v.w, f);
     }
     if (q_dst != nullptr) *reinterpret_cast<uint2*>(q_dst) = q;
-    const int hb = lane & 16;
-    const uint32_t b0 = __shfl_sync(0xffffffffu, byte, hb + 0);
-    const uint32_t b1 = __shfl_sync(0xffffffffu, byte, hb + 4);
-    const uint32_t b2 = __shfl_sync(0xffffffffu, byte, hb + 8);
-    const uint32_t b3 = __shfl_sync(0xffffffffu, byte, hb + 12);
-    if ((lane & 15) == 0) {
-        *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    }
+    if ((lane & 3) == 0) s_tile[swz_word(r) + ((lane & 15) >> 2)] = static_cast<uint8_t>(byte);
 }
 
 }  // namespace mxfp8

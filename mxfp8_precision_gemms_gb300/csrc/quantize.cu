@@ -144,6 +144,59 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Rowwise-only MX quantization, one thread per 32-value block: a CTA covers
+// a 128 x 128 tile; thread t owns block (t & 3) of tile rows t/4 and t/4 + 64,
+// reading each block as two 32-byte loads, computing its scale once and
+// writing 32 payload bytes and one scale byte.
+template <bool FLOOR, bool GROUPED>
+__global__ void __launch_bounds__(kThreads)
+    quantize_mx_row_kernel(QuantMxArgs a, int64_t nkc, bool v8) {
+    __shared__ int64_t s_rows[2];
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    const int64_t rt = blockIdx.x;
+    const int64_t ct = blockIdx.y;
+    int64_t row_begin, row_end;
+    if constexpr (GROUPED) {
+        if (tid < 32) locate_group_tile(a.offsets, a.groups, a.rows, rt, s_rows, &s_ok);
+        __syncthreads();
+        if (!s_ok) {
+            if (rt == 0 && ct == 0 && tid == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
+            return;
+        }
+        row_begin = s_rows[0];
+        row_end = s_rows[1];
+        if (row_begin < 0) return;
+    } else {
+        row_begin = rt * kTile;
+        row_end = min(a.rows, row_begin + kTile);
+    }
+    const int j = tid & 3;
+    const int64_t col = ct * kTile + j * 32;
+    uint32_t w[2][16];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int64_t row = row_begin + (tid >> 2) + 64 * i;
+        if (row < row_end && col < a.cols) {
+            const uint16_t* src = a.x + row * a.ld + col;
+            ld32_stream(src, w[i], v8);
+            ld32_stream(src + 16, w[i] + 8, v8);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[i][k] = 0u;
+        }
+    }
+    uint8_t* s_tile = a.s_row + (rt * nkc + ct) * 512;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = (tid >> 2) + 64 * i;
+        const int64_t row = row_begin + r;
+        const bool in = row < row_end && col < a.cols;
+        mx_block32<FLOOR>(w[i], in ? a.q_row + row * a.cols + col : nullptr, s_tile + swz_word(r) + j,
+                          v8);
+    }
+}
+
 // ---------------------------------------------------------- per-tensor --
 
 __device__ __forceinline__ uint32_t warp_max(uint32_t m) {
@@ -302,7 +355,14 @@ cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
     if (row_tiles <= 0 || col_tiles <= 0) return cudaSuccess;
     if (col_tiles > 65535 || row_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
-    quantize_mx_kernel<ROW, COL, FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, nkc_col);
+    if constexpr (ROW && !COL) {
+        // 256-bit accesses when every block start is 32-byte aligned
+        const bool v8 = (reinterpret_cast<uintptr_t>(a.x) % 32 == 0) && (a.ld % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(a.q_row) % 32 == 0);
+        quantize_mx_row_kernel<FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, v8);
+    } else {
+        quantize_mx_kernel<ROW, COL, FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, nkc_col);
+    }
     return cudaGetLastError();
 }
 

@@ -157,6 +157,17 @@ def test_swiglu_quantize_grouped(counts):
     _swiglu_check(to_dev_bf16(h), offsets=off)
 
 
+def test_swiglu_quantize_16_byte_aligned():
+    """h with a row stride that is a multiple of 16 bytes but not 32 (no
+    256-bit accesses)."""
+    rows, f = 150, 96
+    rng = np.random.default_rng(31)
+    wide = oracle.bf16_round(rng.standard_normal((rows, 2 * f + 8)) * 2)
+    hd = to_dev_bf16(wide)[:, : 2 * f]
+    assert hd.stride(0) % 16 == 8
+    _swiglu_check(hd)
+
+
 def test_swiglu_quantize_full_size():
     """The grouped workload's up/gate output (262144 x 1024, 64 experts)."""
     w = workloads.swiglu_hidden(seed=0, device=device())

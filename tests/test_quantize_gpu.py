@@ -79,6 +79,30 @@ def test_quantize_mx_leading_dimension():
         assert np.array_equal(got[k], want[k]), k
 
 
+@pytest.mark.parametrize("flags", [ROW, ROW | FLOOR])
+@pytest.mark.parametrize("ld,shift,qshift", [(264, 0, 0), (256, 8, 0), (256, 0, 16), (272, 8, 16)])
+def test_quantize_mx_rowwise_16_byte_aligned(flags, ld, shift, qshift):
+    """Rowwise outputs when only the documented 16-byte alignment holds (row
+    stride, input start or payload start off a 32-byte boundary)."""
+    rows, cols = 200, 224
+    bits = random_bits((rows, cols), "student", seed=ld + shift + qshift)
+    wide = np.zeros((rows + 1, ld), np.uint16)
+    flat = wide.reshape(-1)
+    view = np.lib.stride_tricks.as_strided(flat[shift:], shape=(rows, cols), strides=(ld * 2, 2))
+    view[:] = bits
+    xd = to_dev_bf16(flat)[shift:shift + rows * ld].view(rows, ld)[:, :cols]
+    qbuf = filled(rows * cols + 32, 0xA5)
+    q = qbuf[qshift:qshift + rows * cols].view(rows, cols)
+    s = filled(m.mxfp8_scale_bytes(rows, cols), 0xA5)
+    m.fp8_quantize_mx(xd, flags, q_row=q, s_row=s)
+    assert_ok()
+    want = oracle.quantize_mx(bits, flags)
+    assert np.array_equal(host(q), want["q_row"])
+    assert np.array_equal(host(s), want["s_row"])
+    hb = host(qbuf)
+    assert np.all(hb[:qshift] == 0xA5) and np.all(hb[qshift + rows * cols:] == 0xA5)
+
+
 def _anchor_blocks(floor):
     """Blocks whose scale byte is fixed by an anchor value, filled with every
     finite BF16 pattern at or below the anchor: all BF16 values x all scales."""
