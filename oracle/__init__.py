@@ -65,6 +65,10 @@ def _load():
                 "orc_gemm_grouped_rows": (None, [P, P, P, P, P, I32, I64, I64, P, I64, P]),
                 "orc_num_threads": (I, []),
                 "orc_dequantize_mx": (None, [P, P, I64, I64, P, I64]),
+                "orc_quantize_tensor_scaled": (None, [P, I64, I, ctypes.c_float, P, P, P]),
+                "orc_delayed_scale": (ctypes.c_float, [P, I32, I, ctypes.c_float]),
+                "orc_quantize_tensor_delayed": (None, [P, I64, I, ctypes.c_float, P, I32, P, P, P, P, P]),
+                "orc_requantize_tensor": (None, [P, I64, I, ctypes.c_float, ctypes.c_float, I, P, P]),
                 "orc_dequantize_mx_grouped": (None, [P, P, P, I32, I64, P, I64]),
                 "orc_swiglu": (None, [P, I64, I64, I64, P]),
                 "orc_route_weight": (None, [P, I64, I64, P, P, I64, I64, P]),
@@ -230,6 +234,46 @@ def quantize_tensor(x_bits: np.ndarray, fmt: int = E4M3):
     scale = np.zeros(1, np.float32)
     _load().orc_quantize_tensor(_p(x), x.size, fmt, _p(amax), _p(scale), _p(q))
     return amax[0], scale[0], q
+
+
+def quantize_tensor_scaled(x_bits, fmt: int, scale: float):
+    """Cast with a given fp32 scale: (q, amax, saturated count)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    q = np.zeros(x.shape, np.uint8)
+    amax = np.zeros(1, np.float32)
+    sat = np.zeros(1, np.int64)
+    _load().orc_quantize_tensor_scaled(_p(x), x.size, fmt, float(np.float32(scale)), _p(q),
+                                       _p(amax), _p(sat))
+    return q, amax[0], int(sat[0])
+
+
+def delayed_scale(history, fmt: int = E4M3, margin: float = 1.0) -> np.float32:
+    h = np.ascontiguousarray(history, np.float32)
+    return np.float32(_load().orc_delayed_scale(_p(h), h.size, fmt, float(np.float32(margin))))
+
+
+def quantize_tensor_delayed(x_bits, fmt: int, margin: float, history, pos: int):
+    """One delayed-scaling cast.  Returns (q, scale, amax, sat, history', pos')."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    hist = np.array(history, np.float32)
+    p = np.array([pos], np.int32)
+    q = np.zeros(x.shape, np.uint8)
+    scale = np.zeros(1, np.float32)
+    amax = np.zeros(1, np.float32)
+    sat = np.zeros(1, np.int64)
+    _load().orc_quantize_tensor_delayed(_p(x), x.size, fmt, float(np.float32(margin)), _p(hist),
+                                        hist.size, _p(p), _p(scale), _p(q), _p(amax), _p(sat))
+    return q, scale[0], amax[0], int(sat[0]), hist, int(p[0])
+
+
+def requantize_tensor(q_in, fmt_in: int, s_in: float, s_out: float, fmt_out: int):
+    """FP8 payload rescaled from s_in to s_out: (q_out, saturated count)."""
+    q = np.ascontiguousarray(q_in, np.uint8)
+    out = np.zeros(q.shape, np.uint8)
+    sat = np.zeros(1, np.int64)
+    _load().orc_requantize_tensor(_p(q), q.size, fmt_in, float(np.float32(s_in)),
+                                  float(np.float32(s_out)), fmt_out, _p(out), _p(sat))
+    return out, int(sat[0])
 
 
 # ------------------------------------------------------------------ GEMMs --

@@ -439,6 +439,85 @@ void orc_quantize_tensor(const uint16_t* x, int64_t n, int fmt,
     *scale_out = s;
 }
 
+/* Number of payload codes equal to the largest finite code (either sign):
+ * the numerator of [FP8LM]'s overflow ratio (Section 2.1, automatic scaling:
+ * "values that hit the maximum representable value after the cast"). */
+static int64_t count_saturated(const uint8_t* q, int64_t n, int fmt) {
+    int64_t c = 0;
+    int maxc = fp8_max_code(fmt);
+    for (int64_t i = 0; i < n; ++i) c += (q[i] & 0x7F) == maxc;
+    return c;
+}
+
+/* Per-tensor cast with a given scale ([BOOK] delayed-scaling sketch: the
+ * cast uses a scale fixed before this tensor's amax is known; [FP8LM]
+ * Section 2.1 Eq. 3, g' = mu g, is the case s = mu):
+ * q = FP8(fp32(x s)), saturating RNE; also amax = max |x| (NaN wins) and the
+ * number of saturated payloads. */
+void orc_quantize_tensor_scaled(const uint16_t* x, int64_t n, int fmt, float s, uint8_t* q,
+                                float* amax_out, int64_t* sat_out) {
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double a = fabs(orc_bf16_decode(x[i]));
+        if (a > amax || isnan(a)) amax = a;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float y = (float)(orc_bf16_decode(x[i]) * (double)s); /* exact product, one rounding */
+        q[i] = orc_fp8_encode((double)y, fmt);
+    }
+    *amax_out = (float)amax;
+    *sat_out = count_saturated(q, n, fmt);
+}
+
+/* The delayed scale ([BOOK] sketch, compute_scale): a = the largest entry
+ * of the amax history (NaN propagates), clamped below at fp32(1e-12);
+ * s = fp32(fp32(fmax / a) * margin). */
+float orc_delayed_scale(const float* hist, int32_t h, int fmt, float margin) {
+    double a = 0.0;
+    int seen = 0;
+    for (int32_t i = 0; i < h; ++i) {
+        double v = hist[i];
+        if (!seen || v > a || isnan(v)) a = v;
+        seen = 1;
+        if (isnan(a)) break;
+    }
+    double floor_v = (double)1e-12f;
+    if (!(a >= floor_v) && !isnan(a)) a = floor_v;
+    double fmax = fmt == ORC_E5M2 ? 57344.0 : 448.0;
+    float s = (float)(fmax / a);
+    return (float)((double)s * (double)margin);
+}
+
+/* One delayed-scaling cast ([BOOK] sketch, cast_to_fp8): the scale from the
+ * history as it stands, the cast of x with it, then history[pos] = amax(x)
+ * and pos = (pos + 1) % h. */
+void orc_quantize_tensor_delayed(const uint16_t* x, int64_t n, int fmt, float margin,
+                                 float* hist, int32_t h, int32_t* pos, float* scale_out,
+                                 uint8_t* q, float* amax_out, int64_t* sat_out) {
+    float s = orc_delayed_scale(hist, h, fmt, margin);
+    orc_quantize_tensor_scaled(x, n, fmt, s, q, amax_out, sat_out);
+    hist[*pos] = *amax_out;
+    *pos = (*pos + 1) % h;
+    *scale_out = s;
+}
+
+/* Requantization to a shared scale ([FP8LM] Section 2.1, Eq. 4-5): with the
+ * group's scale s_out = min over ranks of s_in, q'' = FP8(s_out (g' / s_in))
+ * evaluated in that order in fp32: t = fp32(decode(q) / s_in),
+ * y = fp32(s_out t), saturating RNE to fmt_out.  Also counts saturated
+ * payloads. */
+void orc_requantize_tensor(const uint8_t* q_in, int64_t n, int fmt_in, float s_in, float s_out,
+                           int fmt_out, uint8_t* q_out, int64_t* sat_out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float t = (float)(orc_fp8_decode(q_in[i], fmt_in) / (double)s_in);
+        float y = (float)((double)s_out * (double)t);
+        q_out[i] = orc_fp8_encode((double)y, fmt_out);
+    }
+    *sat_out = count_saturated(q_out, n, fmt_out);
+}
+
 /* ------------------------------------------------------------------------ */
 /* GEMMs: C = A B^T on dequantized operands, FP64 ([OLMO] Eq. 60 operands,  */
 /* Section 11.1.1: block scales applied inside the product)                  */

@@ -714,3 +714,97 @@ def test_route_weight_is_one_rounding_of_the_exact_product():
         for c in range(0, cols, 7):
             v = Fraction(float(w[i])) * Fraction(float(dyv[tok[i], c]))
             assert got[i, c] == _correctly_rounded_bf16(v, table), (i, c)
+
+
+# ------------------------------------------- delayed and automatic scaling --
+
+def _torch_sat_cast(y32: torch.Tensor, fmt) -> np.ndarray:
+    """torch's float8 cast after clamping to the largest finite value (torch
+    itself does not saturate)."""
+    fmax = 448.0 if fmt == E4M3 else 57344.0
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    y = torch.where(torch.isnan(y32), y32, y32.clamp(-fmax, fmax))
+    return y.to(dt).view(torch.uint8).numpy()
+
+
+def _bf16_tensor(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_scaled_cast_vs_torch(fmt):
+    """q = FP8(fp32(x s)) against torch's fp32 product and float8 cast, for
+    scales that leave the tensor in range, saturate it or push it into the
+    subnormals; the saturated count against torch's values at +-max."""
+    rng = np.random.default_rng(40)
+    bits = oracle.bf16_round(rng.standard_normal(5000) * np.exp(rng.uniform(-12, 12, 5000)))
+    x = _bf16_tensor(bits)
+    fmax = 448.0 if fmt == E4M3 else 57344.0
+    for s in [1.0, 0.37, 1e3, 2.0 ** 20, 3e-5, 1e-12]:
+        q, amax, sat = oracle.quantize_tensor_scaled(bits, fmt, s)
+        y = x.float() * torch.tensor(s, dtype=torch.float32)
+        want = _torch_sat_cast(y, fmt)
+        assert np.array_equal(q, want), s
+        dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+        assert sat == int((torch.from_numpy(want).view(dt).float().abs() == fmax).sum())
+        assert amax == np.float32(np.abs(oracle.bf16_decode(bits)).max())
+
+
+class _BookDelayedScale:
+    """The book's delayed-scaling cast, restated with torch fp32 ops: scale
+    from the max of the amax history (clamped at 1e-12) times the margin,
+    cast, then record this tensor's amax at the ring pointer."""
+
+    def __init__(self, history_len, margin, fmt):
+        self.hist = torch.zeros(history_len, dtype=torch.float32)
+        self.ptr = 0
+        self.margin = margin
+        self.fmt = fmt
+        self.fmax = torch.tensor(448.0 if fmt == E4M3 else 57344.0, dtype=torch.float32)
+
+    def cast(self, x):
+        amax = self.hist.max().clamp_min(1e-12)
+        scale = (self.fmax / amax) * self.margin
+        q = _torch_sat_cast(x.float() * scale, self.fmt)
+        self.hist[self.ptr] = x.float().abs().amax()
+        self.ptr = (self.ptr + 1) % self.hist.numel()
+        return q, scale
+
+
+@pytest.mark.parametrize("fmt,margin", [(E4M3, 1.0), (E4M3, 0.9), (E5M2, 1.0)])
+def test_delayed_scaling_vs_book_recipe(fmt, margin):
+    """Seven steps with a 4-entry history: the zero history of the first step
+    (scale 448e12, everything saturates), growth, a spike that saturates the
+    next step's cast, and the ring wrapping."""
+    rng = np.random.default_rng(41)
+    book = _BookDelayedScale(4, margin, fmt)
+    hist, pos = np.zeros(4, np.float32), 0
+    for step, mag in enumerate([1.0, 1.0, 2.0, 50.0, 1.0, 0.01, 0.01]):
+        bits = oracle.bf16_round(rng.standard_normal(3000) * mag)
+        q, s, amax, sat, hist, pos = oracle.quantize_tensor_delayed(bits, fmt, margin, hist, pos)
+        wq, ws = book.cast(_bf16_tensor(bits))
+        assert np.float32(s) == np.float32(ws.item()), step
+        assert np.array_equal(q, wq), step
+        assert np.array_equal(hist, book.hist.numpy()) and pos == book.ptr, step
+        if step == 0:
+            assert sat == int((np.abs(oracle.bf16_decode(bits)) > 0).sum())  # all nonzero saturate
+
+
+@pytest.mark.parametrize("fmt_in,fmt_out", [(E4M3, E4M3), (E5M2, E5M2), (E4M3, E5M2), (E5M2, E4M3)])
+def test_requantize_vs_torch(fmt_in, fmt_out):
+    """q'' = FP8(s_out (g' / s_in)) in fp32, against torch, for every code;
+    and the identity for s_out = s_in, one format."""
+    codes = np.arange(256, dtype=np.uint8)
+    dt_in = torch.float8_e4m3fn if fmt_in == E4M3 else torch.float8_e5m2
+    g = torch.from_numpy(codes).view(dt_in).float()
+    for s_in, s_out in [(3.0, 1.5), (448.0 / 3.1, 448.0 / 7.9), (1.0, 2.0 ** -10), (0.75, 0.75 * 1.001)]:
+        got, sat = oracle.requantize_tensor(codes, fmt_in, s_in, s_out, fmt_out)
+        y = torch.tensor(s_out, dtype=torch.float32) * (g / torch.tensor(s_in, dtype=torch.float32))
+        want = _torch_sat_cast(y, fmt_out)
+        nan = torch.isnan(g).numpy()
+        assert np.array_equal(got[~nan], want[~nan]), (s_in, s_out)
+        assert np.all((got[nan] & 0x7F) == 0x7F)
+    if fmt_in == fmt_out:
+        same, _ = oracle.requantize_tensor(codes, fmt_in, 5.0, 5.0, fmt_out)
+        finite = ~torch.isnan(g).numpy() & ~torch.isinf(g).numpy()
+        assert np.array_equal(same[finite], codes[finite])
