@@ -244,6 +244,70 @@ mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
                               void* c_bf16, int64_t ldc, mxfp8_stream_t stream);
 
 /*
+ * fp8_quantize_tensor_scaled - per-tensor FP8 cast with a scale the caller
+ * already holds on the device ("3.8 Mixed Precision, bf16 & FP8 Training",
+ * "Per-tensor scaling and the delayed-scaling recipe": the cast uses a scale
+ * chosen before this tensor's amax is known; "FP8-LM: Training FP8 Large
+ * Language Models", Section 2.1 Eq. 3: the gradient cast g' = mu g is the
+ * case s = mu).
+ *
+ *   q = FP8(fp32(x * s)), round-to-nearest-even, saturating at +-fmax.
+ *
+ *  scale_dev      device fp32 scalar s (read).
+ *  amax_dev       device fp32 scalar, written: max |x| (NaN if any x is NaN).
+ *  sat_count_dev  device uint64, written: how many payloads are the largest
+ *                 finite code (+-448 / +-57344) - FP8-LM's overflow count.
+ *  x_bf16, q      n values, 16-byte aligned.  n == 0 writes amax = 0, count 0.
+ */
+mxfp8_status fp8_quantize_tensor_scaled(const void* x_bf16, int64_t n, int fmt,
+                                        const float* scale_dev, void* q, float* amax_dev,
+                                        uint64_t* sat_count_dev, mxfp8_stream_t stream);
+
+/*
+ * fp8_quantize_tensor_delayed - one delayed-scaling cast ("3.8 Mixed
+ * Precision", "Per-tensor scaling and the delayed-scaling recipe"): the scale
+ * comes from a rolling history of past amax values, the cast runs without
+ * waiting for this tensor's amax, and that amax is recorded for later steps.
+ *
+ *   a = max(history) (NaN propagates), clamped below at 1e-12;
+ *   s = fp32(fp32(fmax / a) * margin);  q = FP8(fp32(x * s)) saturating;
+ *   history[pos] = max |x|;  pos = (pos + 1) % history_len.
+ *
+ *  amax_history_dev  device fp32[history_len], read and updated (state the
+ *                    caller keeps across steps; all zeros at the start, which
+ *                    makes the first cast saturate, as in the recipe).
+ *  history_pos_dev   device int32 ring position, read and updated; a value
+ *                    outside [0, history_len) records MXFP8_ERR_DEVICE_CHECK
+ *                    and restarts the ring at 0.
+ *  scale_dev         device fp32, written: the s used.
+ *  amax_dev, sat_count_dev  as in fp8_quantize_tensor_scaled.
+ * 1 <= history_len <= 65536.  Three kernels on `stream`; calls on one state
+ * must be stream ordered.
+ */
+mxfp8_status fp8_quantize_tensor_delayed(const void* x_bf16, int64_t n, int fmt, float margin,
+                                         float* amax_history_dev, int32_t history_len,
+                                         int32_t* history_pos_dev, float* scale_dev, void* q,
+                                         float* amax_dev, uint64_t* sat_count_dev,
+                                         mxfp8_stream_t stream);
+
+/*
+ * fp8_requantize_tensor - rescale a per-tensor FP8 payload to another scale
+ * ("FP8-LM", Section 2.1, Eq. 4-5: before the gradient all-reduce every rank
+ * requantizes to the group's shared scale s'_g = min_i s'_i).
+ *
+ *   q'' = FP8(fp32(s_out * fp32(decode(q) / s_in))), in that order,
+ *         round-to-nearest-even, saturating; fmt_in and fmt_out independent.
+ *
+ *  scale_in_dev, scale_out_dev  device fp32 scalars (read).
+ *  sat_count_dev                device uint64, written: payloads at the
+ *                               largest finite code of fmt_out.
+ *  q_in, q_out                  n bytes, 16-byte aligned; may not overlap.
+ */
+mxfp8_status fp8_requantize_tensor(const void* q_in, int64_t n, int fmt_in, const float* scale_in_dev,
+                                   const float* scale_out_dev, int fmt_out, void* q_out,
+                                   uint64_t* sat_count_dev, mxfp8_stream_t stream);
+
+/*
  * Routed-path kernels around the quantizer ("Olmo-core MoE report", Section
  * 11.4.1 and Table 25).  Each takes optional group offsets: NULL with
  * groups == 0 gives the plain rows x cols layout of fp8_quantize_mx's rowwise

@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
+                "fp8_quantize_tensor_scaled": (st, [P, I64, I, P, P, P, P, P]),
+                "fp8_quantize_tensor_delayed": (st, [P, I64, I, ctypes.c_float, P, I32, P, P, P, P, P, P]),
+                "fp8_requantize_tensor": (st, [P, I64, I, P, P, I, P, P, P]),
                 "fp8_dequantize_mx": (st, [P, P, I64, I64, P, I32, P, I64, P]),
                 "fp8_swiglu_quantize_mx": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
                 "fp8_route_weight_quantize_mx": (st, [P, I64, I64, P, P, I64, I64, P, I32, U, P, P, P]),
@@ -166,6 +169,51 @@ def fp8_quantize_tensor(x: torch.Tensor, fmt: int = FP8_E4M3, q=None, amax=None,
     _check(lib().fp8_quantize_tensor(_ptr(x), x.numel(), fmt, _ptr(amax), _ptr(scale), _ptr(q),
                                      _ptr(workspace), _stream(stream)))
     return q, amax, scale
+
+
+def fp8_quantize_tensor_scaled(x: torch.Tensor, scale: torch.Tensor, fmt: int = FP8_E4M3, q=None,
+                               amax=None, sat_count=None, stream=None):
+    """Cast with a device scale: returns (q, amax fp32[1], sat_count int64[1])."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous() and scale.dtype == torch.float32
+    _need_cuda(x, scale)
+    q = q if q is not None else torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    amax = amax if amax is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    sat_count = sat_count if sat_count is not None else torch.empty(1, dtype=torch.int64, device=x.device)
+    _check(lib().fp8_quantize_tensor_scaled(_ptr(x), x.numel(), fmt, _ptr(scale), _ptr(q), _ptr(amax),
+                                            _ptr(sat_count), _stream(stream)))
+    return q, amax, sat_count
+
+
+def fp8_quantize_tensor_delayed(x: torch.Tensor, history: torch.Tensor, pos: torch.Tensor,
+                                fmt: int = FP8_E4M3, margin: float = 1.0, q=None, scale=None,
+                                amax=None, sat_count=None, stream=None):
+    """One delayed-scaling cast; history (fp32) and pos (int32[1]) are updated
+    in place.  Returns (q, scale, amax, sat_count) as device tensors."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert history.dtype == torch.float32 and pos.dtype == torch.int32
+    _need_cuda(x, history, pos)
+    dev = x.device
+    q = q if q is not None else torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    scale = scale if scale is not None else torch.empty(1, dtype=torch.float32, device=dev)
+    amax = amax if amax is not None else torch.empty(1, dtype=torch.float32, device=dev)
+    sat_count = sat_count if sat_count is not None else torch.empty(1, dtype=torch.int64, device=dev)
+    _check(lib().fp8_quantize_tensor_delayed(_ptr(x), x.numel(), fmt, margin, _ptr(history),
+                                             history.numel(), _ptr(pos), _ptr(scale), _ptr(q), _ptr(amax),
+                                             _ptr(sat_count), _stream(stream)))
+    return q, scale, amax, sat_count
+
+
+def fp8_requantize_tensor(q: torch.Tensor, scale_in: torch.Tensor, scale_out: torch.Tensor,
+                          fmt_in: int = FP8_E4M3, fmt_out: int = FP8_E4M3, out=None, sat_count=None,
+                          stream=None):
+    """Payload rescaled from scale_in to scale_out: returns (q_out, sat_count)."""
+    assert q.dtype == torch.uint8 and q.is_contiguous()
+    _need_cuda(q, scale_in, scale_out)
+    out = out if out is not None else torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    sat_count = sat_count if sat_count is not None else torch.empty(1, dtype=torch.int64, device=q.device)
+    _check(lib().fp8_requantize_tensor(_ptr(q), q.numel(), fmt_in, _ptr(scale_in), _ptr(scale_out), fmt_out,
+                                       _ptr(out), _ptr(sat_count), _stream(stream)))
+    return out, sat_count
 
 
 def mxfp8_tensor_workspace_bytes() -> int:

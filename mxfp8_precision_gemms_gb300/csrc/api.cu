@@ -191,6 +191,71 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
 
 size_t mxfp8_tensor_workspace_bytes(void) { return 256; }
 
+mxfp8_status fp8_quantize_tensor_scaled(const void* x_bf16, int64_t n, int fmt,
+                                        const float* scale_dev, void* q, float* amax_dev,
+                                        uint64_t* sat_count_dev, mxfp8_stream_t stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (!scale_dev || !amax_dev || !sat_count_dev)
+        return fail(MXFP8_ERR_INVALID_ARG, "scale, amax or sat_count is NULL");
+    if (n > 0 && (!x_bf16 || !q)) return fail(MXFP8_ERR_INVALID_ARG, "x or q is NULL");
+    if ((n > 0 && (!aligned16(x_bf16) || !aligned16(q))) ||
+        (reinterpret_cast<uintptr_t>(scale_dev) & 3u) || (reinterpret_cast<uintptr_t>(amax_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count_dev) & 7u))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
+    return cuda_result(launch_quantize_tensor_scaled(static_cast<const uint16_t*>(x_bf16), n, fmt,
+                                                     scale_dev, static_cast<uint8_t*>(q), amax_dev,
+                                                     reinterpret_cast<unsigned long long*>(sat_count_dev),
+                                                     reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_tensor_scaled launch");
+}
+
+mxfp8_status fp8_quantize_tensor_delayed(const void* x_bf16, int64_t n, int fmt, float margin,
+                                         float* amax_history_dev, int32_t history_len,
+                                         int32_t* history_pos_dev, float* scale_dev, void* q,
+                                         float* amax_dev, uint64_t* sat_count_dev,
+                                         mxfp8_stream_t stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (history_len < 1 || history_len > 65536)
+        return fail(MXFP8_ERR_INVALID_ARG, "history_len must be in [1, 65536]");
+    if (!amax_history_dev || !history_pos_dev || !scale_dev || !amax_dev || !sat_count_dev)
+        return fail(MXFP8_ERR_INVALID_ARG, "a state or output pointer is NULL");
+    if (n > 0 && (!x_bf16 || !q)) return fail(MXFP8_ERR_INVALID_ARG, "x or q is NULL");
+    if ((n > 0 && (!aligned16(x_bf16) || !aligned16(q))) ||
+        ((reinterpret_cast<uintptr_t>(amax_history_dev) | reinterpret_cast<uintptr_t>(history_pos_dev) |
+          reinterpret_cast<uintptr_t>(scale_dev) | reinterpret_cast<uintptr_t>(amax_dev)) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count_dev) & 7u))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
+    return cuda_result(
+        launch_quantize_tensor_delayed(static_cast<const uint16_t*>(x_bf16), n, fmt, margin,
+                                       amax_history_dev, history_len, history_pos_dev, scale_dev,
+                                       static_cast<uint8_t*>(q), amax_dev,
+                                       reinterpret_cast<unsigned long long*>(sat_count_dev),
+                                       reinterpret_cast<cudaStream_t>(stream)),
+        "fp8_quantize_tensor_delayed launch");
+}
+
+mxfp8_status fp8_requantize_tensor(const void* q_in, int64_t n, int fmt_in, const float* scale_in_dev,
+                                   const float* scale_out_dev, int fmt_out, void* q_out,
+                                   uint64_t* sat_count_dev, mxfp8_stream_t stream) {
+    if ((fmt_in != FP8_E4M3 && fmt_in != FP8_E5M2) || (fmt_out != FP8_E4M3 && fmt_out != FP8_E5M2))
+        return fail(MXFP8_ERR_INVALID_ARG, "unknown format");
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (!scale_in_dev || !scale_out_dev || !sat_count_dev)
+        return fail(MXFP8_ERR_INVALID_ARG, "a scale or sat_count is NULL");
+    if (n > 0 && (!q_in || !q_out)) return fail(MXFP8_ERR_INVALID_ARG, "q_in or q_out is NULL");
+    if ((n > 0 && (!aligned16(q_in) || !aligned16(q_out))) ||
+        ((reinterpret_cast<uintptr_t>(scale_in_dev) | reinterpret_cast<uintptr_t>(scale_out_dev)) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count_dev) & 7u))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
+    return cuda_result(launch_requantize_tensor(static_cast<const uint8_t*>(q_in), n, fmt_in, scale_in_dev,
+                                                scale_out_dev, fmt_out, static_cast<uint8_t*>(q_out),
+                                                reinterpret_cast<unsigned long long*>(sat_count_dev),
+                                                reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_requantize_tensor launch");
+}
+
 mxfp8_status fp8_dequantize_mx(const void* q, const void* s, int64_t rows, int64_t cols,
                                const int32_t* group_offsets_dev, int32_t groups, void* out_bf16,
                                int64_t ldo, mxfp8_stream_t stream) {

@@ -75,6 +75,18 @@ cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t s);
 cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t s);
 cudaError_t take_status_fused(unsigned* out);
 
+// Delayed / automatic scaling (quantize.cu).  sat: 64-bit saturated count.
+cudaError_t launch_quantize_tensor_scaled(const uint16_t* x, int64_t n, int fmt, const float* scale,
+                                          uint8_t* q, float* amax, unsigned long long* sat,
+                                          cudaStream_t s);
+cudaError_t launch_quantize_tensor_delayed(const uint16_t* x, int64_t n, int fmt, float margin,
+                                           float* hist, int h, int* pos, float* scale,
+                                           uint8_t* q, float* amax, unsigned long long* sat,
+                                           cudaStream_t s);
+cudaError_t launch_requantize_tensor(const uint8_t* q_in, int64_t n, int fmt_in, const float* s_in,
+                                     const float* s_out, int fmt_out, uint8_t* q_out,
+                                     unsigned long long* sat, cudaStream_t s);
+
 struct GemmArgs {
     int mode;          // GEMM_MX or GEMM_TENSOR
     int a_fmt, b_fmt;  // FP8_E4M3 / FP8_E5M2

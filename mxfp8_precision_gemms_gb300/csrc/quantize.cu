@@ -42,7 +42,6 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ int s_ok;
 
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
     const int64_t rt = blockIdx.x;
     const int64_t ct = blockIdx.y;
     int64_t row_begin, row_end;
@@ -347,6 +346,183 @@ __global__ void __launch_bounds__(kFusedThreads)
     }
 }
 
+// ------------------------------------- delayed and automatic scaling --
+
+// True when the saturating RNE cast of y gives the largest finite code:
+// E4M3 448 for |y| >= 432 (the tie with 416 goes to 448, the even code),
+// E5M2 57344 for |y| > 53248 (that tie goes to 49152).  False for NaN.
+template <int FMT>
+__device__ __forceinline__ uint32_t saturates(float y) {
+    const float a = fabsf(y);
+    return (FMT == FP8_E4M3 ? (a >= 432.f) : (a > 53248.f)) ? 1u : 0u;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+    return __reduce_add_sync(0xffffffffu, v);
+}
+
+// Block reduction of (amax bits, saturated count) into the global
+// accumulators: the amax as fp32 bits of a BF16 magnitude (positive fp32
+// patterns order like their values, NaN above Inf), the count 64-bit.
+__device__ __forceinline__ void reduce_amax_sat(uint32_t m, uint32_t cnt, unsigned* amax_bits,
+                                                unsigned long long* sat) {
+    __shared__ uint32_t red_m[8], red_c[8];
+    m = warp_max(m);
+    cnt = warp_sum(cnt);
+    if ((threadIdx.x & 31) == 0) {
+        red_m[threadIdx.x >> 5] = m;
+        red_c[threadIdx.x >> 5] = cnt;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < blockDim.x / 32 ? red_m[threadIdx.x] : 0u;
+        cnt = threadIdx.x < blockDim.x / 32 ? red_c[threadIdx.x] : 0u;
+        m = warp_max(m);
+        cnt = warp_sum(cnt);
+        if (threadIdx.x == 0) {
+            if (m) atomicMax(amax_bits, m << 16);
+            if (cnt) atomicAdd(sat, static_cast<unsigned long long>(cnt));
+        }
+    }
+}
+
+// Cast with a scale read from device memory ("3.8 Mixed Precision", the
+// delayed-scaling sketch; FP8-LM Section 2.1 Eq. 3 with s = mu): q =
+// FP8(fp32(x s)); accumulates amax(x) and the saturated count (both zeroed
+// on the stream before the launch).
+template <int FMT>
+__global__ void __launch_bounds__(256)
+    tensor_cast_scaled_kernel(const uint16_t* __restrict__ x, int64_t n, const float* scale,
+                              uint8_t* __restrict__ q, unsigned* amax_bits,
+                              unsigned long long* sat) {
+    const float s = *scale;
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    uint32_t m = 0, cnt = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += stride) {
+        const uint4 v = x8[i];
+        m = max(m, amax8(v));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __fmul_rn(bf16_lo(w[k]), s), hi = __fmul_rn(bf16_hi(w[k]), s);
+            cnt += saturates<FMT>(lo) + saturates<FMT>(hi);
+            o[k >> 1] |= cvt_fp8x2<FMT>(lo, hi) << (16 * (k & 1));
+        }
+        reinterpret_cast<uint2*>(q)[i] = make_uint2(o[0], o[1]);
+    }
+    for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+         t += stride) {
+        m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
+        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[t]) << 16), s);
+        cnt += saturates<FMT>(y);
+        q[t] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+    }
+    reduce_amax_sat(m, cnt, amax_bits, sat);
+}
+
+// The delayed scale from the amax history ("3.8 Mixed Precision", the
+// delayed-scaling sketch): a = max(history) (NaN propagates), clamped below
+// at 1e-12, s = fp32(fp32(fmax / a) * margin).  One thread; also zeroes
+// the accumulators of the cast that follows.
+__global__ void delayed_scale_kernel(const float* hist, int h, int fmt, float margin,
+                                     float* scale_out, unsigned* amax_bits,
+                                     unsigned long long* sat) {
+    float a = hist[0];
+    for (int i = 1; i < h && !isnan(a); ++i) {
+        const float v = hist[i];
+        if (isnan(v) || v > a) a = v;
+    }
+    if (!(a >= 1e-12f) && !isnan(a)) a = 1e-12f;
+    const float fmax = fmt == FP8_E5M2 ? 57344.0f : 448.0f;
+    *scale_out = __fmul_rn(__fdiv_rn(fmax, a), margin);
+    *amax_bits = 0u;
+    *sat = 0ull;
+}
+
+// history[pos] = this step's amax; pos = (pos + 1) % h.  One thread.
+__global__ void delayed_record_kernel(float* hist, int h, int* pos, const unsigned* amax_bits) {
+    int p = *pos;
+    if (p < 0 || p >= h) {  // a corrupted pointer: record and restart the ring
+        record_status(MXFP8_ERR_DEVICE_CHECK);
+        p = 0;
+    }
+    hist[p] = __uint_as_float(*amax_bits);
+    *pos = (p + 1) % h;
+}
+
+// Two FP8 codes (low byte first) to fp32, exactly (both formats fit f16).
+template <int FMT>
+__device__ __forceinline__ float2 fp8x2_to_f32(uint32_t codes) {
+    uint32_t h2;
+    if constexpr (FMT == FP8_E4M3) {
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes)));
+    } else {
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes)));
+    }
+    float lo, hi;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h2 >> 16)));
+    return make_float2(lo, hi);
+}
+
+// Requantization to a shared scale (FP8-LM Section 2.1, Eq. 4-5): q'' =
+// FP8(fp32(s_out * fp32(decode(q) / s_in))), in the equation's order;
+// accumulates the saturated count (zeroed before the launch).
+template <int FIN, int FOUT>
+__global__ void __launch_bounds__(256)
+    requantize_kernel(const uint8_t* __restrict__ q_in, int64_t n, const float* s_in_p,
+                      const float* s_out_p, uint8_t* __restrict__ q_out, unsigned long long* sat) {
+    const float s_in = *s_in_p, s_out = *s_out_p;
+    const int64_t n16 = n / 16;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const uint4* in16 = reinterpret_cast<const uint4*>(q_in);
+    uint32_t cnt = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += stride) {
+        const uint4 v = in16[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 a = fp8x2_to_f32<FIN>(w[k] & 0xFFFFu);
+            const float2 b = fp8x2_to_f32<FIN>(w[k] >> 16);
+            const float y0 = __fmul_rn(s_out, __fdiv_rn(a.x, s_in));
+            const float y1 = __fmul_rn(s_out, __fdiv_rn(a.y, s_in));
+            const float y2 = __fmul_rn(s_out, __fdiv_rn(b.x, s_in));
+            const float y3 = __fmul_rn(s_out, __fdiv_rn(b.y, s_in));
+            cnt += saturates<FOUT>(y0) + saturates<FOUT>(y1) + saturates<FOUT>(y2) + saturates<FOUT>(y3);
+            o[k] = cvt_fp8x2<FOUT>(y0, y1) | (cvt_fp8x2<FOUT>(y2, y3) << 16);
+        }
+        reinterpret_cast<uint4*>(q_out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    for (int64_t t = n16 * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+         t += stride) {
+        const float2 a = fp8x2_to_f32<FIN>(q_in[t]);
+        const float y = __fmul_rn(s_out, __fdiv_rn(a.x, s_in));
+        cnt += saturates<FOUT>(y);
+        q_out[t] = static_cast<uint8_t>(cvt_fp8x2<FOUT>(y, 0.0f) & 0xFFu);
+    }
+    __shared__ uint32_t red_c[8];
+    cnt = warp_sum(cnt);
+    if ((threadIdx.x & 31) == 0) red_c[threadIdx.x >> 5] = cnt;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        cnt = threadIdx.x < blockDim.x / 32 ? red_c[threadIdx.x] : 0u;
+        cnt = warp_sum(cnt);
+        if (threadIdx.x == 0 && cnt) atomicAdd(sat, static_cast<unsigned long long>(cnt));
+    }
+}
+
+int elementwise_blocks(int64_t n, int per_thread) {
+    const int64_t chunks = n / per_thread + 1;
+    const int64_t max_blocks = static_cast<int64_t>(sm_count_current_device()) * 8;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((chunks + 255) / 256, max_blocks)));
+}
+
 template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
 cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
     const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
@@ -465,6 +641,58 @@ cudaError_t noalloc_scratch_address(uint32_t** out) {
     }
     *out = addr[dev];
     return cudaSuccess;
+}
+
+cudaError_t launch_quantize_tensor_scaled(const uint16_t* x, int64_t n, int fmt, const float* scale,
+                                          uint8_t* q, float* amax, unsigned long long* sat,
+                                          cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(sat, 0, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return e;
+    if (n == 0) return cudaSuccess;
+    const int blocks = elementwise_blocks(n, 8);
+    unsigned* bits = reinterpret_cast<unsigned*>(amax);
+    if (fmt == FP8_E5M2) {
+        tensor_cast_scaled_kernel<FP8_E5M2><<<blocks, 256, 0, s>>>(x, n, scale, q, bits, sat);
+    } else {
+        tensor_cast_scaled_kernel<FP8_E4M3><<<blocks, 256, 0, s>>>(x, n, scale, q, bits, sat);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tensor_delayed(const uint16_t* x, int64_t n, int fmt, float margin,
+                                           float* hist, int h, int* pos, float* scale,
+                                           uint8_t* q, float* amax, unsigned long long* sat,
+                                           cudaStream_t s) {
+    unsigned* bits = reinterpret_cast<unsigned*>(amax);
+    delayed_scale_kernel<<<1, 1, 0, s>>>(hist, h, fmt, margin, scale, bits, sat);
+    if (n > 0) {
+        const int blocks = elementwise_blocks(n, 8);
+        if (fmt == FP8_E5M2) {
+            tensor_cast_scaled_kernel<FP8_E5M2><<<blocks, 256, 0, s>>>(x, n, scale, q, bits, sat);
+        } else {
+            tensor_cast_scaled_kernel<FP8_E4M3><<<blocks, 256, 0, s>>>(x, n, scale, q, bits, sat);
+        }
+    }
+    delayed_record_kernel<<<1, 1, 0, s>>>(hist, h, pos, bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requantize_tensor(const uint8_t* q_in, int64_t n, int fmt_in, const float* s_in,
+                                     const float* s_out, int fmt_out, uint8_t* q_out,
+                                     unsigned long long* sat, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(sat, 0, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return e;
+    if (n == 0) return cudaSuccess;
+    const int blocks = elementwise_blocks(n, 16);
+#define MXFP8_REQ(FI, FO) requantize_kernel<FI, FO><<<blocks, 256, 0, s>>>(q_in, n, s_in, s_out, q_out, sat)
+    if (fmt_in == FP8_E4M3) {
+        if (fmt_out == FP8_E4M3) MXFP8_REQ(FP8_E4M3, FP8_E4M3); else MXFP8_REQ(FP8_E4M3, FP8_E5M2);
+    } else {
+        if (fmt_out == FP8_E4M3) MXFP8_REQ(FP8_E5M2, FP8_E4M3); else MXFP8_REQ(FP8_E5M2, FP8_E5M2);
+    }
+#undef MXFP8_REQ
+    return cudaGetLastError();
 }
 
 cudaError_t take_status_quant(unsigned* out) {
