@@ -340,6 +340,7 @@ def hot_path_rows(m, dev, steps, warmup):
     del Xg, Wg, qa, qwg, Cg, w
 
     rows.update(routed_conversion_rows(m, dev, steps, warmup))
+    rows.update(scaling_rows(m, dev, steps, warmup))
 
     # 256^3, launch-bound
     w = workloads.mx256(seed=0, device=dev)
@@ -429,6 +430,113 @@ def routed_conversion_rows(m, dev, steps, warmup):
         "launches_per_step": 1}
     del dY, qg, sg, w
     return rows
+
+
+def scaling_rows(m, dev, steps, warmup):
+    """Per-tensor delayed scaling of a large gradient-like tensor (E5M2, the
+    gradient format of the hybrid recipe) and FP8-LM's requantization to a
+    shared scale, on 262144 x 2048 values (inputs larger than L2)."""
+    import workloads
+    st = torch.cuda.current_stream().cuda_stream
+    L = m.lib()
+    rows = {}
+    x = workloads.normal((262144, 2048), 1.0, 0, 7, dev).reshape(-1)
+    n = x.numel()
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    hist = torch.zeros(16, **f32)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale, amax = torch.empty(1, **f32), torch.empty(1, **f32)
+    sat = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def dl(timer):
+        _ok(L.fp8_quantize_tensor_delayed(x.data_ptr(), n, m.FP8_E5M2, 1.0, hist.data_ptr(), 16,
+                                          pos.data_ptr(), scale.data_ptr(), q.data_ptr(),
+                                          amax.data_ptr(), sat.data_ptr(), st))
+    ms, _ = _time_steps(dl, steps, warmup)
+    rows["delayed_cast_e5m2_262144x2048"] = {
+        "ms_per_step": ms, "gbs": n * TENSOR_Q_BYTES / ms / 1e6, "bytes_per_value": TENSOR_Q_BYTES,
+        "launches_per_step": 3, "note": "scale from a 16-entry amax history, one-pass cast, record"}
+    del x
+    q2 = torch.empty(n, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.full((1,), 3.0, **f32), torch.full((1,), 1.25, **f32)
+
+    def rq(timer):
+        _ok(L.fp8_requantize_tensor(q.data_ptr(), n, m.FP8_E5M2, s_in.data_ptr(), s_out.data_ptr(),
+                                    m.FP8_E5M2, q2.data_ptr(), sat.data_ptr(), st))
+    ms, _ = _time_steps(rq, steps, warmup)
+    rows["requantize_e5m2_262144x2048"] = {
+        "ms_per_step": ms, "gbs": n * 2.0 / ms / 1e6, "bytes_per_value": 2.0, "launches_per_step": 1}
+    del q, q2
+    return rows
+
+
+def _rule_stats(m, x, flags, orient):
+    """Quantize x (BF16, 2D) with the library, dequantize with the library,
+    and compare with x.  The block scale of every element is read back by
+    dequantizing an all-ones payload (E4M3 0x38 = 1.0) with the same scales."""
+    if orient == "row":
+        out = m.fp8_quantize_mx(x, m.MX_ROWWISE | flags)
+        q, sc = out["q_row"], out["s_row"]
+        ref = x.float()
+    else:
+        out = m.fp8_quantize_mx(x, m.MX_COLWISE | flags)
+        q, sc = out["q_col"], out["s_col"]
+        ref = x.float().t()
+    xh = m.fp8_dequantize_mx(q, sc).float()
+    s_el = m.fp8_dequantize_mx(torch.full_like(q, 0x38), sc).float()
+    err = xh - ref
+    nz = ref != 0
+    n = ref.numel()
+    stats = {
+        "rel_rms_error": float(err.pow(2).sum().sqrt() / ref.pow(2).sum().sqrt()),
+        "snr_db": float(10 * torch.log10(ref.pow(2).sum() / err.pow(2).sum().clamp_min(1e-300))),
+        "clipped_frac": float((ref.abs() > 448.0 * s_el).sum()) / n,
+        "flushed_to_zero_frac": float(((xh == 0) & nz).sum()) / max(1, int(nz.sum())),
+        "mean_rel_error_nonzero": float((err.abs()[nz] / ref.abs()[nz]).mean()),
+    }
+    return stats, (q, sc)
+
+
+def scale_rule_study(m, dev, seed=0):
+    """OCP floor vs rceil E8M0 scale selection ("Olmo-core MoE report",
+    Section 11.3.5) on the MLP up-projection and backward workloads: the
+    element-wise quantization error of each operand and the error of the
+    resulting GEMMs against an fp32 product of the BF16 operands."""
+    import workloads
+    res = {"study": "floor vs rceil E8M0 scale selection", "seed": seed, "tensors": {}, "gemms": {}}
+    up = workloads.mlp_up(seed=seed, device=dev)
+    bw = workloads.backward(seed=seed, device=dev)
+    cases = [("mlp_up.X", up["X"], "row"), ("mlp_up.W", up["W"], "row"),
+             ("backward.dY(row)", bw["dY"], "row"), ("backward.dY(col)", bw["dY"], "col"),
+             ("backward.W(col)", bw["W"], "col"), ("backward.X(col)", bw["X"], "col")]
+    ops = {}
+    for name, x, orient in cases:
+        res["tensors"][name] = {}
+        for rule, flags in (("rceil", 0), ("floor", m.MX_SCALE_FLOOR)):
+            st, ops[(name, rule)] = _rule_stats(m, x, flags, orient)
+            res["tensors"][name][rule] = st
+
+    rows = torch.arange(0, 8192, 16, device=dev)  # 512 sampled output rows
+    ref = up["X"][rows].float() @ up["W"].float().t()
+    res["gemms"]["mlp_up forward (512 sampled rows)"] = {
+        r: gemm_err_rows(m, ops, ("mlp_up.X", r), ("mlp_up.W", r), rows, ref) for r in ("rceil", "floor")}
+    ref = bw["dY"][rows].float() @ bw["W"].float()
+    res["gemms"]["backward dgrad (512 sampled rows)"] = {
+        r: gemm_err_rows(m, ops, ("backward.dY(row)", r), ("backward.W(col)", r), rows, ref) for r in ("rceil", "floor")}
+    rows_w = torch.arange(0, 4096, 8, device=dev)
+    ref = bw["dY"].float().t()[rows_w] @ bw["X"].float()
+    res["gemms"]["backward wgrad (512 sampled rows)"] = {
+        r: gemm_err_rows(m, ops, ("backward.dY(col)", r), ("backward.X(col)", r), rows_w, ref) for r in ("rceil", "floor")}
+    return res
+
+
+def gemm_err_rows(m, ops, a_key, b_key, rows, ref):
+    """Relative Frobenius error of the MX GEMM on the sampled output rows."""
+    qa, sa = ops[a_key]
+    qb, sb = ops[b_key]
+    c = m.fp8_scaled_gemm(m.GEMM_MX, qa, sa, qb, sb)[rows].float()
+    return float((c - ref).pow(2).sum().sqrt() / ref.pow(2).sum().sqrt())
 
 
 # --------------------------------------------------------- CPU oracle --
@@ -606,7 +714,13 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--study", choices=["scale-rules"], default=None,
+                    help="print the floor-vs-rceil quantization error statistics instead")
     args = ap.parse_args()
+    if args.study == "scale-rules":
+        import mxfp8_precision_gemms_gb300 as m
+        print(json.dumps(scale_rule_study(m, torch.device("cuda", 0), args.seed)))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

@@ -120,3 +120,22 @@ def test_shared_scale_reduce_one_rank_on_gpu():
     total, s_total, overflow = scaling.shared_scale_reduce(q, sv, m.FP8_E4M3, None, requant, decode)
     assert s_total == pytest.approx(sv) and overflow == 0
     assert np.array_equal(total.numpy(), oracle.fp8_decode(host(q), oracle.E4M3).astype(np.float32))
+
+
+@pytest.mark.parametrize("orient", ["row", "col"])
+def test_scale_rule_study_counts(orient):
+    """The floor-vs-rceil study's clipped count equals the oracle's: values
+    with |x| > 448 * 2^e for their block's floor exponent; rceil clips none."""
+    import bench
+    rng = np.random.default_rng(9)
+    bits = oracle.bf16_round(rng.standard_t(4, size=(256, 512)))
+    x = to_dev_bf16(bits)
+    st_r, _ = bench._rule_stats(m, x, 0, orient)
+    st_f, _ = bench._rule_stats(m, x, m.MX_SCALE_FLOOR, orient)
+    assert st_r["clipped_frac"] == 0.0
+    v = oracle.bf16_decode(bits)
+    blocks = (v if orient == "row" else v.T).reshape(-1, 32)
+    e = oracle.e8m0_scale_byte(np.abs(blocks).max(axis=1), floor=True).astype(np.int64) - 127
+    want = int((np.abs(blocks) > 448.0 * np.ldexp(1.0, e)[:, None]).sum())
+    assert st_f["clipped_frac"] == pytest.approx(want / v.size, abs=0)
+    assert want > 0
