@@ -21,16 +21,28 @@
 // not help), which is why the 2-SM form pays.
 //   warp 0       TMA producer (both CTAs): A box, this CTA's half of the B box
 //                (128-byte swizzle) and the 512-byte scale tiles per K step
-//                into a shared-memory ring; every load of both CTAs completes
-//                on the leader CTA's "full" mbarrier.
+//                into a shared-memory ring of slots; one "full" / "empty"
+//                mbarrier pair covers two slots, and every load of both CTAs
+//                completes on the leader CTA's "full" mbarrier.
 //   warp 1       TMEM allocator (both CTAs, collectively) and, in the leader
-//                only, the MMA issuer: tcgen05.cp of the block scales into
-//                TMEM, 4 MMAs of K = 32 per stage, tcgen05.commit releasing the
-//                stage in both CTAs and, after the last K step, handing the
-//                accumulators over.
+//                only, the MMA issuer: per K step tcgen05.cp of the block
+//                scales into TMEM and 4 MMAs of K = 32 (in issue order, so the
+//                MMAs see the scales without a wait), per slot pair one
+//                tcgen05.commit releasing the pair in both CTAs and, after the
+//                last K step, handing the accumulators over.  This thread's
+//                issue rate, not the tensor pipe, is the limit (measured:
+//                about 56 cycles per scale copy and 69 per MMA, plus a wait,
+//                a fence, a commit and address bookkeeping, against 512
+//                cycles of MMA work per K step), hence one barrier per two K
+//                steps and constant-stride address updates.  Moving the
+//                copies to another thread was slower: they then have to be
+//                waited for, and they queue behind the MMAs already issued.
 //   warps 2-9    epilogue (both CTAs): tcgen05.ld of this CTA's 128 x 256 FP32
 //                accumulator, release it to the leader, convert to BF16 and
-//                store while the next tile's main loop runs.
+//                store while the next tile's main loop runs: through a 2 KB
+//                swizzled staging tile per warp and TMA stores (plain GEMM;
+//                direct stores cost the main loop ~7 %), or with direct
+//                stores masked to the expert's rows (grouped GEMM).
 // The single-SM form (PAIR = false) is the same pipeline with one CTA.
 // Every wait is bounded; a wait that runs out records MXFP8_ERR_TIMEOUT,
 // the CTA drains its outstanding copies and MMAs, frees TMEM and exits.
@@ -59,6 +71,8 @@ constexpr int SFA_BYTES = 512;   // one 128-row x 4-block scale tile
 constexpr int SFB_BYTES = 1024;  // two of them (the tile's 256 B rows)
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr uint32_t EPI_TILE_BYTES = 32 * 32 * 2;  // 32 rows x 32 BF16 columns
+constexpr int SLOTS_PER_BAR = 2;              // K steps covered by one full/empty barrier
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;           // 128 lanes x 256 FP32 columns
@@ -71,7 +85,8 @@ constexpr uint32_t SF_COLS_PER_STAGE = 12;  // A: 4 columns, B: 8 columns
 template <bool PAIR>
 struct Cfg {
     static constexpr int CG = PAIR ? 2 : 1;  // CTAs per tensor-core operation
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = PAIR ? 6 : 4;   // shared-memory slots of one K step
+    static constexpr int NBARS = STAGES / SLOTS_PER_BAR;
     static constexpr int B_ROWS = BN / CG;   // B rows one CTA holds
     static constexpr int B_BYTES = B_ROWS * BK;
     // shared memory map (offsets from a 1024-byte aligned base)
@@ -80,14 +95,19 @@ struct Cfg {
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4;  // full, empty, tmem_full/empty, drain, never
+    // full, empty per slot pair; tmem_full/empty, drain, never
+    static constexpr uint32_t NUM_BARS = 2 * NBARS + 4;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_PREFIX = OFF_MISC + 32;
-    static constexpr uint32_t SMEM_PLAIN = OFF_PREFIX;
+    // plain GEMM: per epilogue warp a 2 KB staging tile for the TMA stores of C
+    static constexpr uint32_t OFF_EPI = (OFF_PREFIX + 1023) / 1024 * 1024;
+    static constexpr uint32_t SMEM_PLAIN = OFF_EPI + EPI_WARPS * EPI_TILE_BYTES;
     static constexpr uint32_t SMEM_GROUPED = OFF_PREFIX + 3 * (MAX_GROUPS + 1) * 4;
     static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024B alignment");
     static_assert(ACC_COLS + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(STAGES % SLOTS_PER_BAR == 0, "slots come in barrier pairs");
     static_assert(SMEM_GROUPED + 1024 <= 232448, "shared memory budget");
+    static_assert(SMEM_PLAIN + 1024 <= 232448, "shared memory budget");
 };
 
 struct KParams {
@@ -164,14 +184,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // tm_a / tm_b: payload boxes (128 x 128 and B_ROWS x 128 bytes, 128-byte
 // swizzle).  tm_sa / tm_sb: the scale arrays seen as rows of 256 bytes,
 // boxes of 2 rows = one 512-byte scale tile (out-of-range tiles read as 0).
+// tm_c: C as BF16, 32 x 32 boxes with 64-byte swizzle (plain GEMM only; the
+// store clips rows and columns outside M x N).
 template <bool MX, bool GROUPED, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
-                const KParams p) {
+                const __grid_constant__ CUtensorMap tm_c, const KParams p) {
     using C = Cfg<PAIR>;
     constexpr int CG = C::CG;
-    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -184,9 +205,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t num_pairs = gridDim.x / CG;
 
     auto bar = [&](uint32_t i) { return sbase + C::OFF_BAR + 8 * i; };
-    const uint32_t BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_TMEM_FULL = 2 * STAGES,
-                   BAR_TMEM_EMPTY = 2 * STAGES + 1, BAR_DRAIN = 2 * STAGES + 2,
-                   BAR_NEVER = 2 * STAGES + 3;
+    constexpr uint32_t NB = C::NBARS;
+    const uint32_t BAR_FULL = 0, BAR_EMPTY = NB, BAR_TMEM_FULL = 2 * NB,
+                   BAR_TMEM_EMPTY = 2 * NB + 1, BAR_DRAIN = 2 * NB + 2, BAR_NEVER = 2 * NB + 3;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* mtile_prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
@@ -195,9 +216,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     __shared__ int64_t s_total_units;
 
     if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < STAGES; ++s) {
-            mbar_init(bar(BAR_FULL + s), 1);
-            mbar_init(bar(BAR_EMPTY + s), 1);
+        for (uint32_t b = 0; b < NB; ++b) {
+            mbar_init(bar(BAR_FULL + b), 1);
+            mbar_init(bar(BAR_EMPTY + b), 1);
         }
         mbar_init(bar(BAR_TMEM_FULL), 1);
         mbar_init(bar(BAR_TMEM_EMPTY), EPI_WARPS * CG);  // both CTAs' epilogues
@@ -275,53 +296,58 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_prefetch_desc(&tm_sa);
                 tma_prefetch_desc(&tm_sb);
             }
-            uint32_t stage = 0, phase = 0;
-            uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks (leader's drain)
+            uint32_t pb = 0, phase = 0;              // slot pair (barrier) and its parity
+            uint32_t issued = 0, issued_parity = 0;  // per-barrier bit masks (leader's drain)
             bool ok = true;
-            constexpr uint32_t kStageTx =
+            constexpr uint32_t kSlotTx =
                 CG * (A_BYTES + C::B_BYTES + (MX ? SFA_BYTES + SFB_BYTES : 0));
             for (int64_t u = pair_id; u < total && ok; u += num_pairs) {
                 const Tile tl = decode_unit<GROUPED, CG>(p, u, rank, mtile_prefix, mgroup_prefix, offs);
                 const int64_t sfb_base = static_cast<int64_t>(tl.group) * p.sfb_group_chunks +
                                          2 * static_cast<int64_t>(tl.n_tile) * p.num_k_tiles;
                 const int32_t b_row = static_cast<int32_t>(tl.b_row + rank * C::B_ROWS);
-                for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                for (int kt0 = 0; kt0 < p.num_k_tiles; kt0 += SLOTS_PER_BAR) {
+                    const int nslots = min(SLOTS_PER_BAR, p.num_k_tiles - kt0);
+                    if (!mbar_wait(bar(BAR_EMPTY + pb), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    const uint32_t fb_local = bar(BAR_FULL + stage);
-                    if (leader) mbar_arrive_expect_tx(fb_local, kStageTx);
-                    const uint32_t dA = sbase + C::OFF_A + stage * A_BYTES;
-                    const uint32_t dB = sbase + C::OFF_B + stage * C::B_BYTES;
-                    const uint32_t dSA = sbase + C::OFF_SFA + stage * SFA_BYTES;
-                    const uint32_t dSB = sbase + C::OFF_SFB + stage * SFB_BYTES;
-                    const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt));
-                    const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt));
-                    const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
-                    if constexpr (PAIR) {
-                        const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
-                        tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
-                        tma_load_2d_pair(dB, &tm_b, fb, kt * BK, b_row);
-                        if constexpr (MX) {
-                            tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
-                            tma_load_2d_pair(dSB, &tm_sb, fb, 0, yb0);
-                            tma_load_2d_pair(dSB + 512, &tm_sb, fb, 0, yb1);
-                        }
-                    } else {
-                        tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
-                        tma_load_2d(dB, &tm_b, fb_local, kt * BK, b_row);
-                        if constexpr (MX) {
-                            tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
-                            tma_load_2d(dSB, &tm_sb, fb_local, 0, yb0);
-                            tma_load_2d(dSB + 512, &tm_sb, fb_local, 0, yb1);
+                    const uint32_t fb_local = bar(BAR_FULL + pb);
+                    if (leader) mbar_arrive_expect_tx(fb_local, kSlotTx * nslots);
+                    for (int j = 0; j < nslots; ++j) {
+                        const int kt = kt0 + j;
+                        const uint32_t slot = pb * SLOTS_PER_BAR + j;
+                        const uint32_t dA = sbase + C::OFF_A + slot * A_BYTES;
+                        const uint32_t dB = sbase + C::OFF_B + slot * C::B_BYTES;
+                        const uint32_t dSA = sbase + C::OFF_SFA + slot * SFA_BYTES;
+                        const uint32_t dSB = sbase + C::OFF_SFB + slot * SFB_BYTES;
+                        const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt));
+                        const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt));
+                        const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
+                        if constexpr (PAIR) {
+                            const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
+                            tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
+                            tma_load_2d_pair(dB, &tm_b, fb, kt * BK, b_row);
+                            if constexpr (MX) {
+                                tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
+                                tma_load_2d_pair(dSB, &tm_sb, fb, 0, yb0);
+                                tma_load_2d_pair(dSB + 512, &tm_sb, fb, 0, yb1);
+                            }
+                        } else {
+                            tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
+                            tma_load_2d(dB, &tm_b, fb_local, kt * BK, b_row);
+                            if constexpr (MX) {
+                                tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
+                                tma_load_2d(dSB, &tm_sb, fb_local, 0, yb0);
+                                tma_load_2d(dSB + 512, &tm_sb, fb_local, 0, yb1);
+                            }
                         }
                     }
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    issued |= 1u << pb;
+                    issued_parity = (issued_parity & ~(1u << pb)) | (phase << pb);
+                    if (++pb == NB) {
+                        pb = 0;
                         phase ^= 1u;
                     }
                 }
@@ -329,9 +355,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok && leader) {
                 // let every copy already in flight land before the CTA exits
                 const int never = 0;
-                for (uint32_t s = 0; s < STAGES; ++s) {
-                    if (issued & (1u << s))
-                        mbar_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, p.wait_limit_ns,
+                for (uint32_t b = 0; b < NB; ++b) {
+                    if (issued & (1u << b))
+                        mbar_wait(bar(BAR_FULL + b), (issued_parity >> b) & 1u, p.wait_limit_ns,
                                   &never);
                 }
             }
@@ -349,48 +375,83 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             constexpr uint16_t kPairMask = PAIR ? 3 : 1;
-            uint32_t stage = 0, phase = 0, acc_phase = 0;
-            const uint64_t sf_desc_base = smem_desc(0, 0, 128, SWZ_NONE);
+            uint32_t pb = 0, phase = 0, acc_phase = 0;
+            // Descriptors and TMEM addresses of slot pair pb, advanced by
+            // constants (a single thread issues everything: its dependent
+            // bookkeeping, not the tensor pipe, sets the pace).  The smem
+            // start-address fields (bits 0-13, address >> 4) never carry:
+            // shared memory stays below 256 KB.
+            constexpr uint32_t kPairA = SLOTS_PER_BAR * A_BYTES >> 4;
+            constexpr uint32_t kPairB = SLOTS_PER_BAR * C::B_BYTES >> 4;
+            constexpr uint32_t kPairSfa = SLOTS_PER_BAR * SFA_BYTES >> 4;
+            constexpr uint32_t kPairSfb = SLOTS_PER_BAR * SFB_BYTES >> 4;
+            constexpr uint32_t kPairCols = SLOTS_PER_BAR * SF_COLS_PER_STAGE;
+            const uint64_t desc_a0 = smem_desc(sbase + C::OFF_A, 16, 1024, SWZ_128B);
+            const uint64_t desc_b0 = smem_desc(sbase + C::OFF_B, 16, 1024, SWZ_128B);
+            const uint64_t sfa_d0 = smem_desc(sbase + C::OFF_SFA, 0, 128, SWZ_NONE);
+            const uint64_t sfb_d0 = smem_desc(sbase + C::OFF_SFB, 0, 128, SWZ_NONE);
+            const uint32_t sf_t0 = tmem + ACC_COLS;
+            uint64_t da = desc_a0, db = desc_b0, dsa = sfa_d0, dsb = sfb_d0;
+            uint32_t sft = sf_t0;
             for (int64_t u = pair_id; u < total && ok; u += num_pairs) {
                 if (!mbar_wait(bar(BAR_TMEM_EMPTY), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                     fail();
                     break;
                 }
                 tc_fence_after();
-                for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!mbar_wait(bar(BAR_FULL + stage), phase, p.wait_limit_ns, abort_flag)) {
+                uint32_t acc = 0;  // the first MMA of a tile overwrites the accumulator
+                for (int kt0 = 0; kt0 < p.num_k_tiles; kt0 += SLOTS_PER_BAR) {
+                    const int nslots = min(SLOTS_PER_BAR, p.num_k_tiles - kt0);
+                    if (!mbar_wait(bar(BAR_FULL + pb), phase, p.wait_limit_ns, abort_flag)) {
                         fail();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t da = smem_desc(sbase + C::OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
-                    const uint64_t db = smem_desc(sbase + C::OFF_B + stage * C::B_BYTES, 16, 1024, SWZ_128B);
-                    if constexpr (MX) {
-                        const uint32_t sfa_t = tmem + ACC_COLS + stage * SF_COLS_PER_STAGE;
-                        const uint32_t sfb_t = sfa_t + 4;
-                        const uint32_t sa = sbase + C::OFF_SFA + stage * SFA_BYTES;
-                        const uint32_t sb = sbase + C::OFF_SFB + stage * SFB_BYTES;
-                        tc_cp_32x128b_warpx4<CG>(sfa_t, sf_desc_base | ((sa & 0x3FFFFu) >> 4));
-                        tc_cp_32x128b_warpx4<CG>(sfb_t, sf_desc_base | ((sb & 0x3FFFFu) >> 4));
-                        tc_cp_32x128b_warpx4<CG>(sfb_t + 4, sf_desc_base | (((sb + 512) & 0x3FFFFu) >> 4));
 #pragma unroll
-                        for (uint32_t kk = 0; kk < BK / 32; ++kk) {
-                            mma_mxf8<CG>(tmem, da + 2 * kk, db + 2 * kk, idesc_mxf8(BM * CG, BN, kk),
-                                         sfa_t, sfb_t, (kt | kk) != 0);
-                        }
-                    } else {
+                    for (int j = 0; j < SLOTS_PER_BAR; ++j) {
+                        if (j < nslots) {
+                            const uint64_t dja = da + j * (A_BYTES >> 4);
+                            const uint64_t djb = db + j * (C::B_BYTES >> 4);
+                            if constexpr (MX) {
+                                const uint32_t sfa_t = sft + j * SF_COLS_PER_STAGE;
+                                // scales of this K step into TMEM; issued in order with
+                                // the MMAs below, which therefore see them
+                                tc_cp_32x128b_warpx4<CG>(sfa_t, dsa + j * (SFA_BYTES >> 4));
+                                tc_cp_32x128b_warpx4<CG>(sfa_t + 4, dsb + j * (SFB_BYTES >> 4));
+                                tc_cp_32x128b_warpx4<CG>(sfa_t + 8, dsb + j * (SFB_BYTES >> 4) + (512 >> 4));
 #pragma unroll
-                        for (uint32_t kk = 0; kk < BK / 32; ++kk) {
-                            mma_f8<CG>(tmem, da + 2 * kk, db + 2 * kk, p.idesc_tensor, (kt | kk) != 0);
+                                for (uint32_t kk = 0; kk < BK / 32; ++kk) {
+                                    mma_mxf8<CG>(tmem, dja + 2 * kk, djb + 2 * kk,
+                                                 idesc_mxf8(BM * CG, BN, kk), sfa_t, sfa_t + 4, acc);
+                                    acc = 1;
+                                }
+                            } else {
+#pragma unroll
+                                for (uint32_t kk = 0; kk < BK / 32; ++kk) {
+                                    mma_f8<CG>(tmem, dja + 2 * kk, djb + 2 * kk, p.idesc_tensor, acc);
+                                    acc = 1;
+                                }
+                            }
                         }
                     }
-                    // the stage is free in both CTAs once these MMAs completed
-                    if constexpr (PAIR) tc_commit_multicast<CG>(bar(BAR_EMPTY + stage), kPairMask);
-                    else tc_commit<CG>(bar(BAR_EMPTY + stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    // the slot pair is free in both CTAs once these MMAs completed
+                    if constexpr (PAIR) tc_commit_multicast<CG>(bar(BAR_EMPTY + pb), kPairMask);
+                    else tc_commit<CG>(bar(BAR_EMPTY + pb));
+                    if (++pb == NB) {
+                        pb = 0;
                         phase ^= 1u;
+                        da = desc_a0;
+                        db = desc_b0;
+                        dsa = sfa_d0;
+                        dsb = sfb_d0;
+                        sft = sf_t0;
+                    } else {
+                        da += kPairA;
+                        db += kPairB;
+                        dsa += kPairSfa;
+                        dsb += kPairSfb;
+                        sft += kPairCols;
                     }
                 }
                 if (!ok) break;
@@ -405,7 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
         // ------------------------------------------------ epilogue
         const int quarter = warp & 3;        // TMEM lanes this warp may read
-        const int half = (warp - 2) >> 2;    // which 128 accumulator columns
+        const int half = (warp - 2) >> 2;    // which 128 accumulator columns (warps 2-9)
         const uint32_t empty_bar = PAIR ? mapa_shared(bar(BAR_TMEM_EMPTY), 0) : bar(BAR_TMEM_EMPTY);
         float alpha = 1.0f;
         if constexpr (!MX) alpha = __fdiv_rn(1.0f, *p.s_a) * __fdiv_rn(1.0f, *p.s_b);
@@ -430,30 +491,72 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (PAIR) mbar_arrive_cluster(empty_bar);
                 else mbar_arrive(empty_bar);
             }
-            const int64_t row = tl.a_row + quarter * 32 + lane;
-            if (tl.a_valid && row < tl.row_end) {
-                uint16_t* crow = p.c + row * p.ldc;
-                const int64_t col0 = static_cast<int64_t>(tl.n_tile) * BN + half * 128;
+            if constexpr (!GROUPED) {
+                // BF16 through a swizzled 32 x 32 staging tile and TMA stores:
+                // lane = row; 16-byte chunk j of a 64-byte row goes to chunk
+                // j ^ ((row >> 1) & 3), the 64-byte swizzle the store undoes,
+                // which also keeps each 8-lane phase on distinct banks
+                const uint32_t stile = sbase + C::OFF_EPI + (warp - 2) * EPI_TILE_BYTES;
+                const uint32_t srow = stile + lane * 64;
+                const uint32_t sw = (lane >> 1) & 3;
+                if (tl.a_valid) {
+                    const int32_t y = static_cast<int32_t>(tl.a_row + quarter * 32);
+                    const int32_t x0 = tl.n_tile * BN + half * 128;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int64_t col = col0 + j * 8;
-                    if (col < p.N) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * alpha,
-                                          __uint_as_float(v[8 * j + 1]) * alpha);
-                        o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * alpha,
-                                          __uint_as_float(v[8 * j + 3]) * alpha);
-                        o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * alpha,
-                                          __uint_as_float(v[8 * j + 5]) * alpha);
-                        o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * alpha,
-                                          __uint_as_float(v[8 * j + 7]) * alpha);
-                        // evict-first: C streams out to HBM while the GEMM
-                        // runs instead of lingering in L2 as dirty lines
-                        __stcs(reinterpret_cast<uint4*>(crow + col), o);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = pack_bf16x2(__uint_as_float(v[32 * c + 2 * i]) * alpha,
+                                               __uint_as_float(v[32 * c + 2 * i + 1]) * alpha);
+                        if (lane == 0) bulk_wait_group_read0();  // the tile is free again
+                        __syncwarp();
+#pragma unroll
+                        for (uint32_t j = 0; j < 4; ++j) {
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             srow + 16 * (j ^ sw)),
+                                         "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]),
+                                         "r"(w[4 * j + 3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_c, stile, x0 + 32 * c, y);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+            } else {
+                const int64_t row = tl.a_row + quarter * 32 + lane;
+                if (tl.a_valid && row < tl.row_end) {
+                    uint16_t* crow = p.c + row * p.ldc;
+                    const int64_t col0 = static_cast<int64_t>(tl.n_tile) * BN + half * 128;
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t col = col0 + j * 8;
+                        if (col < p.N) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * alpha,
+                                              __uint_as_float(v[8 * j + 1]) * alpha);
+                            o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * alpha,
+                                              __uint_as_float(v[8 * j + 3]) * alpha);
+                            o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * alpha,
+                                              __uint_as_float(v[8 * j + 5]) * alpha);
+                            o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * alpha,
+                                              __uint_as_float(v[8 * j + 7]) * alpha);
+                            // evict-first: C streams out to HBM while the GEMM
+                            // runs instead of lingering in L2 as dirty lines
+                            __stcs(reinterpret_cast<uint4*>(crow + col), o);
+                        }
                     }
                 }
             }
             acc_phase ^= 1u;
+        }
+        if constexpr (!GROUPED) {
+            if (lane == 0) bulk_wait_group0();  // every store of C has completed
+            __syncwarp();
         }
     }
 
@@ -493,7 +596,8 @@ constexpr int kMaxDevices = 64;
 
 template <bool MX, bool GROUPED, bool PAIR>
 cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                          const CUtensorMap& tsb, const KParams& p, int64_t units, cudaStream_t s) {
+                          const CUtensorMap& tsb, const CUtensorMap& tc, const KParams& p,
+                          int64_t units, cudaStream_t s) {
     using C = Cfg<PAIR>;
     static std::atomic<int> resident[kMaxDevices];  // 0 = not yet queried
     const uint32_t smem = (GROUPED ? C::SMEM_GROUPED : C::SMEM_PLAIN) + 1024;
@@ -529,7 +633,7 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     }
     const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, max_clusters));
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::CG), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, k, ta, tb, tsa, tsb, p);
+    e = cudaLaunchKernelEx(&cfg, k, ta, tb, tsa, tsb, tc, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -575,6 +679,11 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     }
     p.c = g.c;
     p.ldc = g.ldc;
+    CUtensorMap tc = ta;  // grouped: unused (C rows of other experts must not be touched)
+    if (!grouped &&
+        !encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
+                              CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     p.offsets = g.offsets;
     p.groups = g.groups;
     p.wait_limit_ns = wait_limit_ns();
@@ -584,10 +693,10 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
         ? (static_cast<int64_t>(p.num_m_tiles) / C::CG + g.groups + 1) * p.num_n_tiles
         : static_cast<int64_t>(p.num_m_groups) * p.num_n_tiles;
     if (mx) {
-        return grouped ? launch_kernel<true, true, kPair>(ta, tb, tsa, tsb, p, units, s)
-                       : launch_kernel<true, false, kPair>(ta, tb, tsa, tsb, p, units, s);
+        return grouped ? launch_kernel<true, true, kPair>(ta, tb, tsa, tsb, tc, p, units, s)
+                       : launch_kernel<true, false, kPair>(ta, tb, tsa, tsb, tc, p, units, s);
     }
-    return launch_kernel<false, false, kPair>(ta, tb, tsa, tsb, p, units, s);
+    return launch_kernel<false, false, kPair>(ta, tb, tsa, tsb, tc, p, units, s);
 }
 
 cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc,
