@@ -143,10 +143,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
+// Arrive on an mbarrier that may live in another CTA of the cluster
+// (default release semantics at CTA scope).  Used to hand TMEM back to the
+// MMA issuer: the TMEM reads are ordered before the arrive by
+// tcgen05.fence::before_thread_sync, so no cluster-scope release (which
+// stalls the warp until its earlier shared-memory writes are visible
+// cluster-wide) is needed.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 // 2D tiled load into this CTA's shared memory whose completion is signalled
