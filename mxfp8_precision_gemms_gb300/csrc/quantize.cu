@@ -471,40 +471,53 @@ __device__ __forceinline__ float2 fp8x2_to_f32(uint32_t codes) {
 
 // Requantization to a shared scale (FP8-LM Section 2.1, Eq. 4-5): q'' =
 // FP8(fp32(s_out * fp32(decode(q) / s_in))), in the equation's order;
-// accumulates the saturated count (zeroed before the launch).
+// accumulates the saturated count (zeroed before the launch).  An FP8 input
+// has 256 codes, so every CTA first evaluates that expression once per code
+// into a shared-memory table (the division correctly rounded, as stated) and
+// then maps bytes through the table: the same result for every byte at a
+// fraction of the arithmetic.
 template <int FIN, int FOUT>
 __global__ void __launch_bounds__(256)
     requantize_kernel(const uint8_t* __restrict__ q_in, int64_t n, const float* s_in_p,
                       const float* s_out_p, uint8_t* __restrict__ q_out, unsigned long long* sat) {
-    const float s_in = *s_in_p, s_out = *s_out_p;
+    __shared__ uint32_t lut[256];  // one output code per input code, widened to 32 bits
+    {
+        const float s_in = *s_in_p, s_out = *s_out_p;
+        const uint32_t c = threadIdx.x;  // blockDim.x == 256
+        const float v = fp8x2_to_f32<FIN>(c).x;
+        const float y = __fmul_rn(s_out, __fdiv_rn(v, s_in));
+        lut[c] = cvt_fp8x2<FOUT>(y, 0.0f) & 0xFFu;
+    }
+    __syncthreads();
+    constexpr uint32_t kMaxCode = FOUT == FP8_E4M3 ? 0x7Eu : 0x7Bu;
     const int64_t n16 = n / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const uint4* in16 = reinterpret_cast<const uint4*>(q_in);
     uint32_t cnt = 0;
+    auto map4 = [&](uint32_t w) {
+        const uint32_t o = lut[w & 0xFFu] | (lut[(w >> 8) & 0xFFu] << 8) |
+                           (lut[(w >> 16) & 0xFFu] << 16) | (lut[w >> 24] << 24);
+        // bytes equal to the largest finite code (either sign): zero bytes of x
+        const uint32_t x = (o & 0x7F7F7F7Fu) ^ (kMaxCode * 0x01010101u);
+        const uint32_t z = ~(((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x | 0x7F7F7F7Fu);
+        cnt += __popc(z);
+        return o;
+    };
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
          i += stride) {
-        const uint4 v = in16[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 a = fp8x2_to_f32<FIN>(w[k] & 0xFFFFu);
-            const float2 b = fp8x2_to_f32<FIN>(w[k] >> 16);
-            const float y0 = __fmul_rn(s_out, __fdiv_rn(a.x, s_in));
-            const float y1 = __fmul_rn(s_out, __fdiv_rn(a.y, s_in));
-            const float y2 = __fmul_rn(s_out, __fdiv_rn(b.x, s_in));
-            const float y3 = __fmul_rn(s_out, __fdiv_rn(b.y, s_in));
-            cnt += saturates<FOUT>(y0) + saturates<FOUT>(y1) + saturates<FOUT>(y2) + saturates<FOUT>(y3);
-            o[k] = cvt_fp8x2<FOUT>(y0, y1) | (cvt_fp8x2<FOUT>(y2, y3) << 16);
-        }
-        reinterpret_cast<uint4*>(q_out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 v = __ldcs(in16 + i);
+        uint4 o;
+        o.x = map4(v.x);
+        o.y = map4(v.y);
+        o.z = map4(v.z);
+        o.w = map4(v.w);
+        reinterpret_cast<uint4*>(q_out)[i] = o;
     }
     for (int64_t t = n16 * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
          t += stride) {
-        const float2 a = fp8x2_to_f32<FIN>(q_in[t]);
-        const float y = __fmul_rn(s_out, __fdiv_rn(a.x, s_in));
-        cnt += saturates<FOUT>(y);
-        q_out[t] = static_cast<uint8_t>(cvt_fp8x2<FOUT>(y, 0.0f) & 0xFFu);
+        const uint32_t o = lut[q_in[t]];
+        cnt += (o & 0x7Fu) == kMaxCode;
+        q_out[t] = static_cast<uint8_t>(o);
     }
     __shared__ uint32_t red_c[8];
     cnt = warp_sum(cnt);
