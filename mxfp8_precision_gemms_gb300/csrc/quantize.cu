@@ -196,6 +196,121 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Rowwise + colwise (or colwise only) MX quantization of a 128 x 128 tile
+// staged by TMA: two 64-column boxes with 128-byte swizzle (16-byte chunk k
+// of a 128-byte half-row r sits at chunk k ^ (r % 8)), so both access
+// patterns below are free of bank conflicts.
+//   colwise: thread t owns columns 4g..4g+3 (g = t % 32) of the 32-row block
+//            j = t / 32, read as 32 64-bit loads (two BF16 pairs per row);
+//            each column's 32 E4M3 bytes are one output row segment of q_col.
+//   rowwise: thread t owns tile row t, its four 32-value blocks read as
+//            16-byte chunks.
+// The E8M0 rule and packing are the row kernel's; 128 threads per CTA.
+constexpr int kTileThreads = 128;
+constexpr uint32_t kTileSmem = kTile * kTile * 2;
+
+template <bool ROW, bool FLOOR>
+__global__ void __launch_bounds__(kTileThreads)
+    quantize_mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, QuantMxArgs a,
+                            int64_t nkc_row, int64_t nkc_col, uint64_t limit_ns, bool v8) {
+    extern __shared__ uint8_t tile_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    uint8_t* tile = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(tile_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t st = smem_u32(tile), bb = smem_u32(&bar);
+    const int tid = threadIdx.x;
+    const int64_t rt = blockIdx.x, ct = blockIdx.y;
+    if (tid == 0) {
+        mbar_init(bb, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bb, kTileSmem);
+        tma_load_2d(st, &tm_x, bb, static_cast<int32_t>(ct * kTile), static_cast<int32_t>(rt * kTile));
+        tma_load_2d(st + kTileSmem / 2, &tm_x, bb, static_cast<int32_t>(ct * kTile + 64),
+                    static_cast<int32_t>(rt * kTile));
+    }
+    const int never = 0;
+    if (!mbar_wait(bb, 0, limit_ns, &never)) {
+        if (tid == 0) record_status(MXFP8_ERR_TIMEOUT);
+        mbar_wait(bb, 0, limit_ns, &never);  // the copy may still land: give it time
+        return;
+    }
+    // 16-byte chunk k (0..15) of tile row r
+    auto chunk_addr = [&](int r, int k) {
+        return st + (k >> 3) * (kTileSmem / 2) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
+    };
+
+    if constexpr (ROW) {
+        const int r = tid;
+        const int64_t row = rt * kTile + r;
+        uint8_t* s_tile = a.s_row + (rt * nkc_row + ct) * 512;
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
+                             : "r"(chunk_addr(r, 4 * b + k)));
+            }
+            const int64_t col = ct * kTile + 32 * b;
+            uint8_t byte;
+            mx_block32<FLOOR>(w, (row < a.rows && col < a.cols) ? a.q_row + row * a.cols + col : nullptr,
+                              &byte, v8);
+            bytes |= static_cast<uint32_t>(byte) << (8 * b);
+        }
+        *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = bytes;
+    }
+
+    // colwise
+    {
+        const int g = tid & 31, j = tid >> 5;
+        uint32_t lo[32], hi[32];  // columns 4g, 4g+1 (lo) and 4g+2, 4g+3 (hi) of rows 32j + i
+        const int k = g >> 1;     // 16-byte chunk holding this column group
+        const uint32_t sub = (g & 1) * 8;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * j + i;
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                         : "=r"(lo[i]), "=r"(hi[i])
+                         : "r"(chunk_addr(r, k) + sub));
+        }
+        uint32_t mlo = 0, mhi = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            mlo = max_u16x2(mlo, lo[i] & 0x7FFF7FFFu);
+            mhi = max_u16x2(mhi, hi[i] & 0x7FFF7FFFu);
+        }
+        const uint32_t bc[4] = {e8m0_byte(mlo & 0xFFFFu, FLOOR), e8m0_byte(mlo >> 16, FLOOR),
+                                e8m0_byte(mhi & 0xFFFFu, FLOOR), e8m0_byte(mhi >> 16, FLOOR)};
+        const int64_t r0 = rt * kTile + 32 * j;  // output column (an input row)
+        uint8_t* s_tile = a.s_col + (ct * nkc_col + rt) * 512;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t* src = c < 2 ? lo : hi;
+            const bool high = c & 1;
+            uint32_t q[8];
+            if (bc[c] == 0xFFu) {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) q[t] = 0x7F7F7F7Fu;
+            } else {
+                const float f = inv_scale(bc[c]);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    q[t] = high ? quant4_half<true>(src[4 * t], src[4 * t + 1], src[4 * t + 2], src[4 * t + 3], f)
+                                : quant4_half<false>(src[4 * t], src[4 * t + 1], src[4 * t + 2], src[4 * t + 3], f);
+                }
+            }
+            const int64_t k0 = ct * kTile + 4 * g + c;  // output row (an input column)
+            if (k0 < a.cols && r0 < a.rows) st32(a.q_col + k0 * a.rows + r0, q, v8);
+            s_tile[swz_word(4 * g + c) + j] = static_cast<uint8_t>(bc[c]);
+        }
+    }
+}
+
 // ---------------------------------------------------------- per-tensor --
 
 __device__ __forceinline__ uint32_t warp_max(uint32_t m) {
@@ -557,10 +672,33 @@ cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
 
 }  // namespace
 
+template <bool ROW, bool FLOOR>
+cudaError_t launch_mx_tile(const QuantMxArgs& a, const CUtensorMap& map, cudaStream_t s) {
+    const int64_t row_tiles = (a.rows + kTile - 1) / kTile;
+    const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
+    if (col_tiles > 65535 || row_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const bool v8 = (reinterpret_cast<uintptr_t>(a.q_col) % 32 == 0) &&
+                    (!ROW || reinterpret_cast<uintptr_t>(a.q_row) % 32 == 0);
+    dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
+    quantize_mx_tile_kernel<ROW, FLOOR><<<grid, kTileThreads, kTileSmem + 1024, s>>>(
+        map, a, col_tiles, row_tiles, wait_limit_ns(), v8);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s) {
     const bool row = a.flags & MX_ROWWISE, col = a.flags & MX_COLWISE;
     const bool fl = a.flags & MX_SCALE_FLOOR;
     const int64_t row_tiles = (a.rows + kTile - 1) / kTile;
+    if (col && a.rows > 0 && a.cols > 0) {
+        // colwise (with or without rowwise): TMA-staged tile kernel; the tensor
+        // map wants a 16-byte aligned base and row stride (checked by the API)
+        CUtensorMap map;
+        if (encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.rows, a.cols,
+                                 a.ld * 2, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) {
+            if (row) return fl ? launch_mx_tile<true, true>(a, map, s) : launch_mx_tile<true, false>(a, map, s);
+            return fl ? launch_mx_tile<false, true>(a, map, s) : launch_mx_tile<false, false>(a, map, s);
+        }
+    }
     if (row && col) {
         return fl ? launch_mx<true, true, true, false>(a, row_tiles, s)
                   : launch_mx<true, true, false, false>(a, row_tiles, s);
