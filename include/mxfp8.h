@@ -244,6 +244,27 @@ mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
                               void* c_bf16, int64_t ldc, mxfp8_stream_t stream);
 
 /*
+ * fp8_quantize_tensor_batch - fp8_quantize_tensor for `count` tensors in one
+ * cooperative launch with one grid barrier (a linear layer's activation and
+ * weight, say; "3.8 Mixed Precision, bf16 & FP8 Training", exercise 6 casts
+ * both operands before the FP8 matmul).  Each tensor t gets its own amax,
+ * scale and payload exactly as fp8_quantize_tensor computes them.
+ *
+ *  count            1 .. 16.
+ *  x_bf16, n, q     HOST arrays of count entries: device pointers to the
+ *                   BF16 inputs and payload outputs (16-byte aligned) and the
+ *                   element counts (n[t] == 0 allowed).
+ *  amax_dev         device fp32[count], written.
+ *  scale_dev        device fp32[count], written.
+ *  workspace        device scratch of mxfp8_tensor_workspace_bytes() bytes,
+ *                   16-byte aligned (zeroed by the library on the stream);
+ *                   calls sharing one workspace must not overlap on the GPU.
+ */
+mxfp8_status fp8_quantize_tensor_batch(int32_t count, const void* const* x_bf16, const int64_t* n,
+                                       int fmt, float* amax_dev, float* scale_dev, void* const* q,
+                                       void* workspace, mxfp8_stream_t stream);
+
+/*
  * fp8_quantize_tensor_scaled - per-tensor FP8 cast with a scale the caller
  * already holds on the device ("3.8 Mixed Precision, bf16 & FP8 Training",
  * "Per-tensor scaling and the delayed-scaling recipe": the cast uses a scale

@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_mx_grouped": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
+                "fp8_quantize_tensor_batch": (st, [I32, P, P, I, P, P, P, P, P]),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
                 "fp8_quantize_tensor_scaled": (st, [P, I64, I, P, P, P, P, P]),
                 "fp8_quantize_tensor_delayed": (st, [P, I64, I, ctypes.c_float, P, I32, P, P, P, P, P, P]),
@@ -214,6 +215,31 @@ def fp8_requantize_tensor(q: torch.Tensor, scale_in: torch.Tensor, scale_out: to
     _check(lib().fp8_requantize_tensor(_ptr(q), q.numel(), fmt_in, _ptr(scale_in), _ptr(scale_out), fmt_out,
                                        _ptr(out), _ptr(sat_count), _stream(stream)))
     return out, sat_count
+
+
+def fp8_quantize_tensor_batch(xs, fmt: int = FP8_E4M3, workspace=None, qs=None, amax=None, scale=None,
+                              stream=None):
+    """Per-tensor FP8 quantization of several BF16 tensors in one launch.
+
+    Returns (list of q, amax fp32[count], scale fp32[count]).  ``workspace``:
+    a device uint8 tensor of ``mxfp8_tensor_workspace_bytes()`` bytes."""
+    count = len(xs)
+    dev = xs[0].device
+    for x in xs:
+        assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    _need_cuda(*xs, workspace)
+    qs = qs if qs is not None else [torch.empty(x.shape, dtype=torch.uint8, device=dev) for x in xs]
+    amax = amax if amax is not None else torch.empty(count, dtype=torch.float32, device=dev)
+    scale = scale if scale is not None else torch.empty(count, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(mxfp8_tensor_workspace_bytes(), dtype=torch.uint8, device=dev)
+    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
+    qp = (ctypes.c_void_p * count)(*[q.data_ptr() for q in qs])
+    ns = (ctypes.c_int64 * count)(*[x.numel() for x in xs])
+    _check(lib().fp8_quantize_tensor_batch(count, ctypes.cast(xp, ctypes.c_void_p), ctypes.cast(ns, ctypes.c_void_p),
+                                           fmt, _ptr(amax), _ptr(scale), ctypes.cast(qp, ctypes.c_void_p),
+                                           _ptr(workspace), _stream(stream)))
+    return qs, amax, scale
 
 
 def mxfp8_tensor_workspace_bytes() -> int:

@@ -370,6 +370,34 @@ mxfp8_status fp8_quantize_tensor(const void* x_bf16, int64_t n, int fmt, float* 
                        "fp8_quantize_tensor launch");
 }
 
+mxfp8_status fp8_quantize_tensor_batch(int32_t count, const void* const* x_bf16, const int64_t* n,
+                                       int fmt, float* amax_dev, float* scale_dev, void* const* q,
+                                       void* workspace, mxfp8_stream_t stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);
+    if (count < 1 || count > kMaxBatch)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "count must be in [1, %d]", kMaxBatch);
+    if (!x_bf16 || !n || !q) return fail(MXFP8_ERR_INVALID_ARG, "x, n or q array is NULL");
+    if (!amax_dev || !scale_dev || !workspace)
+        return fail(MXFP8_ERR_INVALID_ARG, "amax, scale or workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u) ||
+        !aligned16(workspace))
+        return fail(MXFP8_ERR_MISALIGNED, "amax/scale/workspace misaligned");
+    const uint16_t* xs[kMaxBatch];
+    uint8_t* qs[kMaxBatch];
+    for (int t = 0; t < count; ++t) {
+        if (n[t] < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size (tensor %d)", t);
+        if (n[t] > 0 && (!x_bf16[t] || !q[t])) return fail(MXFP8_ERR_INVALID_ARG, "x or q of tensor %d is NULL", t);
+        if (n[t] > 0 && (!aligned16(x_bf16[t]) || !aligned16(q[t])))
+            return fail(MXFP8_ERR_MISALIGNED, "x or q of tensor %d not 16-byte aligned", t);
+        xs[t] = static_cast<const uint16_t*>(x_bf16[t]);
+        qs[t] = static_cast<uint8_t*>(q[t]);
+    }
+    return cuda_result(launch_quantize_tensor_batch(count, xs, n, fmt, amax_dev, scale_dev, qs,
+                                                    static_cast<uint32_t*>(workspace),
+                                                    reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_tensor_batch launch");
+}
+
 mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt, float* amax_dev,
                                          float* scale_dev, void* q, mxfp8_stream_t stream) {
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(MXFP8_ERR_INVALID_ARG, "unknown format %d", fmt);

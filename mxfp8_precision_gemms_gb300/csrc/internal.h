@@ -29,7 +29,17 @@ cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
                                    float* scale, uint8_t* q, cudaStream_t s);
-// Single cooperative launch; ws: 2 uint32 of device scratch (zeroed here).
+// Tensors one batched per-tensor launch accepts.
+constexpr int kMaxBatch = 16;
+
+// Single cooperative launch for `count` tensors (amax[t], scale[t] are
+// consecutive device floats); ws: kMaxBatch + 1 uint32 of device scratch
+// (zeroed here).
+cudaError_t launch_quantize_tensor_batch(int count, const uint16_t* const* x, const int64_t* n,
+                                         int fmt, float* amax, float* scale, uint8_t* const* q,
+                                         uint32_t* ws, cudaStream_t s);
+
+// Single cooperative launch; ws: kMaxBatch + 1 uint32 of device scratch (zeroed here).
 // The scratch it needs, whatever n is: mxfp8_tensor_workspace_bytes().
 cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
                                          float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s);

@@ -376,13 +376,23 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Single-launch per-tensor quantization: every CTA reduces its share of
-// |x| into ws[0] (atomicMax on the fp32 bit pattern), the CTAs meet at a
-// grid barrier (ws[1] counts arrivals; the launch is cooperative so all CTAs
-// are resident; the wait is bounded), then each CTA recomputes the scale and
-// casts its share, re-reading x (from L2 when the tensor fits there).
-// ws[0..1] must be zero at launch.
+// Single-launch per-tensor quantization of a batch of tensors (one grid
+// barrier for all of them, e.g. a linear layer's activation and weight):
+// every CTA reduces its share of |x_t| into ws[t] (atomicMax on the fp32 bit
+// pattern), the CTAs meet at a grid barrier (ws[kMaxBatch] counts arrivals;
+// the launch is cooperative so all CTAs are resident; the wait is bounded),
+// then each CTA computes every tensor's scale and casts its share, re-reading
+// x_t (from L2 when it fits there).  ws[0 .. kMaxBatch] must be zero at launch.
 constexpr int kFusedThreads = 512;
+
+struct TensorBatch {
+    const uint16_t* x[kMaxBatch];
+    uint8_t* q[kMaxBatch];
+    float* amax[kMaxBatch];   // device scalars (outputs)
+    float* scale[kMaxBatch];
+    int64_t n[kMaxBatch];
+    int count;
+};
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
@@ -390,16 +400,11 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kFusedThreads)
-    tensor_quant_fused_kernel(const uint16_t* __restrict__ x, int64_t n, float* amax_out,
-                              float* scale_out, uint8_t* __restrict__ q, uint32_t* ws,
-                              uint64_t limit_ns) {
-    __shared__ uint32_t red[kFusedThreads / 32];
-    __shared__ int s_ok;
+// |x| maximum of one tensor over this thread's grid-stride share, as BF16
+// magnitude bits.
+__device__ __forceinline__ uint32_t amax_share(const uint16_t* __restrict__ x, int64_t n,
+                                               int64_t first, int64_t stride) {
     const int64_t n8 = n / 8;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     uint32_t m = 0;
     int64_t i = first;
@@ -410,21 +415,36 @@ __global__ void __launch_bounds__(kFusedThreads)
     }
     for (; i < n8; i += stride) m = max(m, amax8(x8[i]));
     for (int64_t t = n8 * 8 + first; t < n; t += stride) m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
-    m = warp_max(m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    return m;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kFusedThreads)
+    tensor_quant_batch_kernel(const TensorBatch b, uint32_t* ws, uint64_t limit_ns) {
+    __shared__ uint32_t red[kMaxBatch][kFusedThreads / 32];
+    __shared__ int s_ok;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int t = 0; t < b.count; ++t) {
+        const uint32_t m = warp_max(amax_share(b.x[t], b.n[t], first, stride));
+        if (lane == 0) red[t][warp] = m;
+    }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        m = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0u;
-        m = warp_max(m);
-        if (threadIdx.x == 0) {
-            if (m) atomicMax(ws, m << 16);
+    if (warp == 0) {
+        for (int t = 0; t < b.count; ++t) {
+            uint32_t m = lane < kFusedThreads / 32 ? red[t][lane] : 0u;
+            m = warp_max(m);
+            if (lane == 0 && m) atomicMax(ws + t, m << 16);
+        }
+        if (lane == 0) {
             __threadfence();
-            atomicAdd(ws + 1, 1u);
-            bool ok = ld_acquire_gpu(ws + 1) >= gridDim.x;
+            atomicAdd(ws + kMaxBatch, 1u);
+            bool ok = ld_acquire_gpu(ws + kMaxBatch) >= gridDim.x;
             if (!ok) {
                 const uint64_t t0 = globaltimer_ns();
                 for (uint32_t it = 1;; ++it) {
-                    if (ld_acquire_gpu(ws + 1) >= gridDim.x) {
+                    if (ld_acquire_gpu(ws + kMaxBatch) >= gridDim.x) {
                         ok = true;
                         break;
                     }
@@ -439,25 +459,31 @@ __global__ void __launch_bounds__(kFusedThreads)
         if (threadIdx.x == 0) record_status(MXFP8_ERR_TIMEOUT);
         return;
     }
-    const float amax = __uint_as_float(ld_acquire_gpu(ws));
     const float fmax = FMT == FP8_E4M3 ? 448.0f : 57344.0f;
-    const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *amax_out = amax;
-        *scale_out = s;
-    }
-    for (int64_t j = first; j < n8; j += stride) {
-        const uint4 v = x8[j];
-        uint2 o;
-        o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
-              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
-        o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
-              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
-        reinterpret_cast<uint2*>(q)[j] = o;
-    }
-    for (int64_t t = n8 * 8 + first; t < n; t += stride) {
-        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[t]) << 16), s);
-        q[t] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+    for (int t = 0; t < b.count; ++t) {
+        const float amax = __uint_as_float(ld_acquire_gpu(ws + t));
+        const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            *b.amax[t] = amax;
+            *b.scale[t] = s;
+        }
+        const uint16_t* __restrict__ x = b.x[t];
+        uint8_t* __restrict__ q = b.q[t];
+        const int64_t n = b.n[t], n8 = n / 8;
+        const uint4* x8 = reinterpret_cast<const uint4*>(x);
+        for (int64_t j = first; j < n8; j += stride) {
+            const uint4 v = x8[j];
+            uint2 o;
+            o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
+                  (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
+            o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
+                  (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
+            reinterpret_cast<uint2*>(q)[j] = o;
+        }
+        for (int64_t r = n8 * 8 + first; r < n; r += stride) {
+            const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[r]) << 16), s);
+            q[r] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+        }
     }
 }
 
@@ -735,17 +761,19 @@ cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float*
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
-                                         float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s);
+cudaError_t launch_quantize_tensor_batch(int count, const uint16_t* const* x, const int64_t* n,
+                                         int fmt, float* amax, float* scale, uint8_t* const* q,
+                                         uint32_t* ws, cudaStream_t s) {
+    if (count < 1 || count > kMaxBatch) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(ws, 0, (kMaxBatch + 1) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     // resident blocks per SM, queried once per device and format
     static std::atomic<int> per_sm[2][64];
     const int f = fmt == FP8_E5M2 ? 1 : 0;
-    const void* k = f ? reinterpret_cast<const void*>(tensor_quant_fused_kernel<FP8_E5M2>)
-                      : reinterpret_cast<const void*>(tensor_quant_fused_kernel<FP8_E4M3>);
+    const void* k = f ? reinterpret_cast<const void*>(tensor_quant_batch_kernel<FP8_E5M2>)
+                      : reinterpret_cast<const void*>(tensor_quant_batch_kernel<FP8_E4M3>);
     int bps = dev >= 0 && dev < 64 ? per_sm[f][dev].load() : 0;
     if (bps <= 0) {
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, k, kFusedThreads, 0)) != cudaSuccess)
@@ -753,14 +781,29 @@ cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, 
         if (bps <= 0) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < 64) per_sm[f][dev].store(bps);
     }
-    const int64_t chunks = n / 8 + 1;
+    TensorBatch b{};
+    int64_t chunks = 1;
+    for (int t = 0; t < count; ++t) {
+        b.x[t] = x[t];
+        b.q[t] = q[t];
+        b.amax[t] = amax + t;
+        b.scale[t] = scale + t;
+        b.n[t] = n[t];
+        chunks = std::max<int64_t>(chunks, n[t] / 8 + 1);
+    }
+    b.count = count;
     const int64_t resident = static_cast<int64_t>(sm_count_current_device()) * bps;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((chunks + kFusedThreads - 1) / kFusedThreads, resident)));
     uint64_t limit = wait_limit_ns();
-    void* args[] = {const_cast<uint16_t**>(&x), &n, &amax, &scale, &q, &ws, &limit};
+    void* args[] = {&b, &ws, &limit};
     e = cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kFusedThreads), args, 0, s);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, float* amax,
+                                         float* scale, uint8_t* q, uint32_t* ws, cudaStream_t s) {
+    return launch_quantize_tensor_batch(1, &x, &n, fmt, amax, scale, &q, ws, s);
 }
 
 // Scratch of fp8_quantize_tensor_noalloc: a file-scope device array, so that

@@ -70,6 +70,21 @@ def test_host_validation(lib):
     assert lib.fp8_quantize_tensor(P + 1, 100, 0, P, P, P, None, None) == m.MXFP8_ERR_MISALIGNED
     assert lib.fp8_quantize_tensor(P, 100, 0, P, P, P, P + 8, None) == m.MXFP8_ERR_MISALIGNED
     assert lib.mxfp8_tensor_workspace_bytes() >= 8
+    # batched per-tensor
+    B = lib.fp8_quantize_tensor_batch
+    xs = (ctypes.c_void_p * 17)(*([P] * 17))
+    ns = (ctypes.c_int64 * 17)(*([64] * 17))
+    arr = lambda a: ctypes.cast(a, ctypes.c_void_p)
+    assert B(0, arr(xs), arr(ns), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert B(17, arr(xs), arr(ns), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert B(2, arr(xs), arr(ns), 3, P, P, arr(xs), P, None) == m.MXFP8_ERR_INVALID_ARG
+    assert B(2, None, arr(ns), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_INVALID_ARG
+    assert B(2, arr(xs), arr(ns), 0, P, P, arr(xs), None, None) == m.MXFP8_ERR_INVALID_ARG
+    assert B(2, arr(xs), arr(ns), 0, P, P, arr(xs), P + 4, None) == m.MXFP8_ERR_MISALIGNED
+    bad = (ctypes.c_void_p * 2)(P, P + 2)
+    assert B(2, arr(bad), arr(ns), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_MISALIGNED
+    neg = (ctypes.c_int64 * 2)(64, -1)
+    assert B(2, arr(xs), arr(neg), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_INVALID_ARG
     # GEMM
     G = lib.fp8_scaled_gemm
     assert G(5, 0, 0, P, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG

@@ -202,6 +202,43 @@ def test_quantize_grouped_bad_offsets_recorded(bad):
     assert (host(q) == 0x5A).all() and (host(s) == 0x5A).all()
 
 
+@pytest.mark.parametrize("fmt", [m.FP8_E4M3, m.FP8_E5M2])
+def test_quantize_tensor_batch_matches_oracle(fmt):
+    """Several tensors in one launch: each gets the amax, scale and payload
+    the single-tensor rule gives it (including an empty and an odd-sized one)."""
+    w = workloads.tensor4096(seed=3, device="cpu", m=512, n=384, k=1024)
+    cases = [workloads.bits(w["X"]).reshape(-1), workloads.bits(w["W"]).reshape(-1),
+             np.zeros((0,), np.uint16), random_bits((100003,), "loguniform", seed=5).reshape(-1),
+             workloads.bits((torch.randn(4000) * 1e-30).to(torch.bfloat16)),
+             np.zeros((4096,), np.uint16)]
+    xs = [to_dev_bf16(b) for b in cases]
+    qs = [filled(b.size, 0xA5) for b in cases]
+    amax = filled(len(cases), -1.0, torch.float32)
+    scale = filled(len(cases), -1.0, torch.float32)
+    ws = filled(m.mxfp8_tensor_workspace_bytes(), 0x77)
+    for _ in range(2):
+        m.fp8_quantize_tensor_batch(xs, fmt, workspace=ws, qs=qs, amax=amax, scale=scale)
+        assert_ok()
+    ha, hs = host(amax).view(np.uint32), host(scale).view(np.uint32)
+    for t, b in enumerate(cases):
+        wa, wsc, wq = oracle.quantize_tensor(b, fmt)
+        assert np.array_equal(host(qs[t]), wq.reshape(-1)), t
+        assert ha[t] == np.float32(wa).view(np.uint32), t
+        assert hs[t] == np.float32(wsc).view(np.uint32), t
+
+
+def test_quantize_tensor_batch_of_sixteen():
+    """The largest batch: sixteen tensors of different sizes."""
+    cases = [random_bits((1 + 997 * t,), "normal", seed=10 + t).reshape(-1) for t in range(16)]
+    xs = [to_dev_bf16(b) for b in cases]
+    qs, amax, scale = m.fp8_quantize_tensor_batch(xs, m.FP8_E4M3)
+    assert_ok()
+    for t, b in enumerate(cases):
+        wa, wsc, wq = oracle.quantize_tensor(b, m.FP8_E4M3)
+        assert np.array_equal(host(qs[t]), wq.reshape(-1)), t
+        assert float(host(scale)[t]) == np.float32(wsc), t
+
+
 @pytest.mark.parametrize("fused", [False, True], ids=["two_kernels", "single_launch"])
 @pytest.mark.parametrize("fmt", [m.FP8_E4M3, m.FP8_E5M2])
 @pytest.mark.parametrize("case", ["outliers", "loguniform", "tiny", "zeros", "odd", "empty"])
