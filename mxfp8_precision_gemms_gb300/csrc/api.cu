@@ -110,6 +110,21 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
     return r == CUDA_SUCCESS;
 }
 
+bool encode_kchunk_map_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
+                          uint32_t box_rows, uint32_t box_chunks) {
+    if (k % 128) return false;
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 128)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k), 128};
+    const cuuint32_t box[3] = {128, box_rows, box_chunks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace mxfp8
 
 using namespace mxfp8;

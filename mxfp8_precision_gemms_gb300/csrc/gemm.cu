@@ -18,25 +18,34 @@
 // so the same shared memory keeps 6 stages in flight and each staged byte
 // feeds 1.5x the FLOPs.  The kernel is limited by how many bytes can be in
 // flight from L2, not by raw L2 bandwidth (multicasting B across CTAs did
-// not help), which is why the 2-SM form pays.
+// not help), which is why the 2-SM form pays.  Work units run M-group
+// fastest: the resident pairs cover every 256-row group of A for one or two
+// 256-column tiles of B at a time, so each B tile is read by ~32 pairs at
+// once and A stays in L2.  Banded (4-16 M groups) and diagonal orders were
+// 1-27 % slower under a sustained load and drew more power per GEMM.
 //   warp 0       TMA producer (both CTAs): A box, this CTA's half of the B box
-//                (128-byte swizzle) and the 512-byte scale tiles per K step
-//                into a shared-memory ring of slots; one "full" / "empty"
-//                mbarrier pair covers two slots, and every load of both CTAs
-//                completes on the leader CTA's "full" mbarrier.
+//                (128-byte swizzle) and the 512-byte scale tiles into a
+//                shared-memory ring of slots, one slot per K step; one "full" /
+//                "empty" mbarrier pair covers two slots, and every load of both
+//                CTAs completes on the leader CTA's "full" mbarrier.  When K
+//                splits into whole slot pairs each operand's pair is one copy
+//                (3D K-chunk maps for A and B): each TMA instruction costs the
+//                issuing thread 70-80 cycles whatever its size (measured), so
+//                five copies per pair instead of ten.
 //   warp 1       TMEM allocator (both CTAs, collectively) and, in the leader
 //                only, the MMA issuer: per K step tcgen05.cp of the block
 //                scales into TMEM and 4 MMAs of K = 32 (in issue order, so the
 //                MMAs see the scales without a wait), per slot pair one
 //                tcgen05.commit releasing the pair in both CTAs and, after the
-//                last K step, handing the accumulators over.  This thread's
-//                issue rate, not the tensor pipe, is the limit (measured:
-//                about 56 cycles per scale copy and 69 per MMA, plus a wait,
-//                a fence, a commit and address bookkeeping, against 512
-//                cycles of MMA work per K step), hence one barrier per two K
-//                steps and constant-stride address updates.  Moving the
-//                copies to another thread was slower: they then have to be
-//                waited for, and they queue behind the MMAs already issued.
+//                last K step, handing the accumulators over.  Measured in
+//                isolation, each tcgen05 instruction costs the issuing thread
+//                about 45 cycles (the 3 copies + 4 MMAs of a K step: ~315
+//                cycles against 512 of tensor work), a completed try_wait 48
+//                and a commit 46; the pipe stays full only while the thread is
+//                not waiting, hence one barrier per two K steps and
+//                constant-stride address updates.  Moving the copies to another
+//                thread was slower: they then have to be waited for, and they
+//                queue behind the MMAs already issued.
 //   warps 2-9    epilogue (both CTAs): tcgen05.ld of this CTA's 128 x 256 FP32
 //                accumulator, release it to the leader, convert to BF16 and
 //                store while the next tile's main loop runs: through a 2 KB
@@ -125,6 +134,7 @@ struct KParams {
     uint64_t wait_limit_ns;
     int32_t inject_timeout;
     uint32_t idesc_tensor;
+    int32_t merged;              // 1: one copy per operand loads a whole slot pair
 };
 
 // One CTA's share of a work unit: the unit covers CG consecutive 128-row
@@ -182,8 +192,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // tm_a / tm_b: payload boxes (128 x 128 and B_ROWS x 128 bytes, 128-byte
-// swizzle).  tm_sa / tm_sb: the scale arrays seen as rows of 256 bytes,
-// boxes of 2 rows = one 512-byte scale tile (out-of-range tiles read as 0).
+// swizzle); with p.merged, 3D K-chunk maps whose box is SLOTS_PER_BAR such
+// tiles (one copy fills a slot pair).  tm_sa / tm_sb: the scale arrays seen as
+// rows of 256 bytes, boxes of 2 rows = one 512-byte scale tile, or of
+// 2 * SLOTS_PER_BAR rows with p.merged (out-of-range tiles read as 0).
 // tm_c: C as BF16, 32 x 32 boxes with 64-byte swizzle (plain GEMM only; the
 // store clips rows and columns outside M x N).
 template <bool MX, bool GROUPED, bool PAIR>
@@ -315,32 +327,66 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     const uint32_t fb_local = bar(BAR_FULL + pb);
                     if (leader) mbar_arrive_expect_tx(fb_local, kSlotTx * nslots);
-                    for (int j = 0; j < nslots; ++j) {
-                        const int kt = kt0 + j;
-                        const uint32_t slot = pb * SLOTS_PER_BAR + j;
-                        const uint32_t dA = sbase + C::OFF_A + slot * A_BYTES;
-                        const uint32_t dB = sbase + C::OFF_B + slot * C::B_BYTES;
-                        const uint32_t dSA = sbase + C::OFF_SFA + slot * SFA_BYTES;
-                        const uint32_t dSB = sbase + C::OFF_SFB + slot * SFB_BYTES;
-                        const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt));
-                        const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt));
-                        const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
+                    const uint32_t slot0 = pb * SLOTS_PER_BAR;
+                    // B scales of a slot pair: [half 0 of each slot][half 1 of each slot]
+                    const uint32_t dSBp = sbase + C::OFF_SFB + slot0 * SFB_BYTES;
+                    if (p.merged) {
+                        // K % (BK * SLOTS_PER_BAR) == 0: the pair is full and each
+                        // operand's SLOTS_PER_BAR K steps are one box (A, B: 3D K-chunk
+                        // maps; scales: consecutive 512-byte tiles)
+                        const uint32_t dA = sbase + C::OFF_A + slot0 * A_BYTES;
+                        const uint32_t dB = sbase + C::OFF_B + slot0 * C::B_BYTES;
+                        const uint32_t dSA = sbase + C::OFF_SFA + slot0 * SFA_BYTES;
+                        const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt0));
+                        const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt0));
+                        const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt0));
                         if constexpr (PAIR) {
                             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
-                            tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
-                            tma_load_2d_pair(dB, &tm_b, fb, kt * BK, b_row);
+                            tma_load_3d_pair(dA, &tm_a, fb, 0, static_cast<int32_t>(tl.a_row), kt0);
+                            tma_load_3d_pair(dB, &tm_b, fb, 0, b_row, kt0);
                             if constexpr (MX) {
                                 tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
-                                tma_load_2d_pair(dSB, &tm_sb, fb, 0, yb0);
-                                tma_load_2d_pair(dSB + 512, &tm_sb, fb, 0, yb1);
+                                tma_load_2d_pair(dSBp, &tm_sb, fb, 0, yb0);
+                                tma_load_2d_pair(dSBp + SLOTS_PER_BAR * 512, &tm_sb, fb, 0, yb1);
                             }
                         } else {
-                            tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
-                            tma_load_2d(dB, &tm_b, fb_local, kt * BK, b_row);
+                            tma_load_3d(dA, &tm_a, fb_local, 0, static_cast<int32_t>(tl.a_row), kt0);
+                            tma_load_3d(dB, &tm_b, fb_local, 0, b_row, kt0);
                             if constexpr (MX) {
                                 tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
-                                tma_load_2d(dSB, &tm_sb, fb_local, 0, yb0);
-                                tma_load_2d(dSB + 512, &tm_sb, fb_local, 0, yb1);
+                                tma_load_2d(dSBp, &tm_sb, fb_local, 0, yb0);
+                                tma_load_2d(dSBp + SLOTS_PER_BAR * 512, &tm_sb, fb_local, 0, yb1);
+                            }
+                        }
+                    } else {
+                        for (int j = 0; j < nslots; ++j) {
+                            const int kt = kt0 + j;
+                            const uint32_t slot = slot0 + j;
+                            const uint32_t dA = sbase + C::OFF_A + slot * A_BYTES;
+                            const uint32_t dB = sbase + C::OFF_B + slot * C::B_BYTES;
+                            const uint32_t dSA = sbase + C::OFF_SFA + slot * SFA_BYTES;
+                            const uint32_t dSB0 = dSBp + j * 512;
+                            const uint32_t dSB1 = dSBp + (SLOTS_PER_BAR + j) * 512;
+                            const int32_t ya = static_cast<int32_t>(2 * (tl.sfa_tile * p.num_k_tiles + kt));
+                            const int32_t yb0 = static_cast<int32_t>(2 * (sfb_base + kt));
+                            const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
+                            if constexpr (PAIR) {
+                                const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
+                                tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
+                                tma_load_2d_pair(dB, &tm_b, fb, kt * BK, b_row);
+                                if constexpr (MX) {
+                                    tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
+                                    tma_load_2d_pair(dSB0, &tm_sb, fb, 0, yb0);
+                                    tma_load_2d_pair(dSB1, &tm_sb, fb, 0, yb1);
+                                }
+                            } else {
+                                tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
+                                tma_load_2d(dB, &tm_b, fb_local, kt * BK, b_row);
+                                if constexpr (MX) {
+                                    tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
+                                    tma_load_2d(dSB0, &tm_sb, fb_local, 0, yb0);
+                                    tma_load_2d(dSB1, &tm_sb, fb_local, 0, yb1);
+                                }
                             }
                         }
                     }
@@ -418,8 +464,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 // scales of this K step into TMEM; issued in order with
                                 // the MMAs below, which therefore see them
                                 tc_cp_32x128b_warpx4<CG>(sfa_t, dsa + j * (SFA_BYTES >> 4));
-                                tc_cp_32x128b_warpx4<CG>(sfa_t + 4, dsb + j * (SFB_BYTES >> 4));
-                                tc_cp_32x128b_warpx4<CG>(sfa_t + 8, dsb + j * (SFB_BYTES >> 4) + (512 >> 4));
+                                tc_cp_32x128b_warpx4<CG>(sfa_t + 4, dsb + j * (512 >> 4));
+                                tc_cp_32x128b_warpx4<CG>(sfa_t + 8, dsb + (SLOTS_PER_BAR + j) * (512 >> 4));
 #pragma unroll
                                 for (uint32_t kk = 0; kk < BK / 32; ++kk) {
                                     mma_mxf8<CG>(tmem, dja + 2 * kk, djb + 2 * kk,
@@ -658,16 +704,23 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     p.n_scale_tiles = static_cast<int32_t>((g.N + 127) / 128);
     p.sfb_group_chunks = static_cast<int64_t>(p.n_scale_tiles) * p.num_k_tiles;
     CUtensorMap ta, tb, tsa, tsb;
-    if (!make_map(&ta, g.a, g.M, g.K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tb, g.b, b_rows, g.K, BK, C::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+    // whole slot pairs in one copy per operand when K splits into full pairs
+    p.merged = g.K % (BK * SLOTS_PER_BAR) == 0 &&
+               encode_kchunk_map_u8(&ta, g.a, g.M, g.K, BM, SLOTS_PER_BAR) &&
+               encode_kchunk_map_u8(&tb, g.b, b_rows, g.K, C::B_ROWS, SLOTS_PER_BAR);
+    if (!p.merged &&
+        (!make_map(&ta, g.a, g.M, g.K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(&tb, g.b, b_rows, g.K, BK, C::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorInvalidValue;
+    const uint32_t sf_box_rows = p.merged ? 2 * SLOTS_PER_BAR : 2;
     if (mx) {
-        // scale arrays as 256-byte rows; a 512-byte scale tile is a 2-row box
+        // scale arrays as 256-byte rows; a 512-byte scale tile is 2 rows, the
+        // tiles of consecutive K steps are consecutive
         const int64_t a_tiles = grouped ? (g.M + 127) / 128 + g.groups : p.num_m_tiles;
         const int64_t a_chunks = a_tiles * p.num_k_tiles;
         const int64_t b_chunks = (grouped ? g.groups : 1) * p.sfb_group_chunks;
-        if (!make_map(&tsa, g.a_scale, 2 * a_chunks, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !make_map(&tsb, g.b_scale, 2 * b_chunks, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!make_map(&tsa, g.a_scale, 2 * a_chunks, 256, 256, sf_box_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map(&tsb, g.b_scale, 2 * b_chunks, 256, 256, sf_box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
         tsa = ta;  // unused

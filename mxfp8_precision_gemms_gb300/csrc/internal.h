@@ -137,4 +137,10 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
                           int64_t rows, int64_t width, int64_t row_stride_bytes, uint32_t box_w,
                           uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
+// A row-major rows x k byte matrix (row stride k, k % 128 == 0) seen as
+// [k / 128 chunks][rows][128 bytes]: one box of box_rows x box_chunks lands
+// as box_chunks consecutive (box_rows x 128)-byte tiles, 128-byte swizzled.
+bool encode_kchunk_map_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
+                          uint32_t box_rows, uint32_t box_chunks);
+
 }  // namespace mxfp8
