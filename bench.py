@@ -193,18 +193,27 @@ class MlpUp:
         self.sW = torch.empty(m.mxfp8_scale_bytes(self.N, self.K), **u8)
         self.C = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
         self.flops = 2.0 * self.M * self.N * self.K
-        self.launches_per_step = 3
+        self.launches_per_step = 2
         self.lib = m.lib()
+        # host arrays of the batched rowwise quantizer (X and W in one launch)
+        import ctypes
+        self._ct = ctypes
+        self._rows = (ctypes.c_int64 * 2)(self.M, self.N)
+        self._cols = (ctypes.c_int64 * 2)(self.K, self.K)
+        self._qs = (ctypes.c_void_p * 2)(self.qX.data_ptr(), self.qW.data_ptr())
+        self._ss = (ctypes.c_void_p * 2)(self.sX.data_ptr(), self.sW.data_ptr())
+
+    def quantize(self, x_ptr, w_ptr, stream):
+        ct = self._ct
+        xs = (ct.c_void_p * 2)(x_ptr, w_ptr)
+        vp = lambda a: ct.cast(a, ct.c_void_p)
+        _ok(self.lib.fp8_quantize_mx_batch(2, vp(xs), vp(self._rows), vp(self._cols), vp(self._cols),
+                                           self.m.MX_ROWWISE, vp(self._qs), vp(self._ss), stream))
 
     def step(self, timer=None, stream=0):
         L, m = self.lib, self.m
-        e = timer.mark("quantize_x") if timer else None
-        _ok(L.fp8_quantize_mx(self.X.data_ptr(), self.M, self.K, self.K, m.MX_ROWWISE,
-                              self.qX.data_ptr(), self.sX.data_ptr(), None, None, stream))
-        if e: e.record()
-        e = timer.mark("quantize_w") if timer else None
-        _ok(L.fp8_quantize_mx(self.W.data_ptr(), self.N, self.K, self.K, m.MX_ROWWISE,
-                              self.qW.data_ptr(), self.sW.data_ptr(), None, None, stream))
+        e = timer.mark("quantize") if timer else None
+        self.quantize(self.X.data_ptr(), self.W.data_ptr(), stream)
         if e: e.record()
         e = timer.mark("gemm") if timer else None
         _ok(L.fp8_scaled_gemm(m.GEMM_MX, 0, 0, self.qX.data_ptr(), self.sX.data_ptr(),
@@ -670,10 +679,7 @@ def e2e_pipelined(m, wl, dev, steps, pg):
             s_comp.wait_event(loaded)
             s_comp.wait_event(out_free[b])
             st = s_comp.cuda_stream
-            _ok(L.fp8_quantize_mx(Xd[b].data_ptr(), wl.M, wl.K, wl.K, m.MX_ROWWISE,
-                                  wl.qX.data_ptr(), wl.sX.data_ptr(), None, None, st))
-            _ok(L.fp8_quantize_mx(Wd[b].data_ptr(), wl.N, wl.K, wl.K, m.MX_ROWWISE,
-                                  wl.qW.data_ptr(), wl.sW.data_ptr(), None, None, st))
+            wl.quantize(Xd[b].data_ptr(), Wd[b].data_ptr(), st)
             inputs_free[b].record(s_comp)
             _ok(L.fp8_scaled_gemm(m.GEMM_MX, 0, 0, wl.qX.data_ptr(), wl.sX.data_ptr(),
                                   wl.qW.data_ptr(), wl.sW.data_ptr(), wl.M, wl.N, wl.K,
@@ -769,7 +775,7 @@ def main():
     clk = clocks.stop()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     gemm_ms = timer.avg_ms("gemm")
-    qx_ms, qw_ms = timer.avg_ms("quantize_x"), timer.avg_ms("quantize_w")
+    q_ms = timer.avg_ms("quantize")
     ms_step = ms_total / args.steps
     value = job_throughput(wl.flops, world, ms_step)
 
@@ -794,7 +800,7 @@ def main():
     fp8_peak = pk["bf16_sustained"] * FP8_OVER_BF16
     achieved = wl.flops / (gemm_ms / 1e3) / 1e12
     q_bytes = (wl.M * wl.K + wl.N * wl.K) * MX_ROW_BYTES
-    q_gbs = q_bytes / ((qx_ms + qw_ms) / 1e3) / 1e9
+    q_gbs = q_bytes / (q_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -809,7 +815,7 @@ def main():
         "dtype": "e4m3+e8m0 operands, f32 accumulate, bf16 out",
         "data": "synthetic (seeded; Student-t(4) activations, N(0,0.02) weights)",
         "config": {"workload": "mlp_up", "shape": "X[8192x4096] . W[16384x4096]^T -> bf16",
-                   "M": wl.M, "N": wl.N, "K": wl.K, "step": "quantize X + quantize W + MX GEMM",
+                   "M": wl.M, "N": wl.N, "K": wl.K, "step": "quantize X and W rowwise (one launch) + MX GEMM",
                    "weights_cached": False, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (X+W bf16 = 192 MB > 129 MB); no flush"},
         "roofline": {"bound": "tensor", "kernel": "gemm_kernel<MX>", "achieved": achieved,
@@ -820,7 +826,8 @@ def main():
                      "avg_launch_ms": gemm_ms},
         "quantize": {"bound": "hbm", "achieved": q_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": q_gbs / pk["hbm_gbs"], "peak_source": pk["source"],
-                     "avg_ms_x": qx_ms, "avg_ms_w": qw_ms,
+                     "kernel": "quantize_mx_row_batch_kernel (X and W in one launch)",
+                     "avg_launch_ms": q_ms,
                      "bytes_per_value": MX_ROW_BYTES},
         "e2e": e2e,
         "gpu_launches": wl.launches_per_step * args.steps,

@@ -107,6 +107,29 @@ mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int
                              void* s_col, mxfp8_stream_t stream);
 
 /*
+ * fp8_quantize_mx_batch - the rowwise fp8_quantize_mx of up to 16 tensors in
+ * one launch (a linear layer's activation and weight, say, both of which the
+ * MX GEMM consumes rowwise: "Olmo-core MoE report, Section 11: MXFP8
+ * Training", Section 11.2.3).  Results are those of count separate
+ * fp8_quantize_mx calls with flags = MX_ROWWISE (| MX_SCALE_FLOOR).
+ *
+ *  count                  1 .. 16.
+ *  x_bf16, q_row, s_row   HOST arrays of count DEVICE pointers: BF16 input
+ *                         (row stride ld[t] elements), payload (rows[t] x
+ *                         cols[t] bytes, row stride cols[t]) and swizzled
+ *                         scales (mxfp8_scale_bytes(rows[t], cols[t]) bytes);
+ *                         all 16-byte aligned.
+ *  rows, cols, ld         HOST arrays of count sizes; cols[t] % 32 == 0,
+ *                         ld[t] >= cols[t], ld[t] % 8 == 0; a tensor with no
+ *                         rows or no columns is skipped (its pointers unused).
+ *  flags                  MX_ROWWISE, optionally | MX_SCALE_FLOOR (applies to
+ *                         every tensor); MX_COLWISE is rejected.
+ */
+mxfp8_status fp8_quantize_mx_batch(int32_t count, const void* const* x_bf16, const int64_t* rows,
+                                   const int64_t* cols, const int64_t* ld, unsigned flags,
+                                   void* const* q_row, void* const* s_row, mxfp8_stream_t stream);
+
+/*
  * fp8_quantize_mx_grouped - rowwise MXFP8 quantization of an expert-dispatched
  * matrix whose rows are sorted by expert ("Olmo-core MoE report", Section
  * 11.4.1: dispatch places each token row's qdata and scales in its expert's

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_quantize_tensor_batch": (st, [I32, P, P, I, P, P, P, P, P]),
+                "fp8_quantize_mx_batch": (st, [I32, P, P, P, P, ctypes.c_uint, P, P, P]),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
                 "fp8_quantize_tensor_scaled": (st, [P, I64, I, P, P, P, P, P]),
                 "fp8_quantize_tensor_delayed": (st, [P, I64, I, ctypes.c_float, P, I32, P, P, P, P, P, P]),
@@ -215,6 +216,31 @@ def fp8_requantize_tensor(q: torch.Tensor, scale_in: torch.Tensor, scale_out: to
     _check(lib().fp8_requantize_tensor(_ptr(q), q.numel(), fmt_in, _ptr(scale_in), _ptr(scale_out), fmt_out,
                                        _ptr(out), _ptr(sat_count), _stream(stream)))
     return out, sat_count
+
+
+def fp8_quantize_mx_batch(xs, flags: int = MX_ROWWISE, outs=None, stream=None):
+    """Rowwise MX quantization of several 2D BF16 tensors in one launch.
+
+    ``xs``: list of CUDA bf16 tensors [rows, cols] (row stride may exceed
+    cols).  Returns a list of (q_row, s_row) pairs; ``outs`` may supply them."""
+    count = len(xs)
+    for x in xs:
+        assert x.dtype == torch.bfloat16 and x.dim() == 2 and (x.numel() == 0 or x.stride(1) == 1)
+    _need_cuda(*xs)
+    dev = xs[0].device
+    if outs is None:
+        outs = [(torch.empty((x.shape[0], x.shape[1]), dtype=torch.uint8, device=dev),
+                 torch.empty(mxfp8_scale_bytes(x.shape[0], x.shape[1]), dtype=torch.uint8, device=dev))
+                for x in xs]
+    keep = [(ctypes.c_void_p * count)(*[x.data_ptr() for x in xs]),
+            (ctypes.c_int64 * count)(*[x.shape[0] for x in xs]),
+            (ctypes.c_int64 * count)(*[x.shape[1] for x in xs]),
+            (ctypes.c_int64 * count)(*[max(x.stride(0), x.shape[1]) for x in xs]),
+            (ctypes.c_void_p * count)(*[q.data_ptr() for q, _ in outs]),
+            (ctypes.c_void_p * count)(*[s.data_ptr() for _, s in outs])]
+    xp, rp, cp, lp, qp, sp = (ctypes.cast(a, ctypes.c_void_p) for a in keep)
+    _check(lib().fp8_quantize_mx_batch(count, xp, rp, cp, lp, flags, qp, sp, _stream(stream)))
+    return outs
 
 
 def fp8_quantize_tensor_batch(xs, fmt: int = FP8_E4M3, workspace=None, qs=None, amax=None, scale=None,

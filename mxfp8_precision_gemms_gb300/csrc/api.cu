@@ -173,6 +173,41 @@ mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int
     return cuda_result(launch_quantize_mx(a, reinterpret_cast<cudaStream_t>(stream)), "fp8_quantize_mx launch");
 }
 
+mxfp8_status fp8_quantize_mx_batch(int32_t count, const void* const* x_bf16, const int64_t* rows,
+                                   const int64_t* cols, const int64_t* ld, unsigned flags,
+                                   void* const* q_row, void* const* s_row, mxfp8_stream_t stream) {
+    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
+        return fail(MXFP8_ERR_INVALID_ARG, "batched quantization is rowwise only (flags 0x%x)", flags);
+    if (!(flags & MX_ROWWISE)) return fail(MXFP8_ERR_INVALID_ARG, "flags select no orientation");
+    if (count < 1 || count > kMaxBatch)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "count must be in [1, %d]", kMaxBatch);
+    if (!x_bf16 || !rows || !cols || !ld || !q_row || !s_row)
+        return fail(MXFP8_ERR_INVALID_ARG, "an argument array is NULL");
+    QuantMxArgs a[kMaxBatch] = {};
+    for (int t = 0; t < count; ++t) {
+        if (rows[t] < 0 || cols[t] < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size (tensor %d)", t);
+        a[t].rows = rows[t];
+        a[t].cols = cols[t];
+        a[t].flags = flags;
+        if (rows[t] == 0 || cols[t] == 0) continue;
+        if (!x_bf16[t] || !q_row[t] || !s_row[t])
+            return fail(MXFP8_ERR_INVALID_ARG, "x or an output of tensor %d is NULL", t);
+        if (cols[t] % 32)
+            return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (tensor %d, cols=%lld)", t, (long long)cols[t]);
+        if (ld[t] < cols[t]) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols (tensor %d)", t);
+        if (ld[t] % 8 || !aligned16(x_bf16[t]) || !aligned16(q_row[t]) || !aligned16(s_row[t]))
+            return fail(MXFP8_ERR_MISALIGNED, "pointer or ld of tensor %d not 16-byte aligned", t);
+        if ((cols[t] + 127) / 128 > 65535 || rows[t] > 0x7FFFFFFF)
+            return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "tensor %d too large", t);
+        a[t].x = static_cast<const uint16_t*>(x_bf16[t]);
+        a[t].ld = ld[t];
+        a[t].q_row = static_cast<uint8_t*>(q_row[t]);
+        a[t].s_row = static_cast<uint8_t*>(s_row[t]);
+    }
+    return cuda_result(launch_quantize_mx_rows_batch(count, a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_quantize_mx_batch launch");
+}
+
 mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int64_t cols,
                                      int64_t ld, const int32_t* group_offsets_dev, int32_t groups,
                                      unsigned flags, void* q, void* s, mxfp8_stream_t stream) {

@@ -147,6 +147,40 @@ __global__ void __launch_bounds__(kThreads)
 // a 128 x 128 tile; thread t owns block (t & 3) of tile rows t/4 and t/4 + 64,
 // reading each block as two 32-byte loads, computing its scale once and
 // writing 32 payload bytes and one scale byte.
+// One 128 x 128 tile of the rowwise quantization: thread t owns 32-value
+// block t & 3 of tile rows t / 4 and t / 4 + 64 (rows from row_begin, below
+// row_end; columns from ct * 128, below cols), reads it, and writes its 32
+// payload bytes and its scale byte into the tile's 512-byte swizzled scale
+// block s_tile.
+template <bool FLOOR>
+__device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t ld, int64_t cols,
+                                         uint8_t* __restrict__ q, uint8_t* __restrict__ s_tile,
+                                         int64_t row_begin, int64_t row_end, int64_t ct, bool v8) {
+    const int tid = threadIdx.x;
+    const int j = tid & 3;
+    const int64_t col = ct * kTile + j * 32;
+    uint32_t w[2][16];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int64_t row = row_begin + (tid >> 2) + 64 * i;
+        if (row < row_end && col < cols) {
+            const uint16_t* src = x + row * ld + col;
+            ld32_stream(src, w[i], v8);
+            ld32_stream(src + 16, w[i] + 8, v8);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[i][k] = 0u;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = (tid >> 2) + 64 * i;
+        const int64_t row = row_begin + r;
+        const bool in = row < row_end && col < cols;
+        mx_block32<FLOOR>(w[i], in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
+    }
+}
+
 template <bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_row_kernel(QuantMxArgs a, int64_t nkc, bool v8) {
@@ -170,30 +204,36 @@ __global__ void __launch_bounds__(kThreads)
         row_begin = rt * kTile;
         row_end = min(a.rows, row_begin + kTile);
     }
-    const int j = tid & 3;
-    const int64_t col = ct * kTile + j * 32;
-    uint32_t w[2][16];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int64_t row = row_begin + (tid >> 2) + 64 * i;
-        if (row < row_end && col < a.cols) {
-            const uint16_t* src = a.x + row * a.ld + col;
-            ld32_stream(src, w[i], v8);
-            ld32_stream(src + 16, w[i] + 8, v8);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) w[i][k] = 0u;
-        }
-    }
-    uint8_t* s_tile = a.s_row + (rt * nkc + ct) * 512;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int r = (tid >> 2) + 64 * i;
-        const int64_t row = row_begin + r;
-        const bool in = row < row_end && col < a.cols;
-        mx_block32<FLOOR>(w[i], in ? a.q_row + row * a.cols + col : nullptr, s_tile + swz_word(r) + j,
-                          v8);
-    }
+    row_tile<FLOOR>(a.x, a.ld, a.cols, a.q_row, a.s_row + (rt * nkc + ct) * 512, row_begin, row_end,
+                    ct, v8);
+}
+
+// Rowwise MX quantization of several tensors in one launch: a 1D grid over
+// all tensors' 128 x 128 tiles (tensor t owns blocks [tile_end[t-1],
+// tile_end[t]), row tiles fastest), each tile done as above.
+struct MxRowBatch {
+    const uint16_t* x[kMaxBatch];
+    uint8_t* q[kMaxBatch];
+    uint8_t* s[kMaxBatch];
+    int64_t rows[kMaxBatch], cols[kMaxBatch], ld[kMaxBatch];
+    int64_t row_tiles[kMaxBatch], nkc[kMaxBatch], tile_end[kMaxBatch];
+    uint8_t v8[kMaxBatch];
+    int count;
+};
+
+template <bool FLOOR>
+__global__ void __launch_bounds__(kThreads)
+    quantize_mx_row_batch_kernel(const __grid_constant__ MxRowBatch b) {
+    const int64_t blk = blockIdx.x;
+    int t = 0;
+    while (t + 1 < b.count && blk >= b.tile_end[t]) ++t;
+    const int64_t local = blk - (t ? b.tile_end[t - 1] : 0);
+    const int64_t rt = local % b.row_tiles[t];
+    const int64_t ct = local / b.row_tiles[t];
+    const int64_t row_begin = rt * kTile;
+    const int64_t row_end = min(b.rows[t], row_begin + kTile);
+    row_tile<FLOOR>(b.x[t], b.ld[t], b.cols[t], b.q[t], b.s[t] + (rt * b.nkc[t] + ct) * 512, row_begin,
+                    row_end, ct, b.v8[t] != 0);
 }
 
 // Rowwise + colwise (or colwise only) MX quantization of a 128 x 128 tile
@@ -697,6 +737,42 @@ cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_quantize_mx_rows_batch(int count, const QuantMxArgs* a, cudaStream_t s) {
+    if (count < 1 || count > kMaxBatch) return cudaErrorInvalidValue;
+    MxRowBatch b{};
+    int64_t tiles = 0;
+    bool floor = false;
+    int n = 0;
+    for (int t = 0; t < count; ++t) {
+        if (a[t].rows <= 0 || a[t].cols <= 0) continue;  // nothing to do for an empty tensor
+        const int64_t row_tiles = (a[t].rows + kTile - 1) / kTile;
+        const int64_t col_tiles = (a[t].cols + kTile - 1) / kTile;
+        b.x[n] = a[t].x;
+        b.q[n] = a[t].q_row;
+        b.s[n] = a[t].s_row;
+        b.rows[n] = a[t].rows;
+        b.cols[n] = a[t].cols;
+        b.ld[n] = a[t].ld;
+        b.row_tiles[n] = row_tiles;
+        b.nkc[n] = col_tiles;
+        tiles += row_tiles * col_tiles;
+        b.tile_end[n] = tiles;
+        b.v8[n] = (reinterpret_cast<uintptr_t>(a[t].x) % 32 == 0) && (a[t].ld % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(a[t].q_row) % 32 == 0);
+        floor = (a[t].flags & MX_SCALE_FLOOR) != 0;
+        ++n;
+    }
+    if (n == 0) return cudaSuccess;
+    if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    b.count = n;
+    if (floor) {
+        quantize_mx_row_batch_kernel<true><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(b);
+    } else {
+        quantize_mx_row_batch_kernel<false><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(b);
+    }
+    return cudaGetLastError();
+}
 
 template <bool ROW, bool FLOOR>
 cudaError_t launch_mx_tile(const QuantMxArgs& a, const CUtensorMap& map, cudaStream_t s) {

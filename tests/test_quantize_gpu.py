@@ -103,6 +103,50 @@ def test_quantize_mx_rowwise_16_byte_aligned(flags, ld, shift, qshift):
     assert np.all(hb[:qshift] == 0xA5) and np.all(hb[qshift + rows * cols:] == 0xA5)
 
 
+@pytest.mark.parametrize("flags", [ROW, ROW | FLOOR])
+def test_quantize_mx_batch_matches_oracle(flags):
+    """Several tensors in one launch: ragged rows, a wide row stride, an empty
+    tensor, a 16- but not 32-byte aligned input; each equals the oracle."""
+    shapes = [(300, 256), (1024, 4096), (0, 64), (96, 96), (200, 224), (128, 32)]
+    bits = [random_bits(sh, "student", seed=11 + i) if sh[0] else np.zeros(sh, np.uint16)
+            for i, sh in enumerate(shapes)]
+    xs = []
+    for i, b in enumerate(bits):
+        if i == 1:  # row stride 4104 > cols
+            wide = np.zeros((b.shape[0], 4104), np.uint16)
+            wide[:, :b.shape[1]] = b
+            xs.append(to_dev_bf16(wide)[:, :b.shape[1]])
+        elif i == 4:  # input start 16 bytes past a 32-byte boundary
+            flat = np.zeros(b.size + 8, np.uint16)
+            flat[8:] = b.reshape(-1)
+            xs.append(to_dev_bf16(flat)[8:].view(b.shape))
+        else:
+            xs.append(to_dev_bf16(b))
+    outs = [(filled(b.shape, 0xA5), filled(m.mxfp8_scale_bytes(*b.shape), 0xA5)) for b in bits]
+    m.fp8_quantize_mx_batch(xs, flags, outs=outs)
+    assert_ok()
+    for b, (q, sc) in zip(bits, outs):
+        if b.size == 0:
+            continue
+        want = oracle.quantize_mx(b, flags)
+        assert np.array_equal(host(q), want["q_row"])
+        assert np.array_equal(host(sc), want["s_row"])
+
+
+def test_quantize_mx_batch_of_sixteen_mlp_operands():
+    """Sixteen tensors; the first two are the MLP up-projection's X and W rows
+    (student-t activations, N(0, 0.02) weights) at a reduced size."""
+    w = workloads.mlp_up(seed=2, device="cpu", tokens=512, d_in=1024, d_out=768)
+    bits = [workloads.bits(w["X"]), workloads.bits(w["W"])]
+    bits += [random_bits((32 * (t + 1), 64 * ((t % 3) + 1)), "wide", seed=40 + t) for t in range(14)]
+    outs = m.fp8_quantize_mx_batch([to_dev_bf16(b) for b in bits])
+    assert_ok()
+    for b, (q, sc) in zip(bits, outs):
+        want = oracle.quantize_mx(b, ROW)
+        assert np.array_equal(host(q), want["q_row"])
+        assert np.array_equal(host(sc), want["s_row"])
+
+
 def _anchor_blocks(floor):
     """Blocks whose scale byte is fixed by an anchor value, filled with every
     finite BF16 pattern at or below the anchor: all BF16 values x all scales."""
