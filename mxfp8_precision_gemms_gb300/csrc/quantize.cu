@@ -431,6 +431,7 @@ struct TensorBatch {
     float* amax[kMaxBatch];   // device scalars (outputs)
     float* scale[kMaxBatch];
     int64_t n[kMaxBatch];
+    uint8_t v8[kMaxBatch];    // x 32-byte aligned: 256-bit loads
     int count;
 };
 
@@ -442,20 +443,67 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 
 // |x| maximum of one tensor over this thread's grid-stride share, as BF16
 // magnitude bits.
+// This thread's share of max |x| (as BF16 magnitude bits) over 32-byte
+// chunks first, first + stride, ...: four chunks in flight per round, kept
+// in L2 (normal caching) for the cast that re-reads them.
 __device__ __forceinline__ uint32_t amax_share(const uint16_t* __restrict__ x, int64_t n,
-                                               int64_t first, int64_t stride) {
-    const int64_t n8 = n / 8;
-    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+                                               int64_t first, int64_t stride, bool v8) {
+    const int64_t n16 = n / 16;
     uint32_t m = 0;
-    int64_t i = first;
-    for (; i + 3 * stride < n8; i += 4 * stride) {
-        const uint4 a0 = x8[i], a1 = x8[i + stride], a2 = x8[i + 2 * stride],
-                    a3 = x8[i + 3 * stride];
-        m = max(m, max(max(amax8(a0), amax8(a1)), max(amax8(a2), amax8(a3))));
+    for (int64_t i = first; i < n16; i += 4 * stride) {
+        uint32_t w[4][8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = i + k * stride;
+            if (c < n16) {
+                ld32_cached(x + c * 16, w[k], v8);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[k][e] = 0u;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m = max(m, max(amax8(make_uint4(w[k][0], w[k][1], w[k][2], w[k][3])),
+                           amax8(make_uint4(w[k][4], w[k][5], w[k][6], w[k][7]))));
     }
-    for (; i < n8; i += stride) m = max(m, amax8(x8[i]));
-    for (int64_t t = n8 * 8 + first; t < n; t += stride) m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
+    for (int64_t t = n16 * 16 + first; t < n; t += stride) m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
     return m;
+}
+
+// Cast this thread's share (the same chunks as amax_share) with scale s:
+// four 32-byte chunks in flight, 16 payload bytes stored per chunk.
+template <int FMT>
+__device__ __forceinline__ void cast_share(const uint16_t* __restrict__ x, uint8_t* __restrict__ q,
+                                           int64_t n, float s, int64_t first, int64_t stride,
+                                           bool v8) {
+    const int64_t n16 = n / 16;
+    for (int64_t i = first; i < n16; i += 4 * stride) {
+        uint32_t w[4][8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = i + k * stride;
+            if (c < n16) ld32_stream(x + c * 16, w[k], v8);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = i + k * stride;
+            if (c < n16) {
+                uint4 o;
+                uint32_t* po = &o.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    po[e] = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(w[k][2 * e]), s), __fmul_rn(bf16_hi(w[k][2 * e]), s)) |
+                            (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(w[k][2 * e + 1]), s),
+                                            __fmul_rn(bf16_hi(w[k][2 * e + 1]), s)) << 16);
+                reinterpret_cast<uint4*>(q)[c] = o;
+            }
+        }
+    }
+    for (int64_t r = n16 * 16 + first; r < n; r += stride) {
+        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[r]) << 16), s);
+        q[r] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
+    }
 }
 
 template <int FMT>
@@ -467,7 +515,7 @@ __global__ void __launch_bounds__(kFusedThreads)
     const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int t = 0; t < b.count; ++t) {
-        const uint32_t m = warp_max(amax_share(b.x[t], b.n[t], first, stride));
+        const uint32_t m = warp_max(amax_share(b.x[t], b.n[t], first, stride, b.v8[t] != 0));
         if (lane == 0) red[t][warp] = m;
     }
     __syncthreads();
@@ -507,23 +555,7 @@ __global__ void __launch_bounds__(kFusedThreads)
             *b.amax[t] = amax;
             *b.scale[t] = s;
         }
-        const uint16_t* __restrict__ x = b.x[t];
-        uint8_t* __restrict__ q = b.q[t];
-        const int64_t n = b.n[t], n8 = n / 8;
-        const uint4* x8 = reinterpret_cast<const uint4*>(x);
-        for (int64_t j = first; j < n8; j += stride) {
-            const uint4 v = x8[j];
-            uint2 o;
-            o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
-                  (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
-            o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
-                  (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
-            reinterpret_cast<uint2*>(q)[j] = o;
-        }
-        for (int64_t r = n8 * 8 + first; r < n; r += stride) {
-            const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[r]) << 16), s);
-            q[r] = static_cast<uint8_t>(cvt_fp8x2<FMT>(y, 0.0f) & 0xFFu);
-        }
+        cast_share<FMT>(b.x[t], b.q[t], b.n[t], s, first, stride, b.v8[t] != 0);
     }
 }
 
@@ -865,7 +897,8 @@ cudaError_t launch_quantize_tensor_batch(int count, const uint16_t* const* x, co
         b.amax[t] = amax + t;
         b.scale[t] = scale + t;
         b.n[t] = n[t];
-        chunks = std::max<int64_t>(chunks, n[t] / 8 + 1);
+        b.v8[t] = reinterpret_cast<uintptr_t>(x[t]) % 32 == 0;
+        chunks = std::max<int64_t>(chunks, n[t] / 16 + 1);
     }
     b.count = count;
     const int64_t resident = static_cast<int64_t>(sm_count_current_device()) * bps;
