@@ -391,7 +391,7 @@ mxfp8_status fp8_dequantize_mx(const void* q, const void* s, int64_t rows, int64
  *          (or the group-padded scale array).
  * The hidden value a = bf16_RNE(g * sigma(g) * u), sigma(g) = 1/(1+e^-g), is
  * what an unfused SwiGLU would store in BF16; it is formed in fp32 within
- * 14 * 2^-24 relative of the exact value (in double, rounded once, for
+ * 7.5 * 2^-24 relative of the exact value (in double, rounded once, for
  * g < -80), so a is the correctly rounded BF16 value except within that
  * distance of a rounding midpoint, where it may be the neighbour.  a is then quantized by the MX rule
  * of fp8_quantize_mx (flags: MX_SCALE_FLOOR optional, rowwise implied) and
@@ -456,6 +456,15 @@ void mxfp8_set_wait_limit_ns(uint64_t ns);
  * resets itself after one launch.
  */
 void mxfp8_debug_inject_wait_timeout(int enable);
+
+/*
+ * Test hook: y[i] = the fp32 value g[i] sigma(g[i]) u[i] that
+ * fp8_swiglu_quantize_mx forms on its fast path (gates >= -80), before the
+ * BF16 rounding, so its error bound can be checked.  g, u: device BF16[n];
+ * y: device fp32[n].
+ */
+mxfp8_status mxfp8_debug_swiglu_f32(const void* g_bf16, const void* u_bf16, int64_t n, float* y,
+                                    mxfp8_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_quantize_tensor_batch": (st, [I32, P, P, I, P, P, P, P, P]),
                 "fp8_quantize_mx_batch": (st, [I32, P, P, P, P, ctypes.c_uint, P, P, P]),
+                "mxfp8_debug_swiglu_f32": (st, [P, P, I64, P, P]),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
                 "fp8_quantize_tensor_scaled": (st, [P, I64, I, P, P, P, P, P]),
                 "fp8_quantize_tensor_delayed": (st, [P, I64, I, ctypes.c_float, P, I32, P, P, P, P, P, P]),
@@ -216,6 +217,16 @@ def fp8_requantize_tensor(q: torch.Tensor, scale_in: torch.Tensor, scale_out: to
     _check(lib().fp8_requantize_tensor(_ptr(q), q.numel(), fmt_in, _ptr(scale_in), _ptr(scale_out), fmt_out,
                                        _ptr(out), _ptr(sat_count), _stream(stream)))
     return out, sat_count
+
+
+def mxfp8_debug_swiglu_f32(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tensor:
+    """Test hook: the SwiGLU fast path's fp32 g sigma(g) u per element."""
+    assert g.dtype == torch.bfloat16 and u.dtype == torch.bfloat16 and g.shape == u.shape
+    assert g.is_contiguous() and u.is_contiguous()
+    _need_cuda(g, u)
+    y = torch.empty(g.shape, dtype=torch.float32, device=g.device)
+    _check(lib().mxfp8_debug_swiglu_f32(_ptr(g), _ptr(u), g.numel(), _ptr(y), _stream(stream)))
+    return y
 
 
 def fp8_quantize_mx_batch(xs, flags: int = MX_ROWWISE, outs=None, stream=None):

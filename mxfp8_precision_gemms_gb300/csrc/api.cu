@@ -585,6 +585,17 @@ const char* mxfp8_last_error(void) { return g_err; }
 
 void mxfp8_set_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns ? ns : 2000000000ull); }
 
+mxfp8_status mxfp8_debug_swiglu_f32(const void* g_bf16, const void* u_bf16, int64_t n, float* y,
+                                    mxfp8_stream_t stream) {
+    if (n < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (n == 0) return ok();
+    if (!g_bf16 || !u_bf16 || !y) return fail(MXFP8_ERR_INVALID_ARG, "NULL pointer");
+    return cuda_result(launch_debug_swiglu_f32(static_cast<const uint16_t*>(g_bf16),
+                                               static_cast<const uint16_t*>(u_bf16), n, y,
+                                               reinterpret_cast<cudaStream_t>(stream)),
+                       "mxfp8_debug_swiglu_f32 launch");
+}
+
 void mxfp8_debug_inject_wait_timeout(int enable) { g_inject.store(enable ? 1 : 0); }
 
 }  // extern "C"

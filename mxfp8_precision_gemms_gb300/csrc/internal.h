@@ -86,6 +86,9 @@ struct WeightedQuantArgs {
 cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t s);
 cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t s);
+// Test hook: the SwiGLU fast path's fp32 value per element.
+cudaError_t launch_debug_swiglu_f32(const uint16_t* g, const uint16_t* u, int64_t n, float* y,
+                                    cudaStream_t s);
 cudaError_t take_status_fused(unsigned* out);
 
 // Delayed / automatic scaling (quantize.cu).  sat: 64-bit saturated count.

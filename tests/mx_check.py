@@ -1,10 +1,9 @@
 """Comparison of a GPU MX quantization with the oracle's when the BF16 values
 being quantized are only known to lie in a small set.
 
-The fused SwiGLU quantizer forms g sigma(g) u in fp32 (error below 14 *
-2^-24 relative from the documented 2-ulp bounds of expf and __fdividef plus
-three roundings, plus an absolute 2^-149 where fp32 underflows) before the
-BF16 rounding.  Where the exact value lies within that distance of a BF16
+The fused SwiGLU quantizer forms g sigma(g) u in fp32 (error below 7.5 *
+2^-24 relative: checked for every BF16 gate by the fast-path test, plus an
+absolute 2^-149 where fp32 underflows) before the BF16 rounding.  Where the exact value lies within that distance of a BF16
 rounding midpoint either neighbour is a correct result, so the check takes,
 per element, the set {bf16(y - band), bf16(y + band)} around the oracle's
 FP64 value y, band = 2^-19 |y| + 2^-140 (both bounds with margin).  Blocks

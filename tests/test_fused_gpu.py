@@ -125,6 +125,61 @@ def _swiglu_check(h_dev, offsets=None, floor=False):
     return check_set_quantization(host(q), host(s), lo, hi, q_exp, s_exp, offsets, floor)
 
 
+# documented bound of the fast path: 4.5 * 2^-24 with u = 1 (exhaustive over
+# the BF16 gates below), 7.5 * 2^-24 for a general u (three more half-ulp
+# roundings at most)
+SWIGLU_BOUND_U1 = 4.5 * 2.0 ** -24
+SWIGLU_BOUND = 7.5 * 2.0 ** -24
+
+
+def _swiglu_rel_err(gb, ub, bound):
+    """Largest relative error of the fast path over values above 2^-100,
+    after checking every value against bound * |y| + 2^-149."""
+    y = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(gb), to_dev_bf16(ub))).astype(np.float64)
+    assert_ok()
+    want = oracle.swiglu(np.concatenate([gb[None, :], ub[None, :]], axis=1))[0]
+    # well beyond fp32's range both are infinite (so is the BF16 value); right
+    # at the edge either FLT_MAX or infinity is a correct fp32 result
+    a = np.abs(want)
+    over = a >= 2.0 ** 128 * (1 + 2.0 ** -20)
+    edge = ~over & (a >= float(np.finfo(np.float32).max) * (1 - 2.0 ** -20))
+    assert np.all(np.isinf(y[over]) & (np.sign(y[over]) == np.sign(want[over])))
+    y, want = y[~(over | edge)], want[~(over | edge)]
+    err = np.abs(y - want)
+    assert np.all(err <= bound * np.abs(want) + 2.0 ** -149)
+    big = np.abs(want) >= 2.0 ** -100
+    return np.max(err[big] / np.abs(want[big]), initial=0.0)
+
+
+def test_swiglu_fast_path_error_every_gate():
+    """Every finite BF16 gate the fast path takes (g >= -80) with u = 1: the
+    fp32 value the quantizer rounds to BF16 is within the documented bound of
+    g sigma(g) computed in FP64 by the oracle; with random ups, within the
+    general bound."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g = oracle.bf16_decode(allb)
+    gb = allb[np.isfinite(g) & (g >= -80) & (g != 0)]
+    rel = _swiglu_rel_err(gb, np.full(gb.shape, 0x3F80, np.uint16), SWIGLU_BOUND_U1)
+    assert rel <= SWIGLU_BOUND_U1, rel / 2.0 ** -24
+    rng = np.random.default_rng(5)
+    ub = oracle.bf16_round(rng.standard_normal(gb.size) * np.exp(rng.uniform(-20, 20, gb.size)))
+    rel = _swiglu_rel_err(gb, ub, SWIGLU_BOUND)
+    assert rel <= SWIGLU_BOUND, rel / 2.0 ** -24
+
+
+def test_swiglu_fast_path_special_gates():
+    """+Inf and NaN gates propagate (the quantizer then marks the block),
+    gates past 87 (e^-g flushes to 0) give g u exactly, zero gates give 0."""
+    gb = np.array([0x7F80, 0x7FC0, 0x42B0, 0x4300, 0x7F7F, 0x0000, 0x8000], np.uint16)
+    ub = np.array([0x3F80] * 5 + [0x4000, 0x4000], np.uint16)
+    y = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(gb), to_dev_bf16(ub)))
+    assert np.isinf(y[0]) and y[0] > 0
+    assert np.isnan(y[1])
+    gd = oracle.bf16_decode(gb)
+    assert y[2] == np.float32(gd[2]) and y[3] == np.float32(gd[3]) and y[4] == np.float32(gd[4])
+    assert y[5] == 0 and y[6] == 0
+
+
 @pytest.mark.parametrize("rows,f", SHAPES)
 @pytest.mark.parametrize("floor", [False, True])
 def test_swiglu_quantize_plain(rows, f, floor):
