@@ -24,8 +24,12 @@ def quantize_both(bits, flags=m.MX_ROWWISE):
     return got, want
 
 
+# K % 256 == 0 loads each slot pair with one copy per operand (3D K-chunk
+# maps); other K (384, 640: odd numbers of 128-wide K steps) take the
+# per-slot copies with a half-empty last pair
 MX_SHAPES = [(128, 256, 128), (256, 256, 256), (200, 136, 96), (1, 8, 32), (384, 512, 1024),
-             (130, 264, 4096), (1000, 1024, 160), (256, 768, 2048)]
+             (130, 264, 4096), (1000, 1024, 160), (256, 768, 2048), (300, 512, 384),
+             (512, 256, 640)]
 
 
 @pytest.mark.parametrize("M,N,K", MX_SHAPES)
@@ -164,7 +168,8 @@ def _grouped_case(counts, N, K, seed=0):
 
 @pytest.mark.parametrize("counts,N,K", [([0, 1, 127, 128, 129, 0, 300, 5], 256, 256),
                                         ([64] * 4, 136, 96), ([0, 0, 1000, 0], 512, 512),
-                                        ([3, 700, 2, 90, 11, 256, 1, 0, 45], 1024, 2048)])
+                                        ([3, 700, 2, 90, 11, 256, 1, 0, 45], 1024, 2048),
+                                        ([40, 0, 300, 129], 256, 384)])
 def test_grouped_gemm_matches_oracle(counts, N, K):
     off, off_d, qa, sa, qw, sw, rqa, rsa, rqw, rsw = _grouped_case(counts, N, K)
     c = filled((int(off[-1]), N), 0x7FC0, torch.int16).view(torch.bfloat16)
