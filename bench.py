@@ -200,6 +200,7 @@ class MlpUp:
         self._ct = ctypes
         self._rows = (ctypes.c_int64 * 2)(self.M, self.N)
         self._cols = (ctypes.c_int64 * 2)(self.K, self.K)
+        self._flags = (ctypes.c_uint * 2)(m.MX_ROWWISE, m.MX_ROWWISE)
         self._qs = (ctypes.c_void_p * 2)(self.qX.data_ptr(), self.qW.data_ptr())
         self._ss = (ctypes.c_void_p * 2)(self.sX.data_ptr(), self.sW.data_ptr())
 
@@ -208,7 +209,8 @@ class MlpUp:
         xs = (ct.c_void_p * 2)(x_ptr, w_ptr)
         vp = lambda a: ct.cast(a, ct.c_void_p)
         _ok(self.lib.fp8_quantize_mx_batch(2, vp(xs), vp(self._rows), vp(self._cols), vp(self._cols),
-                                           self.m.MX_ROWWISE, vp(self._qs), vp(self._ss), stream))
+                                           vp(self._flags), vp(self._qs), vp(self._ss), None, None,
+                                           stream))
 
     def step(self, timer=None, stream=0):
         L, m = self.lib, self.m
@@ -310,14 +312,21 @@ def hot_path_rows(m, dev, steps, warmup):
     dX = torch.empty((T, din), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((dout, din), dtype=torch.bfloat16, device=dev)
 
+    # dY both ways, W and X colwise: one batched launch
+    import ctypes
+    bq = [(ctypes.c_void_p * 3)(dY.data_ptr(), W.data_ptr(), X.data_ptr()),
+          (ctypes.c_int64 * 3)(T, dout, T), (ctypes.c_int64 * 3)(dout, din, din),
+          (ctypes.c_int64 * 3)(dout, din, din),
+          (ctypes.c_uint * 3)(m.MX_ROWWISE | m.MX_COLWISE, m.MX_COLWISE, m.MX_COLWISE),
+          (ctypes.c_void_p * 3)(q_dy.data_ptr(), None, None),
+          (ctypes.c_void_p * 3)(s_dy.data_ptr(), None, None),
+          (ctypes.c_void_p * 3)(q_dyt.data_ptr(), q_wt.data_ptr(), q_xt.data_ptr()),
+          (ctypes.c_void_p * 3)(s_dyt.data_ptr(), s_wt.data_ptr(), s_xt.data_ptr())]
+    bq_p = [ctypes.cast(a, ctypes.c_void_p) for a in bq]
+
     def bw(timer):
         e = timer.mark("quantize") if timer else None
-        _ok(L.fp8_quantize_mx(dY.data_ptr(), T, dout, dout, m.MX_ROWWISE | m.MX_COLWISE,
-                              q_dy.data_ptr(), s_dy.data_ptr(), q_dyt.data_ptr(), s_dyt.data_ptr(), st))
-        _ok(L.fp8_quantize_mx(W.data_ptr(), dout, din, din, m.MX_COLWISE, None, None,
-                              q_wt.data_ptr(), s_wt.data_ptr(), st))
-        _ok(L.fp8_quantize_mx(X.data_ptr(), T, din, din, m.MX_COLWISE, None, None,
-                              q_xt.data_ptr(), s_xt.data_ptr(), st))
+        _ok(L.fp8_quantize_mx_batch(3, *bq_p, st))
         if e: e.record()
         e = timer.mark("gemm") if timer else None
         _ok(L.fp8_scaled_gemm(m.GEMM_MX, 0, 0, q_dy.data_ptr(), s_dy.data_ptr(), q_wt.data_ptr(),
@@ -331,7 +340,8 @@ def hot_path_rows(m, dev, steps, warmup):
     rows["backward_8192x4096"] = {
         "ms_per_step": ms, "tflops_incl_quantize": fl / ms / 1e9,
         "gemm_tflops": fl / t.avg_ms("gemm") / 1e9,
-        "quantize_gbs": qbytes / t.avg_ms("quantize") / 1e6, "launches_per_step": 5}
+        "quantize_gbs": qbytes / t.avg_ms("quantize") / 1e6, "launches_per_step": 3,
+        "quantize_path": "dY both ways, W and X colwise in one batched launch"}
     del dY, W, X, q_dy, q_dyt, q_wt, q_xt, dX, dW, w
 
     # grouped experts: 64 experts, top-8 of 32768 tokens, 2048 -> 1024

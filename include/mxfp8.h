@@ -107,27 +107,30 @@ mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int
                              void* s_col, mxfp8_stream_t stream);
 
 /*
- * fp8_quantize_mx_batch - the rowwise fp8_quantize_mx of up to 16 tensors in
- * one launch (a linear layer's activation and weight, say, both of which the
- * MX GEMM consumes rowwise: "Olmo-core MoE report, Section 11: MXFP8
- * Training", Section 11.2.3).  Results are those of count separate
- * fp8_quantize_mx calls with flags = MX_ROWWISE (| MX_SCALE_FLOOR).
+ * fp8_quantize_mx_batch - fp8_quantize_mx for up to 16 tensors with as few
+ * launches as possible (a linear layer's activation and weight rowwise for
+ * the forward GEMM, or the backward's dY both ways and W and X colwise:
+ * "Olmo-core MoE report, Section 11: MXFP8 Training", Section 11.3.2, Eq. 60).
+ * Each tensor gets exactly what fp8_quantize_mx(x[t], rows[t], cols[t],
+ * ld[t], flags[t], ...) gives it.  Rowwise-only tensors share one launch;
+ * tensors with MX_COLWISE share one launch per 8.
  *
  *  count                  1 .. 16.
- *  x_bf16, q_row, s_row   HOST arrays of count DEVICE pointers: BF16 input
- *                         (row stride ld[t] elements), payload (rows[t] x
- *                         cols[t] bytes, row stride cols[t]) and swizzled
- *                         scales (mxfp8_scale_bytes(rows[t], cols[t]) bytes);
- *                         all 16-byte aligned.
- *  rows, cols, ld         HOST arrays of count sizes; cols[t] % 32 == 0,
- *                         ld[t] >= cols[t], ld[t] % 8 == 0; a tensor with no
- *                         rows or no columns is skipped (its pointers unused).
- *  flags                  MX_ROWWISE, optionally | MX_SCALE_FLOOR (applies to
- *                         every tensor); MX_COLWISE is rejected.
+ *  x_bf16                 HOST array of count DEVICE pointers to the BF16
+ *                         inputs (row stride ld[t] elements), 16-byte aligned.
+ *  rows, cols, ld, flags  HOST arrays of count values, with fp8_quantize_mx's
+ *                         rules per tensor; MX_SCALE_FLOOR must be the same for
+ *                         every non-empty tensor.  A tensor with no rows or no
+ *                         columns is skipped (its pointers unused).
+ *  q_row, s_row           HOST arrays of count DEVICE pointers (rowwise
+ *                         outputs of the tensors whose flags have MX_ROWWISE;
+ *                         the arrays may be NULL when none has).
+ *  q_col, s_col           the same for MX_COLWISE.
  */
 mxfp8_status fp8_quantize_mx_batch(int32_t count, const void* const* x_bf16, const int64_t* rows,
-                                   const int64_t* cols, const int64_t* ld, unsigned flags,
-                                   void* const* q_row, void* const* s_row, mxfp8_stream_t stream);
+                                   const int64_t* cols, const int64_t* ld, const unsigned* flags,
+                                   void* const* q_row, void* const* s_row, void* const* q_col,
+                                   void* const* s_col, mxfp8_stream_t stream);
 
 /*
  * fp8_quantize_mx_grouped - rowwise MXFP8 quantization of an expert-dispatched

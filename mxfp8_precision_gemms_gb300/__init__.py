@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_tensor": (st, [P, I64, I, P, P, P, P, P]),
                 "mxfp8_tensor_workspace_bytes": (ctypes.c_size_t, []),
                 "fp8_quantize_tensor_batch": (st, [I32, P, P, I, P, P, P, P, P]),
-                "fp8_quantize_mx_batch": (st, [I32, P, P, P, P, ctypes.c_uint, P, P, P]),
+                "fp8_quantize_mx_batch": (st, [I32, P, P, P, P, P, P, P, P, P, P]),
                 "mxfp8_debug_swiglu_f32": (st, [P, P, I64, P, P]),
                 "fp8_quantize_tensor_noalloc": (st, [P, I64, I, P, P, P, P]),
                 "fp8_quantize_tensor_scaled": (st, [P, I64, I, P, P, P, P, P]),
@@ -229,28 +229,39 @@ def mxfp8_debug_swiglu_f32(g: torch.Tensor, u: torch.Tensor, stream=None) -> tor
     return y
 
 
-def fp8_quantize_mx_batch(xs, flags: int = MX_ROWWISE, outs=None, stream=None):
-    """Rowwise MX quantization of several 2D BF16 tensors in one launch.
-
-    ``xs``: list of CUDA bf16 tensors [rows, cols] (row stride may exceed
-    cols).  Returns a list of (q_row, s_row) pairs; ``outs`` may supply them."""
+def fp8_quantize_mx_batch(xs, flags=MX_ROWWISE, outs=None, stream=None):
+    """fp8_quantize_mx for several 2D BF16 tensors with as few launches as
+    possible.  ``flags``: one value for all tensors or a list (one per
+    tensor).  Returns a list of dicts like fp8_quantize_mx's; ``outs`` may
+    supply them (the keys the flags need)."""
     count = len(xs)
+    fl = [int(flags)] * count if isinstance(flags, int) else [int(f) for f in flags]
+    assert len(fl) == count
     for x in xs:
         assert x.dtype == torch.bfloat16 and x.dim() == 2 and (x.numel() == 0 or x.stride(1) == 1)
     _need_cuda(*xs)
     dev = xs[0].device
     if outs is None:
-        outs = [(torch.empty((x.shape[0], x.shape[1]), dtype=torch.uint8, device=dev),
-                 torch.empty(mxfp8_scale_bytes(x.shape[0], x.shape[1]), dtype=torch.uint8, device=dev))
-                for x in xs]
+        outs = []
+        for x, f in zip(xs, fl):
+            r, c = x.shape
+            o = {}
+            if f & MX_ROWWISE:
+                o["q_row"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
+                o["s_row"] = torch.empty(mxfp8_scale_bytes(r, c), dtype=torch.uint8, device=dev)
+            if f & MX_COLWISE:
+                o["q_col"] = torch.empty((c, r), dtype=torch.uint8, device=dev)
+                o["s_col"] = torch.empty(mxfp8_scale_bytes(c, r), dtype=torch.uint8, device=dev)
+            outs.append(o)
+    ptr = lambda o, k: o[k].data_ptr() if k in o else None
     keep = [(ctypes.c_void_p * count)(*[x.data_ptr() for x in xs]),
             (ctypes.c_int64 * count)(*[x.shape[0] for x in xs]),
             (ctypes.c_int64 * count)(*[x.shape[1] for x in xs]),
             (ctypes.c_int64 * count)(*[max(x.stride(0), x.shape[1]) for x in xs]),
-            (ctypes.c_void_p * count)(*[q.data_ptr() for q, _ in outs]),
-            (ctypes.c_void_p * count)(*[s.data_ptr() for _, s in outs])]
-    xp, rp, cp, lp, qp, sp = (ctypes.cast(a, ctypes.c_void_p) for a in keep)
-    _check(lib().fp8_quantize_mx_batch(count, xp, rp, cp, lp, flags, qp, sp, _stream(stream)))
+            (ctypes.c_uint * count)(*fl)]
+    keep += [(ctypes.c_void_p * count)(*[ptr(o, k) for o in outs]) for k in ("q_row", "s_row", "q_col", "s_col")]
+    args = [ctypes.cast(a, ctypes.c_void_p) for a in keep]
+    _check(lib().fp8_quantize_mx_batch(count, *args, _stream(stream)))
     return outs
 
 

@@ -174,38 +174,60 @@ mxfp8_status fp8_quantize_mx(const void* x_bf16, int64_t rows, int64_t cols, int
 }
 
 mxfp8_status fp8_quantize_mx_batch(int32_t count, const void* const* x_bf16, const int64_t* rows,
-                                   const int64_t* cols, const int64_t* ld, unsigned flags,
-                                   void* const* q_row, void* const* s_row, mxfp8_stream_t stream) {
-    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
-        return fail(MXFP8_ERR_INVALID_ARG, "batched quantization is rowwise only (flags 0x%x)", flags);
-    if (!(flags & MX_ROWWISE)) return fail(MXFP8_ERR_INVALID_ARG, "flags select no orientation");
+                                   const int64_t* cols, const int64_t* ld, const unsigned* flags,
+                                   void* const* q_row, void* const* s_row, void* const* q_col,
+                                   void* const* s_col, mxfp8_stream_t stream) {
     if (count < 1 || count > kMaxBatch)
         return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "count must be in [1, %d]", kMaxBatch);
-    if (!x_bf16 || !rows || !cols || !ld || !q_row || !s_row)
+    if (!x_bf16 || !rows || !cols || !ld || !flags)
         return fail(MXFP8_ERR_INVALID_ARG, "an argument array is NULL");
-    QuantMxArgs a[kMaxBatch] = {};
+    QuantMxArgs row_only[kMaxBatch] = {}, with_col[kMaxBatch] = {};
+    int n_row = 0, n_col = 0;
+    int floor_bit = -1;
     for (int t = 0; t < count; ++t) {
+        const unsigned f = flags[t];
+        const bool row = f & MX_ROWWISE, col = f & MX_COLWISE;
+        if (f & ~7u) return fail(MXFP8_ERR_INVALID_ARG, "unknown flag bits 0x%x (tensor %d)", f, t);
+        if (!row && !col) return fail(MXFP8_ERR_INVALID_ARG, "flags of tensor %d select no orientation", t);
         if (rows[t] < 0 || cols[t] < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size (tensor %d)", t);
-        a[t].rows = rows[t];
-        a[t].cols = cols[t];
-        a[t].flags = flags;
         if (rows[t] == 0 || cols[t] == 0) continue;
-        if (!x_bf16[t] || !q_row[t] || !s_row[t])
-            return fail(MXFP8_ERR_INVALID_ARG, "x or an output of tensor %d is NULL", t);
+        const int fb = (f & MX_SCALE_FLOOR) ? 1 : 0;
+        if (floor_bit >= 0 && fb != floor_bit)
+            return fail(MXFP8_ERR_INVALID_ARG, "MX_SCALE_FLOOR must be the same for every tensor");
+        floor_bit = fb;
+        if (!x_bf16[t]) return fail(MXFP8_ERR_INVALID_ARG, "x of tensor %d is NULL", t);
+        if (row && (!q_row || !s_row || !q_row[t] || !s_row[t]))
+            return fail(MXFP8_ERR_INVALID_ARG, "rowwise output of tensor %d is NULL", t);
+        if (col && (!q_col || !s_col || !q_col[t] || !s_col[t]))
+            return fail(MXFP8_ERR_INVALID_ARG, "colwise output of tensor %d is NULL", t);
         if (cols[t] % 32)
             return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (tensor %d, cols=%lld)", t, (long long)cols[t]);
+        if (col && rows[t] % 32)
+            return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "colwise needs rows %% 32 == 0 (tensor %d)", t);
         if (ld[t] < cols[t]) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols (tensor %d)", t);
-        if (ld[t] % 8 || !aligned16(x_bf16[t]) || !aligned16(q_row[t]) || !aligned16(s_row[t]))
-            return fail(MXFP8_ERR_MISALIGNED, "pointer or ld of tensor %d not 16-byte aligned", t);
+        if (ld[t] % 8 || !aligned16(x_bf16[t]))
+            return fail(MXFP8_ERR_MISALIGNED, "x or ld of tensor %d not 16-byte aligned", t);
+        if ((row && (!aligned16(q_row[t]) || !aligned16(s_row[t]))) ||
+            (col && (!aligned16(q_col[t]) || !aligned16(s_col[t]))))
+            return fail(MXFP8_ERR_MISALIGNED, "an output of tensor %d is not 16-byte aligned", t);
         if ((cols[t] + 127) / 128 > 65535 || rows[t] > 0x7FFFFFFF)
             return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "tensor %d too large", t);
-        a[t].x = static_cast<const uint16_t*>(x_bf16[t]);
-        a[t].ld = ld[t];
-        a[t].q_row = static_cast<uint8_t*>(q_row[t]);
-        a[t].s_row = static_cast<uint8_t*>(s_row[t]);
+        QuantMxArgs& a = col ? with_col[n_col++] : row_only[n_row++];
+        a.x = static_cast<const uint16_t*>(x_bf16[t]);
+        a.rows = rows[t];
+        a.cols = cols[t];
+        a.ld = ld[t];
+        a.q_row = row ? static_cast<uint8_t*>(q_row[t]) : nullptr;
+        a.s_row = row ? static_cast<uint8_t*>(s_row[t]) : nullptr;
+        a.q_col = col ? static_cast<uint8_t*>(q_col[t]) : nullptr;
+        a.s_col = col ? static_cast<uint8_t*>(s_col[t]) : nullptr;
+        a.flags = f;
     }
-    return cuda_result(launch_quantize_mx_rows_batch(count, a, reinterpret_cast<cudaStream_t>(stream)),
-                       "fp8_quantize_mx_batch launch");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (n_row) e = launch_quantize_mx_rows_batch(n_row, row_only, st);
+    if (e == cudaSuccess && n_col) e = launch_quantize_mx_cols_batch(n_col, with_col, st);
+    return cuda_result(e, "fp8_quantize_mx_batch launch");
 }
 
 mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int64_t cols,

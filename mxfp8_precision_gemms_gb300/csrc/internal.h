@@ -30,6 +30,10 @@ cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s);
 // Rowwise MX quantization of count (<= kMaxBatch) tensors in one launch;
 // every a[t].flags carries the same MX_SCALE_FLOOR choice.
 cudaError_t launch_quantize_mx_rows_batch(int count, const QuantMxArgs* a, cudaStream_t s);
+// Colwise (or both-orientation) MX quantization of count tensors with as few
+// launches as possible (one per 8 tensors); every a[t].flags includes
+// MX_COLWISE and carries the same MX_SCALE_FLOOR choice.
+cudaError_t launch_quantize_mx_cols_batch(int count, const QuantMxArgs* a, cudaStream_t s);
 cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float* amax,
                                    float* scale, uint8_t* q, cudaStream_t s);
 // Tensors one batched per-tensor launch accepts.

@@ -249,43 +249,49 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kTileThreads = 128;
 constexpr uint32_t kTileSmem = kTile * kTile * 2;
 
-template <bool ROW, bool FLOOR>
-__global__ void __launch_bounds__(kTileThreads)
-    quantize_mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, QuantMxArgs a,
-                            int64_t nkc_row, int64_t nkc_col, uint64_t limit_ns, bool v8) {
-    extern __shared__ uint8_t tile_raw[];
-    __shared__ __align__(8) uint64_t bar;
-    uint8_t* tile = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(tile_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t st = smem_u32(tile), bb = smem_u32(&bar);
+// What one tile kernel needs to know about its tensor.
+struct TileArgs {
+    int64_t rows, cols;
+    uint8_t* q_row;
+    uint8_t* s_row;
+    uint8_t* q_col;
+    uint8_t* s_col;
+    int64_t nkc_row;  // 128-wide K tiles of the rowwise operand (column tiles)
+    int64_t nkc_col;  // ... of the colwise one (row tiles)
+    bool row;         // rowwise outputs too
+    bool v8;          // 32-byte aligned outputs: 256-bit stores
+};
+
+// One 128 x 128 tile (row tile rt, column tile ct) of tensor `map` / `a`,
+// staged in the CTA's 32 KB shared tile `st` through mbarrier `bb` whose
+// next phase has parity `parity`.  Returns false when the copy did not land
+// in time (the status is recorded).
+template <bool FLOOR>
+__device__ __forceinline__ bool tile_quantize(const CUtensorMap* map, const TileArgs& a, int64_t rt,
+                                              int64_t ct, uint32_t st, uint32_t bb, uint32_t parity,
+                                              uint64_t limit_ns) {
     const int tid = threadIdx.x;
-    const int64_t rt = blockIdx.x, ct = blockIdx.y;
-    if (tid == 0) {
-        mbar_init(bb, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
     if (tid == 0) {
         mbar_arrive_expect_tx(bb, kTileSmem);
-        tma_load_2d(st, &tm_x, bb, static_cast<int32_t>(ct * kTile), static_cast<int32_t>(rt * kTile));
-        tma_load_2d(st + kTileSmem / 2, &tm_x, bb, static_cast<int32_t>(ct * kTile + 64),
+        tma_load_2d(st, map, bb, static_cast<int32_t>(ct * kTile), static_cast<int32_t>(rt * kTile));
+        tma_load_2d(st + kTileSmem / 2, map, bb, static_cast<int32_t>(ct * kTile + 64),
                     static_cast<int32_t>(rt * kTile));
     }
     const int never = 0;
-    if (!mbar_wait(bb, 0, limit_ns, &never)) {
+    if (!mbar_wait(bb, parity, limit_ns, &never)) {
         if (tid == 0) record_status(MXFP8_ERR_TIMEOUT);
-        mbar_wait(bb, 0, limit_ns, &never);  // the copy may still land: give it time
-        return;
+        mbar_wait(bb, parity, limit_ns, &never);  // the copy may still land: give it time
+        return false;
     }
     // 16-byte chunk k (0..15) of tile row r
     auto chunk_addr = [&](int r, int k) {
         return st + (k >> 3) * (kTileSmem / 2) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
     };
 
-    if constexpr (ROW) {
+    if (a.row) {
         const int r = tid;
         const int64_t row = rt * kTile + r;
-        uint8_t* s_tile = a.s_row + (rt * nkc_row + ct) * 512;
+        uint8_t* s_tile = a.s_row + (rt * a.nkc_row + ct) * 512;
         uint32_t bytes = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kTileThreads)
             const int64_t col = ct * kTile + 32 * b;
             uint8_t byte;
             mx_block32<FLOOR>(w, (row < a.rows && col < a.cols) ? a.q_row + row * a.cols + col : nullptr,
-                              &byte, v8);
+                              &byte, a.v8);
             bytes |= static_cast<uint32_t>(byte) << (8 * b);
         }
         *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = bytes;
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kTileThreads)
         const uint32_t bc[4] = {e8m0_byte(mlo & 0xFFFFu, FLOOR), e8m0_byte(mlo >> 16, FLOOR),
                                 e8m0_byte(mhi & 0xFFFFu, FLOOR), e8m0_byte(mhi >> 16, FLOOR)};
         const int64_t r0 = rt * kTile + 32 * j;  // output column (an input row)
-        uint8_t* s_tile = a.s_col + (ct * nkc_col + rt) * 512;
+        uint8_t* s_tile = a.s_col + (ct * a.nkc_col + rt) * 512;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t* src = c < 2 ? lo : hi;
@@ -345,10 +351,71 @@ __global__ void __launch_bounds__(kTileThreads)
                 }
             }
             const int64_t k0 = ct * kTile + 4 * g + c;  // output row (an input column)
-            if (k0 < a.cols && r0 < a.rows) st32(a.q_col + k0 * a.rows + r0, q, v8);
+            if (k0 < a.cols && r0 < a.rows) st32(a.q_col + k0 * a.rows + r0, q, a.v8);
             s_tile[swz_word(4 * g + c) + j] = static_cast<uint8_t>(bc[c]);
         }
     }
+    return true;
+}
+
+// Rowwise + colwise (or colwise only) MX quantization of a 128 x 128 tile
+// staged by TMA: two 64-column boxes with 128-byte swizzle (16-byte chunk k
+// of a 128-byte half-row r sits at chunk k ^ (r % 8)), so both access
+// patterns are free of bank conflicts.
+//   colwise: thread t owns columns 4g..4g+3 (g = t % 32) of the 32-row block
+//            j = t / 32, read as 32 64-bit loads (two BF16 pairs per row);
+//            each column's 32 E4M3 bytes are one output row segment of q_col.
+//   rowwise: thread t owns tile row t, its four 32-value blocks read as
+//            16-byte chunks.
+// The E8M0 rule and packing are the row kernel's; 128 threads per CTA, one
+// tile per CTA (grid: row tiles x column tiles).
+template <bool FLOOR>
+__global__ void __launch_bounds__(kTileThreads)
+    quantize_mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, TileArgs a, uint64_t limit_ns) {
+    extern __shared__ uint8_t tile_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    uint8_t* tile = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(tile_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t bb = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bb, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    tile_quantize<FLOOR>(&tm_x, a, blockIdx.x, blockIdx.y, smem_u32(tile), bb, 0, limit_ns);
+}
+
+// The same over several tensors in one launch: a 1D grid over all their
+// tiles (tensor t owns blocks [tile_end[t-1], tile_end[t]), row tiles
+// fastest), each CTA one tile.
+constexpr int kMaxTileBatch = 8;
+struct MxTileBatch {
+    CUtensorMap map[kMaxTileBatch];
+    TileArgs arg[kMaxTileBatch];
+    int64_t row_tiles[kMaxTileBatch];
+    int64_t tile_end[kMaxTileBatch];
+    int count;
+};
+
+template <bool FLOOR>
+__global__ void __launch_bounds__(kTileThreads)
+    quantize_mx_tile_batch_kernel(const __grid_constant__ MxTileBatch b, uint64_t limit_ns) {
+    extern __shared__ uint8_t tile_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    uint8_t* tile = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(tile_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t bb = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bb, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int64_t blk = blockIdx.x;
+    int t = 0;
+    while (t + 1 < b.count && blk >= b.tile_end[t]) ++t;
+    const int64_t local = blk - (t ? b.tile_end[t - 1] : 0);
+    tile_quantize<FLOOR>(&b.map[t], b.arg[t], local % b.row_tiles[t], local / b.row_tiles[t],
+                         smem_u32(tile), bb, 0, limit_ns);
 }
 
 // ---------------------------------------------------------- per-tensor --
@@ -806,16 +873,38 @@ cudaError_t launch_quantize_mx_rows_batch(int count, const QuantMxArgs* a, cudaS
     return cudaGetLastError();
 }
 
-template <bool ROW, bool FLOOR>
-cudaError_t launch_mx_tile(const QuantMxArgs& a, const CUtensorMap& map, cudaStream_t s) {
+// The tile kernels' view of a tensor; false when its TMA map cannot be made.
+bool tile_args(const QuantMxArgs& a, CUtensorMap* map, TileArgs* t) {
     const int64_t row_tiles = (a.rows + kTile - 1) / kTile;
     const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
-    if (col_tiles > 65535 || row_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    const bool v8 = (reinterpret_cast<uintptr_t>(a.q_col) % 32 == 0) &&
-                    (!ROW || reinterpret_cast<uintptr_t>(a.q_row) % 32 == 0);
-    dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
-    quantize_mx_tile_kernel<ROW, FLOOR><<<grid, kTileThreads, kTileSmem + 1024, s>>>(
-        map, a, col_tiles, row_tiles, wait_limit_ns(), v8);
+    if (col_tiles > 65535 || row_tiles > 0x7FFFFFFF) return false;
+    // the tensor map wants a 16-byte aligned base and row stride (checked by the API)
+    if (!encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.rows, a.cols, a.ld * 2,
+                              64, kTile, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    const bool row = (a.flags & MX_ROWWISE) != 0;
+    t->rows = a.rows;
+    t->cols = a.cols;
+    t->q_row = a.q_row;
+    t->s_row = a.s_row;
+    t->q_col = a.q_col;
+    t->s_col = a.s_col;
+    t->nkc_row = col_tiles;
+    t->nkc_col = row_tiles;
+    t->row = row;
+    t->v8 = (reinterpret_cast<uintptr_t>(a.q_col) % 32 == 0) &&
+            (!row || reinterpret_cast<uintptr_t>(a.q_row) % 32 == 0);
+    return true;
+}
+
+cudaError_t launch_mx_tile(const QuantMxArgs& a, const CUtensorMap& map, const TileArgs& t,
+                           cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>(t.nkc_col), static_cast<unsigned>(t.nkc_row));
+    if (a.flags & MX_SCALE_FLOOR) {
+        quantize_mx_tile_kernel<true><<<grid, kTileThreads, kTileSmem + 1024, s>>>(map, t, wait_limit_ns());
+    } else {
+        quantize_mx_tile_kernel<false><<<grid, kTileThreads, kTileSmem + 1024, s>>>(map, t, wait_limit_ns());
+    }
     return cudaGetLastError();
 }
 
@@ -824,14 +913,10 @@ cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s) {
     const bool fl = a.flags & MX_SCALE_FLOOR;
     const int64_t row_tiles = (a.rows + kTile - 1) / kTile;
     if (col && a.rows > 0 && a.cols > 0) {
-        // colwise (with or without rowwise): TMA-staged tile kernel; the tensor
-        // map wants a 16-byte aligned base and row stride (checked by the API)
+        // colwise (with or without rowwise): TMA-staged tile kernel
         CUtensorMap map;
-        if (encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.rows, a.cols,
-                                 a.ld * 2, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) {
-            if (row) return fl ? launch_mx_tile<true, true>(a, map, s) : launch_mx_tile<true, false>(a, map, s);
-            return fl ? launch_mx_tile<false, true>(a, map, s) : launch_mx_tile<false, false>(a, map, s);
-        }
+        TileArgs t;
+        if (tile_args(a, &map, &t)) return launch_mx_tile(a, map, t, s);
     }
     if (row && col) {
         return fl ? launch_mx<true, true, true, false>(a, row_tiles, s)
@@ -843,6 +928,46 @@ cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s) {
     }
     return fl ? launch_mx<false, true, true, false>(a, row_tiles, s)
               : launch_mx<false, true, false, false>(a, row_tiles, s);
+}
+
+cudaError_t launch_quantize_mx_cols_batch(int count, const QuantMxArgs* a, cudaStream_t s) {
+    MxTileBatch b{};
+    int n = 0;
+    int64_t tiles = 0;
+    bool floor = false;
+    cudaError_t e = cudaSuccess;
+    auto flush = [&]() -> cudaError_t {
+        if (n == 0) return cudaSuccess;
+        b.count = n;
+        const unsigned grid = static_cast<unsigned>(tiles);
+        if (floor) {
+            quantize_mx_tile_batch_kernel<true><<<grid, kTileThreads, kTileSmem + 1024, s>>>(b, wait_limit_ns());
+        } else {
+            quantize_mx_tile_batch_kernel<false><<<grid, kTileThreads, kTileSmem + 1024, s>>>(b, wait_limit_ns());
+        }
+        n = 0;
+        tiles = 0;
+        return cudaGetLastError();
+    };
+    for (int t = 0; t < count && e == cudaSuccess; ++t) {
+        if (a[t].rows <= 0 || a[t].cols <= 0) continue;
+        floor = (a[t].flags & MX_SCALE_FLOOR) != 0;
+        if (!tile_args(a[t], &b.map[n], &b.arg[n])) {
+            e = launch_quantize_mx(a[t], s);  // no TMA map for this tensor: the register-staged kernel
+            continue;
+        }
+        const int64_t t_tiles = b.arg[n].nkc_col * b.arg[n].nkc_row;
+        if (tiles + t_tiles > 0x7FFFFFFF) {
+            if ((e = flush()) != cudaSuccess) break;
+            if (!tile_args(a[t], &b.map[0], &b.arg[0])) return cudaErrorInvalidValue;
+        }
+        b.row_tiles[n] = b.arg[n].nkc_col;
+        tiles += t_tiles;
+        b.tile_end[n] = tiles;
+        if (++n == kMaxTileBatch) e = flush();
+    }
+    if (e == cudaSuccess) e = flush();
+    return e;
 }
 
 cudaError_t launch_quantize_mx_grouped(const QuantMxArgs& a, cudaStream_t s) {

@@ -85,22 +85,30 @@ def test_host_validation(lib):
     assert B(2, arr(bad), arr(ns), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_MISALIGNED
     neg = (ctypes.c_int64 * 2)(64, -1)
     assert B(2, arr(xs), arr(neg), 0, P, P, arr(xs), P, None) == m.MXFP8_ERR_INVALID_ARG
-    # batched rowwise MX
+    # batched MX
     QB = lib.fp8_quantize_mx_batch
     r64 = (ctypes.c_int64 * 3)(64, 64, 64)
     c48 = (ctypes.c_int64 * 3)(64, 48, 64)
+    r48 = (ctypes.c_int64 * 3)(64, 48, 64)
     l60 = (ctypes.c_int64 * 3)(64, 64, 60)
-    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), m.MX_COLWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_INVALID_ARG
-    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), m.MX_ROWWISE | m.MX_COLWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_INVALID_ARG
-    assert QB(0, arr(xs), arr(r64), arr(r64), arr(r64), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
-    assert QB(17, arr(xs), arr(r64), arr(r64), arr(r64), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
-    assert QB(3, arr(xs), arr(r64), arr(c48), arr(r64), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
-    assert QB(3, arr(xs), arr(r64), arr(r64), arr(l60), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_INVALID_ARG
-    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), m.MX_ROWWISE, None, arr(xs), None) == m.MXFP8_ERR_INVALID_ARG
+    fl = lambda *v: arr((ctypes.c_uint * 3)(*v))
+    R, C, F = m.MX_ROWWISE, m.MX_COLWISE, m.MX_SCALE_FLOOR
+    qs = arr(xs)
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, 0, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, 9, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, R | F, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(0, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, R, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert QB(17, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, R, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert QB(3, arr(xs), arr(r64), arr(c48), arr(r64), fl(R, R, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert QB(3, arr(xs), arr(r48), arr(r64), arr(r64), fl(R, C, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(l60), fl(R, R, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, R, R), None, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), fl(R, C, R), qs, qs, None, None, None) == m.MXFP8_ERR_INVALID_ARG
+    assert QB(3, arr(xs), arr(r64), arr(r64), arr(r64), None, qs, qs, qs, qs, None) == m.MXFP8_ERR_INVALID_ARG
     bad3 = (ctypes.c_void_p * 3)(P, P, P + 8)
-    assert QB(3, arr(bad3), arr(r64), arr(r64), arr(r64), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_ERR_MISALIGNED
+    assert QB(3, arr(bad3), arr(r64), arr(r64), arr(r64), fl(R, R, R), qs, qs, qs, qs, None) == m.MXFP8_ERR_MISALIGNED
     z3 = (ctypes.c_int64 * 3)(0, 0, 0)
-    assert QB(3, arr(xs), arr(z3), arr(r64), arr(r64), m.MX_ROWWISE, arr(xs), arr(xs), None) == m.MXFP8_OK
+    assert QB(3, arr(xs), arr(z3), arr(r64), arr(r64), fl(R, C, R | C), None, None, None, None, None) == m.MXFP8_OK
     # GEMM
     G = lib.fp8_scaled_gemm
     assert G(5, 0, 0, P, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG

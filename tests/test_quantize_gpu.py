@@ -122,15 +122,16 @@ def test_quantize_mx_batch_matches_oracle(flags):
             xs.append(to_dev_bf16(flat)[8:].view(b.shape))
         else:
             xs.append(to_dev_bf16(b))
-    outs = [(filled(b.shape, 0xA5), filled(m.mxfp8_scale_bytes(*b.shape), 0xA5)) for b in bits]
+    outs = [{"q_row": filled(b.shape, 0xA5), "s_row": filled(m.mxfp8_scale_bytes(*b.shape), 0xA5)}
+            for b in bits]
     m.fp8_quantize_mx_batch(xs, flags, outs=outs)
     assert_ok()
-    for b, (q, sc) in zip(bits, outs):
+    for b, o in zip(bits, outs):
         if b.size == 0:
             continue
         want = oracle.quantize_mx(b, flags)
-        assert np.array_equal(host(q), want["q_row"])
-        assert np.array_equal(host(sc), want["s_row"])
+        assert np.array_equal(host(o["q_row"]), want["q_row"])
+        assert np.array_equal(host(o["s_row"]), want["s_row"])
 
 
 def test_quantize_mx_batch_of_sixteen_mlp_operands():
@@ -141,10 +142,33 @@ def test_quantize_mx_batch_of_sixteen_mlp_operands():
     bits += [random_bits((32 * (t + 1), 64 * ((t % 3) + 1)), "wide", seed=40 + t) for t in range(14)]
     outs = m.fp8_quantize_mx_batch([to_dev_bf16(b) for b in bits])
     assert_ok()
-    for b, (q, sc) in zip(bits, outs):
+    for b, o in zip(bits, outs):
         want = oracle.quantize_mx(b, ROW)
-        assert np.array_equal(host(q), want["q_row"])
-        assert np.array_equal(host(sc), want["s_row"])
+        assert np.array_equal(host(o["q_row"]), want["q_row"])
+        assert np.array_equal(host(o["s_row"]), want["s_row"])
+
+
+@pytest.mark.parametrize("floor", [0, FLOOR])
+def test_quantize_mx_batch_mixed_orientations(floor):
+    """The backward's operands in one call (dY both ways, W and X colwise) plus
+    rowwise-only and empty tensors, and more colwise tensors than one launch
+    takes (nine): every output equals the oracle's."""
+    w = workloads.backward(seed=4, device="cpu", tokens=512, d_in=384, d_out=256)
+    bits = [workloads.bits(w["dY"]), workloads.bits(w["W"]), workloads.bits(w["X"])]
+    flags = [ROW | COL, COL, COL]
+    bits += [random_bits((96, 160), "student", seed=60), np.zeros((0, 64), np.uint16)]
+    flags += [ROW, COL]
+    bits += [random_bits((32 * (t + 1), 32 * (t + 2)), "wide", seed=70 + t) for t in range(7)]
+    flags += [COL if t % 2 else ROW | COL for t in range(7)]
+    flags = [f | floor for f in flags]
+    outs = m.fp8_quantize_mx_batch([to_dev_bf16(b) for b in bits], flags)
+    assert_ok()
+    for b, f, o in zip(bits, flags, outs):
+        if b.size == 0:
+            continue
+        want = oracle.quantize_mx(b, f)
+        for k in want:
+            assert np.array_equal(host(o[k]), want[k]), k
 
 
 def _anchor_blocks(floor):
