@@ -111,12 +111,16 @@ struct Cfg {
     // plain GEMM: per epilogue warp a 2 KB staging tile for the TMA stores of C
     static constexpr uint32_t OFF_EPI = (OFF_PREFIX + 1023) / 1024 * 1024;
     static constexpr uint32_t SMEM_PLAIN = OFF_EPI + EPI_WARPS * EPI_TILE_BYTES;
-    static constexpr uint32_t SMEM_GROUPED = OFF_PREFIX + 3 * (MAX_GROUPS + 1) * 4;
+    // grouped GEMM: two prefix tables (tiles and units per expert group), then
+    // the staging tiles (512-byte aligned: the 64-byte swizzle's period)
+    static constexpr uint32_t OFF_EPI_G = (OFF_PREFIX + 2 * (MAX_GROUPS + 1) * 4 + 511) / 512 * 512;
+    static constexpr uint32_t SMEM_GROUPED = OFF_EPI_G + EPI_WARPS * EPI_TILE_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024B alignment");
     static_assert(ACC_COLS + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(STAGES % SLOTS_PER_BAR == 0, "slots come in barrier pairs");
-    static_assert(SMEM_GROUPED + 1024 <= 232448, "shared memory budget");
-    static_assert(SMEM_PLAIN + 1024 <= 232448, "shared memory budget");
+    // + 1024: the base is aligned up at run time; + 16: the static variables
+    static_assert(SMEM_GROUPED + 1024 + 16 <= 232448, "shared memory budget");
+    static_assert(SMEM_PLAIN + 1024 + 16 <= 232448, "shared memory budget");
 };
 
 struct KParams {
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* mtile_prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
     int32_t* mgroup_prefix = mtile_prefix + (MAX_GROUPS + 1);
-    int32_t* offs = mgroup_prefix + (MAX_GROUPS + 1);
+    const int32_t* offs = p.offsets;  // validated below before any use
     __shared__ int64_t s_total_units;
 
     if (threadIdx.x == 0) {
@@ -249,7 +253,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int g0 = 0; g0 <= G; g0 += 32) {
                 const int g = g0 + lane;
                 int32_t tiles = 0;
-                if (g <= G) offs[g] = p.offsets[g];
                 if (g < G) {
                     const int32_t m = p.offsets[g + 1] - p.offsets[g];
                     if (m < 0) ok = false;
@@ -537,15 +540,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (PAIR) mbar_arrive_cluster(empty_bar);
                 else mbar_arrive(empty_bar);
             }
-            if constexpr (!GROUPED) {
+            // This warp's 32 rows go out through TMA stores when they are all
+            // rows of C this tile owns (always, for a valid plain tile; for an
+            // expert group's last tile only the warps inside the group), else
+            // with masked direct stores.
+            bool staged = tl.a_valid;
+            if constexpr (GROUPED) staged = staged && tl.a_row + quarter * 32 + 32 <= tl.row_end;
+            {
                 // BF16 through a swizzled 32 x 32 staging tile and TMA stores:
                 // lane = row; 16-byte chunk j of a 64-byte row goes to chunk
                 // j ^ ((row >> 1) & 3), the 64-byte swizzle the store undoes,
                 // which also keeps each 8-lane phase on distinct banks
-                const uint32_t stile = sbase + C::OFF_EPI + (warp - 2) * EPI_TILE_BYTES;
+                const uint32_t stile =
+                    sbase + (GROUPED ? C::OFF_EPI_G : C::OFF_EPI) + (warp - 2) * EPI_TILE_BYTES;
                 const uint32_t srow = stile + lane * 64;
                 const uint32_t sw = (lane >> 1) & 3;
-                if (tl.a_valid) {
+                if (staged) {
                     const int32_t y = static_cast<int32_t>(tl.a_row + quarter * 32);
                     const int32_t x0 = tl.n_tile * BN + half * 128;
 #pragma unroll
@@ -573,7 +583,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
-            } else {
+            }
+            if (GROUPED && !staged) {
                 const int64_t row = tl.a_row + quarter * 32 + lane;
                 if (tl.a_valid && row < tl.row_end) {
                     uint16_t* crow = p.c + row * p.ldc;
@@ -600,10 +611,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             acc_phase ^= 1u;
         }
-        if constexpr (!GROUPED) {
-            if (lane == 0) bulk_wait_group0();  // every store of C has completed
-            __syncwarp();
-        }
+        if (lane == 0) bulk_wait_group0();  // every store of C has completed
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -732,9 +741,10 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     }
     p.c = g.c;
     p.ldc = g.ldc;
-    CUtensorMap tc = ta;  // grouped: unused (C rows of other experts must not be touched)
-    if (!grouped &&
-        !encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
+    // C as BF16 32 x 32 boxes (grouped: only warps whose rows all lie in one
+    // expert group store through it)
+    CUtensorMap tc;
+    if (!encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
                               CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     p.offsets = g.offsets;
