@@ -619,23 +619,49 @@ def oracle_inputs(seed: int, m_rows: int, n_rows: int, d_in=4096):
     return x, w
 
 
-def oracle_sample(x, w):
+def oracle_sample(x, w, keep=None):
     """Time the FP64 oracle on a slice: quantize X and W rowwise, then their
-    GEMM.  Returns (seconds, flops of the slice)."""
+    GEMM.  Returns (seconds, flops of the slice); `keep` (a dict) receives the
+    oracle's outputs."""
     import oracle
     t0 = time.perf_counter()
     a = oracle.quantize_mx(x, oracle.ROWWISE)
     b = oracle.quantize_mx(w, oracle.ROWWISE)
-    oracle.gemm_mx(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
-    return time.perf_counter() - t0, 2.0 * x.shape[0] * w.shape[0] * x.shape[1]
+    c = oracle.gemm_mx(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
+    t = time.perf_counter() - t0
+    if keep is not None:
+        keep.update(a=a, b=b, c=c)
+    return t, 2.0 * x.shape[0] * w.shape[0] * x.shape[1]
 
 
-def cpu_baseline(seed=0, budget_s=15.0):
+def sample_check(m, x, w, ref):
+    """The library's path (one batched quantize launch, the MX GEMM) on the
+    oracle's sample: quantized bytes must equal the oracle's, C must lie within
+    |c - ref| <= 1e-2 |ref| + 1e-3 rms(ref)."""
+    import numpy as np
+    dev = torch.device("cuda", torch.cuda.current_device())
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    qa, qb = m.fp8_quantize_mx_batch([to_dev(x), to_dev(w)])
+    c = m.fp8_scaled_gemm(m.GEMM_MX, qa["q_row"], qa["s_row"], qb["q_row"], qb["s_row"])
+    torch.cuda.synchronize()
+    bytes_equal = all(np.array_equal(t.cpu().numpy(), ref[k][f])
+                      for t, k, f in ((qa["q_row"], "a", "q_row"), (qa["s_row"], "a", "s_row"),
+                                      (qb["q_row"], "b", "q_row"), (qb["s_row"], "b", "s_row")))
+    g = c.float().cpu().numpy().astype(np.float64)
+    r = ref["c"]
+    rms = float(np.sqrt(np.mean(r * r)))
+    ratio = float(np.max(np.abs(g - r) / (1e-2 * np.abs(r) + 1e-3 * rms)))
+    return {"quantized_bytes_equal": bool(bytes_equal), "gemm_max_err_over_tolerance": ratio,
+            "pass": bool(bytes_equal and ratio <= 1.0), "status": m.mxfp8_last_device_status()}
+
+
+def cpu_baseline(m, seed=0, budget_s=15.0):
     import oracle
     X, W = oracle_inputs(seed, 8192, 2048)
     m_rows, n_rows = 64, 256
+    keep = {}
     while True:
-        t, fl = oracle_sample(X[:m_rows], W[:n_rows])
+        t, fl = oracle_sample(X[:m_rows], W[:n_rows], keep)
         if t >= budget_s / 2 or (m_rows >= X.shape[0] and n_rows >= W.shape[0]):
             break
         f = max(2, int(budget_s / max(t, 1e-3) / 1.5))
@@ -646,7 +672,8 @@ def cpu_baseline(seed=0, budget_s=15.0):
     return {"value": fl / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"X rows 0..{m_rows - 1} of 8192 and W rows 0..{n_rows - 1} of 16384 "
                       f"(full K=4096), quantized rowwise then multiplied in FP64; {t:.1f} s",
-            "seconds": t}
+            "seconds": t,
+            "check": sample_check(m, X[:m_rows], W[:n_rows], keep)}
 
 
 def run_reference(args):
@@ -892,7 +919,7 @@ def main():
     if rows is not None:
         line["hot_path_rows"] = rows
     if world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.seed)
+        line["cpu_baseline"] = cpu_baseline(m, args.seed)
     print(json.dumps(line))
     if pg:
         pg.destroy_process_group()
