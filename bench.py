@@ -841,19 +841,25 @@ def main():
             pg.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-resident timed region
+    # ---- device-resident timed region (NVTX ranges name the phases for a
+    # profiler's timeline; they sit outside the per-step loop)
+    nvtx = torch.cuda.nvtx
+    nvtx.range_push("warmup")
     for _ in range(args.warmup):
         wl.step(None, st)
+    nvtx.range_pop()
     barrier()
     clocks = ClockSampler(local)
     clocks.start()
     timer = Timer()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    nvtx.range_push(f"timed: {args.steps} steps of quantize X and W + MX GEMM")
     ev0.record()
     for _ in range(args.steps):
         wl.step(timer, st)
     ev1.record()
+    nvtx.range_pop()
     barrier()
     clk = clocks.stop()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
@@ -867,12 +873,16 @@ def main():
     # memory; steps are pipelined over three streams (H2D, compute, D2H) with
     # double-buffered device tensors, so one step's copies overlap its
     # neighbours' compute.
+    nvtx.range_push("e2e: host buffers, pipelined copies")
     e2e = e2e_pipelined(m, wl, dev, args.e2e_steps, pg)
+    nvtx.range_pop()
     e2e["value"] = job_throughput(wl.flops, world, e2e["ms_per_step"])
 
     rows = None
     if not args.no_rows:
+        nvtx.range_push("hot-path rows")
         rows = hot_path_rows(m, dev, steps=max(20, args.steps // 8), warmup=args.warmup)
+        nvtx.range_pop()
 
     if rank != 0:
         if pg:
