@@ -855,9 +855,11 @@ def main():
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     nvtx.range_push(f"timed: {args.steps} steps of quantize X and W + MX GEMM")
+    # per-kernel spans on every 4th step: events around every launch cost the
+    # step ~0.5 % (measured), a quarter of that sampled this way
     ev0.record()
-    for _ in range(args.steps):
-        wl.step(timer, st)
+    for i in range(args.steps):
+        wl.step(timer if i % 4 == 0 else None, st)
     ev1.record()
     nvtx.range_pop()
     barrier()
