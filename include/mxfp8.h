@@ -216,7 +216,6 @@ mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt,
                                          mxfp8_stream_t stream);
 
 /*
- * fp8_scaled_gemm - C = A . B^T/*
  * fp8_scaled_gemm - C = A . B^T with FP32 accumulation and a BF16 epilogue
  * (round to nearest even).
  * ("Olmo-core MoE report", Section 11.1.1: block-scaled tcgen05.mma with an
