@@ -67,7 +67,7 @@ def _worker(rank, world, port, out):
 @pytest.fixture(scope="module")
 def two_ranks():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     return dict(out)

@@ -31,7 +31,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_replicas_take_the_slowest_rank():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     for r in range(world):
