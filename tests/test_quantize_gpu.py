@@ -295,6 +295,30 @@ def test_quantize_tensor_batch_matches_oracle(fmt):
         assert hs[t] == np.float32(wsc).view(np.uint32), t
 
 
+@pytest.mark.parametrize("fmt", [m.FP8_E4M3, m.FP8_E5M2])
+def test_quantize_tensor_16_byte_aligned(fmt):
+    """Inputs that start 16 bytes past a 32-byte boundary (the 16-byte load
+    path of the single-launch kernel), with odd sizes, alone and batched."""
+    sizes = [1000003, 4097, 40]
+    bits = [random_bits((n,), "student", seed=80 + n % 7).reshape(-1) for n in sizes]
+    xs = []
+    for b in bits:
+        flat = np.zeros(b.size + 8, np.uint16)
+        flat[8:] = b
+        xs.append(to_dev_bf16(flat)[8:])
+    ws = torch.zeros(m.mxfp8_tensor_workspace_bytes(), dtype=torch.uint8, device=device())
+    qs, amax, scale = m.fp8_quantize_tensor_batch(xs, fmt, workspace=ws)
+    assert_ok()
+    for t, b in enumerate(bits):
+        wa, wsc, wq = oracle.quantize_tensor(b, fmt)
+        assert np.array_equal(host(qs[t]), wq.reshape(-1)), t
+        assert host(amax).view(np.uint32)[t] == np.float32(wa).view(np.uint32)
+        assert host(scale).view(np.uint32)[t] == np.float32(wsc).view(np.uint32)
+        q1, a1, s1 = m.fp8_quantize_tensor(xs[t], fmt, workspace=ws)
+        assert_ok()
+        assert np.array_equal(host(q1), wq.reshape(-1)), t
+
+
 def test_quantize_tensor_batch_of_sixteen():
     """The largest batch: sixteen tensors of different sizes."""
     cases = [random_bits((1 + 997 * t,), "normal", seed=10 + t).reshape(-1) for t in range(16)]
