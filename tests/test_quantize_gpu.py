@@ -171,6 +171,37 @@ def test_quantize_mx_batch_mixed_orientations(floor):
             assert np.array_equal(host(o[k]), want[k]), k
 
 
+@pytest.mark.parametrize("flags", [COL, ROW | COL, COL | FLOOR])
+def test_quantize_mx_colwise_16_byte_aligned_outputs(flags):
+    """Colwise (and both-orientation) outputs that start 16 bytes past a
+    32-byte boundary (the tile kernel's 16-byte store path), alone and in a
+    batch."""
+    rows, cols = 224, 160
+    bits = random_bits((rows, cols), "student", seed=90 + flags)
+    want = oracle.quantize_mx(bits, flags)
+    for batched in (False, True):
+        bufs, out = [], {}
+        for k, shape in (("q_row", (rows, cols)), ("q_col", (cols, rows))):
+            if k in want:
+                b = filled(rows * cols + 64, 0xA5)
+                bufs.append(b)
+                out[k] = b[16:16 + rows * cols].view(shape)
+        for k, n in (("s_row", m.mxfp8_scale_bytes(rows, cols)), ("s_col", m.mxfp8_scale_bytes(cols, rows))):
+            if k in want:
+                out[k] = filled(n, 0xA5)
+        x = to_dev_bf16(bits)
+        if batched:
+            m.fp8_quantize_mx_batch([x, x], [flags, flags], outs=[out, {k: torch.empty_like(v) for k, v in out.items()}])
+        else:
+            m.fp8_quantize_mx(x, flags, **out)
+        assert_ok()
+        for k in want:
+            assert np.array_equal(host(out[k]).reshape(want[k].shape), want[k]), (k, batched)
+        for b in bufs:
+            hb = host(b)
+            assert np.all(hb[:16] == 0xA5) and np.all(hb[16 + rows * cols:] == 0xA5)
+
+
 def _anchor_blocks(floor):
     """Blocks whose scale byte is fixed by an anchor value, filled with every
     finite BF16 pattern at or below the anchor: all BF16 values x all scales."""
