@@ -900,6 +900,7 @@ def main():
         "metric": METRIC,
         "value": value,
         "unit": UNIT,
+        "value_frac_of_4500_fp8_dense": value / (4500.0 * world),
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
