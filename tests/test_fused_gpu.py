@@ -262,6 +262,20 @@ def test_route_weight_quantize_plain(rows, cols, floor):
     assert _weighted_check(dy, tok, wt, floor=floor) == m.MXFP8_OK
 
 
+def test_route_weight_quantize_16_byte_aligned():
+    """dY rows 16 bytes apart from a 32-byte boundary (row stride cols + 8:
+    the 16-byte load path)."""
+    rng = np.random.default_rng(31)
+    tokens, cols, rows = 50, 224, 300
+    dyb = oracle.bf16_round(rng.standard_normal((tokens, cols)))
+    wide = np.zeros((tokens, cols + 8), np.uint16)
+    wide[:, :cols] = dyb
+    dy = to_dev_bf16(wide)[:, :cols]
+    tok = rng.integers(0, tokens, rows).astype(np.int32)
+    wt = rng.uniform(0, 1, rows).astype(np.float32)
+    assert _weighted_check(dy, tok, wt) == m.MXFP8_OK
+
+
 def test_route_weight_quantize_extremes():
     """Exact-product ties, products below fp32's normal range (the double
     branch), overflow to Inf, zero weights, and an out-of-range token index
