@@ -18,6 +18,8 @@ GEMM_CASES = [(int(_rng.integers(1, 700)), int(_rng.integers(1, 90)) * 8, int(_r
               for _ in range(24)]
 QUANT_CASES = [(int(_rng.integers(1, 40)) * 32, int(_rng.integers(1, 60)) * 32) for _ in range(16)]
 GROUP_CASES = [[int(c) for c in _rng.integers(0, 400, int(_rng.integers(1, 9)))] for _ in range(8)]
+TENSOR_CASES = [(int(_rng.integers(1, 600)), int(_rng.integers(1, 70)) * 8, int(_rng.integers(1, 40)) * 16,
+                 int(_rng.integers(0, 2)), int(_rng.integers(0, 2))) for _ in range(12)]
 
 
 def _bits(shape, seed, scale=1.0):
@@ -75,3 +77,17 @@ def test_grouped_gemm_random_groups(counts):
         ref = oracle.gemm_mx(xa["q_row"], xa["s_row"], rw["q_row"][g * N:(g + 1) * N],
                              oracle.quantize_mx(w[g * N:(g + 1) * N], oracle.ROWWISE)["s_row"])
         gemm_tolerance_check(c[lo:hi], ref, f"group {g} of {counts}")
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb", TENSOR_CASES)
+def test_tensor_gemm_random_shapes(M, N, K, fa, fb):
+    a, b = _bits((M, K), M + 5 * K), _bits((N, K), N + 7 * K)
+    qa, _, sa = m.fp8_quantize_tensor(to_dev_bf16(a).reshape(-1), fa)
+    qb, _, sb = m.fp8_quantize_tensor(to_dev_bf16(b).reshape(-1), fb)
+    c = m.fp8_scaled_gemm(m.GEMM_TENSOR, qa.view(M, K), sa, qb.view(N, K), sb, a_fmt=fa, b_fmt=fb)
+    assert_ok()
+    wa, wsa, wqa = oracle.quantize_tensor(a.reshape(-1), fa)
+    wb, wsb, wqb = oracle.quantize_tensor(b.reshape(-1), fb)
+    assert np.array_equal(host(qa), wqa.reshape(-1)) and np.array_equal(host(qb), wqb.reshape(-1))
+    ref = oracle.gemm_tensor(wqa.reshape(M, K), fa, wsa, wqb.reshape(N, K), fb, wsb)
+    gemm_tolerance_check(c, ref, f"tensor gemm {M}x{N}x{K} fmts {fa}{fb}")
