@@ -1,8 +1,9 @@
 """Sizes past 2^31 elements or bytes, where any 32-bit index in a kernel
 would wrap: the MX quantizer (both orientations) on a 65600 x 32768 BF16
 tensor (2.15 G values), MX GEMMs whose A, B or C each hold more than 2^31
-bytes, the per-tensor quantizer over 2.15 G values and a grouped GEMM over
-65600 x 32768 expert rows.  The outputs are too large for the oracle, so
+bytes, the per-tensor quantizer over 2.15 G values, a grouped GEMM over
+65600 x 32768 expert rows, and the routed conversions (dequantize, SwiGLU +
+quantize, route weighting + quantize) reading or writing past 2^31 values.  The outputs are too large for the oracle, so
 sampled row tiles, rows and columns (the first, one in the middle and the
 ragged last ones, where a wrapped index would land) are checked against it:
 the MX rule is local to a 32-value block, so the oracle quantizing a sampled
@@ -15,6 +16,7 @@ import torch
 import mxfp8_precision_gemms_gb300 as m
 import oracle
 from gpu_util import assert_ok, device, gemm_tolerance_check, host
+from mx_check import bf16_candidates, check_set_quantization
 
 pytestmark = pytest.mark.gpu
 
@@ -141,3 +143,54 @@ def test_grouped_gemm_past_2g_bytes(big_x):
         ref = oracle.gemm_mx(rx["q_row"], rx["s_row"], rw["q_row"], rw["s_row"])
         gemm_tolerance_check(c[torch.tensor(rows, device=device())], ref, f"expert {g}")
     del c, qa, sa, qw, w
+
+
+def _row_tiles(rows):
+    last = (rows + 127) // 128 - 1
+    return [(rt, rt * 128, min(rows, rt * 128 + 128)) for rt in (0, last // 2, last)]
+
+
+def test_dequantize_past_2g_values(big_x):
+    qx = m.fp8_quantize_mx(big_x, m.MX_ROWWISE)
+    out = m.fp8_dequantize_mx(qx["q_row"], qx["s_row"])
+    assert_ok()
+    for rt, r0, r1 in _row_tiles(ROWS):
+        want = oracle.quantize_mx(_bits(big_x[r0:r1]), oracle.ROWWISE)
+        assert np.array_equal(_bits(out[r0:r1]), oracle.dequantize_mx(want["q_row"], want["s_row"])), rt
+    del qx, out
+
+
+def test_swiglu_quantize_past_2g_values(big_x):
+    """h = the 65600 x 32768 tensor as gate | up (f = 16384): input offsets
+    past 2^31 values."""
+    f = K // 2
+    q, s = m.fp8_swiglu_quantize_mx(big_x)
+    assert_ok()
+    nkc = f // 128
+    sh = host(s)
+    for rt, r0, r1 in _row_tiles(ROWS):
+        c, lo, hi = bf16_candidates(oracle.swiglu(_bits(big_x[r0:r1])))
+        want = oracle.quantize_mx(c, oracle.ROWWISE)
+        check_set_quantization(host(q[r0:r1]), sh[rt * nkc * 512:(rt + 1) * nkc * 512], lo, hi,
+                               want["q_row"], want["s_row"])
+    del q, s
+
+
+def test_route_weight_quantize_past_2g_values(big_x):
+    """dY = the 65600 x 32768 tensor; 65600 dispatched rows gather scattered
+    tokens with random fp32 weights."""
+    rows = ROWS
+    tok = torch.from_numpy((np.arange(rows, dtype=np.int64) * 7919 % ROWS).astype(np.int32)).to(device())
+    g = torch.Generator(device=device()).manual_seed(15)
+    wt = torch.rand(rows, generator=g, device=device(), dtype=torch.float32)
+    q, s = m.fp8_route_weight_quantize_mx(big_x, tok, wt)
+    assert_ok()
+    nkc = K // 128
+    sh = host(s)
+    for rt, r0, r1 in _row_tiles(rows):
+        gathered = _bits(big_x[tok[r0:r1].long()])
+        bits = oracle.route_weight(gathered, np.arange(r1 - r0, dtype=np.int32), host(wt[r0:r1]))
+        want = oracle.quantize_mx(bits, oracle.ROWWISE)
+        assert np.array_equal(host(q[r0:r1]), want["q_row"]), rt
+        assert np.array_equal(sh[rt * nkc * 512:(rt + 1) * nkc * 512], want["s_row"]), rt
+    del q, s
