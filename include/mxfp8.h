@@ -10,7 +10,13 @@
  *    memory owned and allocated by the caller.  The library allocates
  *    nothing, frees nothing and keeps no reference after the call returns.
  *  - Work is stream ordered on `stream` (NULL = the legacy default stream).
- *    Calls never synchronize, except mxfp8_last_device_status().
+ *    Calls never synchronize, except mxfp8_last_device_status().  A call
+ *    issues only kernel launches and memsets on `stream`, so a sequence of
+ *    calls can be captured into a CUDA graph and replayed; make each kind
+ *    of call once on the device before capturing it (its first use sets
+ *    kernel attributes and caches occupancy queries).  Calls on different
+ *    streams may run concurrently when they share no output buffer (and,
+ *    for the entry points that take one, no workspace or history state).
  *  - Errors the host can see (null pointers, bad shapes, misaligned pointers
  *    or strides) are returned at once and launch nothing.  Errors only the
  *    device can see (inconsistent group offsets, a wait that exceeded its
