@@ -48,6 +48,14 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Per-half max(|a|, |b|) of packed BF16 (sign: the XOR of the inputs' signs;
+// a NaN input gives the canonical NaN).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Largest BF16 magnitude bits among the 8 values of a 16-byte vector.
 __device__ __forceinline__ uint32_t amax8(const uint4& v) {
     uint32_t m = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
@@ -193,16 +201,20 @@ __device__ __forceinline__ bool aligned32(const void* p) {
 // MX quantization of one 32-value block held by one thread as 16 words of
 // packed BF16 (value 2i in the low half of w[i]).  Writes the 32 E4M3 bytes
 // to q_dst (skipped when null; 32-byte aligned when v8) and the E8M0 byte to
-// *s_dst.
+// *s_dst.  The block maximum is taken with the packed BF16 abs-max (one
+// instruction per pair of words): the magnitudes of non-NaN BF16 values order
+// like their bit patterns, so the masked result is the largest magnitude's
+// bits, and a NaN anywhere gives 0x7FFF, which e8m0_byte maps to the NaN
+// scale as it does any NaN or Inf bits.
 template <bool FLOOR>
 __device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, uint8_t* s_dst,
                                            bool v8) {
     uint32_t m8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = max_u16x2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+    for (int i = 0; i < 8; ++i) m8[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m8[i] = max_u16x2(m8[i], m8[i + 4]);
-    const uint32_t m2 = max_u16x2(max_u16x2(m8[0], m8[1]), max_u16x2(m8[2], m8[3]));
+    for (int i = 0; i < 4; ++i) m8[i] = absmax_bf16x2(m8[i], m8[i + 4]);
+    const uint32_t m2 = absmax_bf16x2(absmax_bf16x2(m8[0], m8[1]), absmax_bf16x2(m8[2], m8[3])) & 0x7FFF7FFFu;
     const uint32_t byte = e8m0_byte(max(m2 & 0xFFFFu, m2 >> 16), FLOOR);
     uint32_t q[8];
     if (byte == 0xFFu) {
