@@ -45,6 +45,24 @@ def test_mx_gemm_matches_oracle(M, N, K):
     gemm_tolerance_check(c, ref, f"MX {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("K", [128, 256])
+def test_mx_gemm_short_last_wave(K):
+    """4096 x 4032: 256 tiles leave 28 for the last wave of 76 CTA pairs,
+    which run as 56 half tiles of 128 columns (the last tile's second half
+    holds 64 valid columns); K = 128 takes the per-slot copies, K = 256 the
+    slot-pair copies.  Every element against the oracle."""
+    M, N = 4096, 4032
+    a = workloads.bits(workloads.student_t((M, K), 4, 3, 0))
+    b = workloads.bits(workloads.normal((N, K), 0.02, 3, 1))
+    ga, wa = quantize_both(a)
+    gb, wb = quantize_both(b)
+    c = filled((M, N), 0x7FC0, torch.int16).view(torch.bfloat16)
+    m.fp8_scaled_gemm(m.GEMM_MX, ga["q_row"], ga["s_row"], gb["q_row"], gb["s_row"], c=c)
+    assert_ok()
+    ref = oracle.gemm_mx(wa["q_row"], wa["s_row"], wb["q_row"], wb["s_row"])
+    gemm_tolerance_check(c, ref, f"short last wave K={K}")
+
+
 def test_mx_gemm_ldc_and_untouched_padding():
     M, N, K, ldc = 192, 264, 256, 280
     a = workloads.bits(workloads.normal((M, K), 1.0, 2, 0))
