@@ -657,7 +657,7 @@ def sample_check(m, x, w, ref):
 
 def cpu_baseline(m, seed=0, budget_s=15.0):
     import oracle
-    X, W = oracle_inputs(seed, 8192, 2048)
+    X, W = oracle_inputs(seed, 8192, 8192)   # room to grow the sample to ~10 s
     m_rows, n_rows = 64, 256
     keep = {}
     while True:
