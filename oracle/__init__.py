@@ -71,6 +71,7 @@ def _load():
                 "orc_requantize_tensor": (None, [P, I64, I, ctypes.c_float, ctypes.c_float, I, P, P]),
                 "orc_dequantize_mx_grouped": (None, [P, P, P, I32, I64, P, I64]),
                 "orc_swiglu": (None, [P, I64, I64, I64, P]),
+                "orc_swiglu_bf16": (None, [P, I64, I64, I64, P]),
                 "orc_route_weight": (None, [P, I64, I64, P, P, I64, I64, P]),
             }
             for name, (res, args) in sig.items():
@@ -198,6 +199,23 @@ def swiglu(h, f: int | None = None) -> np.ndarray:
     f = width // 2 if f is None else f
     out = np.zeros((rows, f), np.float64)
     _load().orc_swiglu(_p(h), rows, f, width, _p(out))
+    return out
+
+
+def swiglu_bf16(h, f: int | None = None) -> np.ndarray:
+    """BF16 bits of g * sigma(g) * u correctly rounded (never a tie: the exact
+    value is irrational), h as in swiglu.  Raises if FP64 could not decide the
+    rounding side of some value (never observed)."""
+    h = np.ascontiguousarray(h, np.uint16)
+    rows, width = h.shape
+    f = width // 2 if f is None else f
+    out = np.zeros((rows, f), np.uint16)
+    lib = _load()
+    before = ctypes.c_int64.in_dll(lib, "orc_swiglu_undecided").value
+    lib.orc_swiglu_bf16(_p(h), rows, f, width, _p(out))
+    after = ctypes.c_int64.in_dll(lib, "orc_swiglu_undecided").value
+    if after != before:
+        raise ArithmeticError(f"{after - before} SwiGLU values undecided in FP64")
     return out
 
 

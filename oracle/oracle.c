@@ -383,6 +383,87 @@ void orc_swiglu(const uint16_t* h, int64_t rows, int64_t f, int64_t ld, double* 
     }
 }
 
+/* Running count of SwiGLU values whose rounding side could not be decided in
+ * FP64 (never observed; the Python wrapper raises when it grows). */
+int64_t orc_swiglu_undecided = 0;
+
+/* The correctly rounded BF16 value of y = g sigma(g) u ([OLMO] Section
+ * 11.4.1; the hidden value an unfused SwiGLU stores in BF16).
+ *
+ * For a finite g != 0 and u != 0, e^-g is transcendental (g is rational;
+ * Lindemann-Weierstrass), so y is irrational and never equals a BF16 rounding
+ * midpoint: round-to-nearest never meets a tie.  The FP64 value v of
+ * orc_swiglu lies within a few 2^-53 |y| of y, so wherever v is farther than
+ * 2^-44 |v| from every midpoint, bf16_RNE(v) is the rounding of y.  Next to a
+ * midpoint m the side of |y| against m is decided from forms without the
+ * cancellation of |p| sigma(g) - m (p = g u, exact in FP64):
+ *   g > 0:  |y| = |p| / (1 + e^-g),    |y| > m  <=>  (|p| - m) - m e^-g > 0,
+ *           where |p| - m is exact (m lies within a factor of 2 of |p|) and
+ *           |p| == m puts |y| below m whatever the size of e^-g > 0;
+ *   g < 0:  |y| = |p| e^g / (1 + e^g), |y| > m  <=>  e^g (|p| - m) - m > 0.
+ * A form whose value lies within 2^-48 of the magnitude of its terms counts
+ * as undecided (the result then falls back to bf16_RNE(v)). */
+static uint16_t swiglu_bf16_one(double g, double u, int64_t* undecided) {
+    double v;
+    if (g >= 0.0) {
+        v = g * (1.0 / (1.0 + exp(-g))) * u;
+    } else {
+        double e = exp(g);
+        v = g * (e / (1.0 + e)) * u;
+    }
+    if (!isfinite(v) || v == 0.0) return orc_bf16_round(v);
+    double a = fabs(v);
+    /* consecutive BF16 magnitudes below <= a < above (2^128 past the largest) */
+    int lo = 0, hi = 0x7F80;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (orc_bf16_decode((uint16_t)mid) <= a) lo = mid; else hi = mid;
+    }
+    double below = orc_bf16_decode((uint16_t)lo);
+    double above = lo == 0x7F7F ? ldexp(1.0, 128) : orc_bf16_decode((uint16_t)(lo + 1));
+    double m = 0.5 * (below + above); /* exact: both are multiples of 2^-133 */
+    if (fabs(a - m) > ldexp(a, -44)) return orc_bf16_round(v);
+    double ap = fabs(g * u);
+    int up;
+    if (g > 0.0) {
+        double d = ap - m;
+        if (d == 0.0) {
+            up = 0;
+        } else {
+            double mt = m * exp(-g);
+            double z = d - mt;
+            if (fabs(z) <= ldexp(mt, -48)) {
+                ++*undecided;
+                return orc_bf16_round(v);
+            }
+            up = z > 0.0;
+        }
+    } else {
+        double t = exp(g);
+        double z = t * (ap - m) - m;
+        if (fabs(z) <= ldexp(m, -48)) {
+            ++*undecided;
+            return orc_bf16_round(v);
+        }
+        up = z > 0.0;
+    }
+    return (uint16_t)((signbit(v) ? 0x8000 : 0) | (up ? lo + 1 : lo));
+}
+
+/* orc_swiglu rounded to BF16 bits with swiglu_bf16_one; out is rows x f. */
+void orc_swiglu_bf16(const uint16_t* h, int64_t rows, int64_t f, int64_t ld, uint16_t* out) {
+    int64_t undecided = 0;
+#pragma omp parallel for schedule(static) reduction(+ : undecided)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < f; ++c) {
+            double g = orc_bf16_decode(h[r * ld + c]);
+            double u = orc_bf16_decode(h[r * ld + f + c]);
+            out[r * f + c] = swiglu_bf16_one(g, u, &undecided);
+        }
+    }
+    orc_swiglu_undecided += undecided;
+}
+
 /* Route-weighted gradient rows of combine backward ([OLMO] Section 11.4.1):
  * row i = bf16_RNE(w_i * dy[tok_i]); the product of a BF16 value and an fp32
  * weight is exact in FP64, so this is one rounding of the exact product.

@@ -808,3 +808,115 @@ def test_requantize_vs_torch(fmt_in, fmt_out):
         same, _ = oracle.requantize_tensor(codes, fmt_in, 5.0, 5.0, fmt_out)
         finite = ~torch.isnan(g).numpy() & ~torch.isinf(g).numpy()
         assert np.array_equal(same[finite], codes[finite])
+
+
+# ------------------------------------------- SwiGLU, correctly rounded --
+
+def _mp_swiglu_bf16(gbits, ubits, table, digits=90):
+    """BF16 RNE of g sigma(g) u from a 90-digit mpmath evaluation (exact
+    rational rounding of the high-precision value)."""
+    mpmath = pytest.importorskip("mpmath")
+    out = []
+    with mpmath.workdps(digits):
+        for gb, ub in zip(gbits, ubits):
+            g = Fraction(float(oracle.bf16_decode(np.array([gb], np.uint16))[0]))
+            u = Fraction(float(oracle.bf16_decode(np.array([ub], np.uint16))[0]))
+            gm = mpmath.mpf(g.numerator) / g.denominator
+            um = mpmath.mpf(u.numerator) / u.denominator
+            y = gm * um / (1 + mpmath.exp(-gm))
+            man, exp = mpmath.mpf(y).man_exp if y != 0 else (0, 0)  # |mantissa|
+            yf = Fraction(int(man)) * (Fraction(2) ** int(exp)) if y != 0 else Fraction(0)
+            yf = -yf if y < 0 else yf
+            b = _correctly_rounded_bf16(yf, table)
+            if yf == 0:
+                b = 0x8000 if (g < 0) != (u < 0) else 0x0000
+            out.append(b)
+    return np.array(out, np.uint16)
+
+
+def _near_midpoint_pairs(n, rel, seed):
+    """(g, u) BF16 pairs whose FP64 SwiGLU value lies within rel of a BF16
+    rounding midpoint: the values a fast fp32 evaluation cannot round."""
+    rng = np.random.default_rng(seed)
+    found_g, found_u = [], []
+    while len(found_g) < n:
+        g = oracle.bf16_round(rng.standard_normal(1 << 20) * np.exp(rng.uniform(-3, 3, 1 << 20)))
+        u = oracle.bf16_round(rng.standard_normal(1 << 20) * np.exp(rng.uniform(-20, 20, 1 << 20)))
+        y = oracle.swiglu(np.stack([g, u], axis=1))[:, 0]
+        a = np.abs(y)
+        # the midpoint next to a: a's BF16 truncation plus half its unit
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+        unit = np.ldexp(1.0, (e - 7).astype(int))
+        mid = np.floor(a / unit) * unit + unit / 2
+        hit = (a > 2.0 ** -120) & (np.abs(a - mid) <= rel * a)
+        found_g += list(g[hit])
+        found_u += list(u[hit])
+    return np.array(found_g[:n], np.uint16), np.array(found_u[:n], np.uint16)
+
+
+def test_swiglu_bf16_vs_mpmath_random():
+    """Correctly rounded SwiGLU against a 90-digit evaluation on random gates
+    and ups spanning many binades (both signs, tiny and huge values)."""
+    rng = np.random.default_rng(41)
+    n = 3000
+    g = oracle.bf16_round(rng.standard_normal(n) * np.exp(rng.uniform(-12, 5, n)))
+    u = oracle.bf16_round(rng.standard_normal(n) * np.exp(rng.uniform(-60, 60, n)))
+    g[:40] = oracle.bf16_round(-rng.uniform(60, 90, 40))  # e^g near fp32's normal limit
+    got = oracle.swiglu_bf16(np.stack([g, u], axis=1))[:, 0]
+    want = _mp_swiglu_bf16(g, u, _bf16_neighbours_table())
+    assert np.array_equal(got, want), np.nonzero(got != want)[0][:8]
+
+
+def test_swiglu_bf16_vs_mpmath_near_midpoints():
+    """Values within 2^-24 of a BF16 rounding midpoint (where fp32 cannot
+    tell the side): every one rounded as the 90-digit value says."""
+    g, u = _near_midpoint_pairs(120, 2.0 ** -24, 42)
+    got = oracle.swiglu_bf16(np.stack([g, u], axis=1))[:, 0]
+    want = _mp_swiglu_bf16(g, u, _bf16_neighbours_table())
+    assert np.array_equal(got, want), np.nonzero(got != want)[0][:8]
+    # the plain FP64 rounding differs exactly where sigma(g) rounds to 1 in
+    # FP64 (gates past ~37) and g u is itself a midpoint: it ties to even there
+    h = np.stack([g, u], axis=1)
+    plain = oracle.bf16_round(oracle.swiglu(h)[:, 0])
+    d = plain != want
+    gd, ud = oracle.bf16_decode(g), oracle.bf16_decode(u)
+    assert np.all(gd[d] > 36) and np.all(oracle.swiglu(h)[d, 0] == gd[d] * ud[d])
+
+
+def test_swiglu_bf16_saturated_gate_on_a_midpoint():
+    """g u exactly a BF16 midpoint with a large positive gate: y = g u (1 -
+    e^-g + ...) lies just below |g u| however small e^-g is, so it rounds
+    toward zero; an FP64 evaluation lands on the midpoint itself and would
+    take the even neighbour.  321 = 3 * 107, 259 = 7 * 37 and 265 = 5 * 53
+    are odd 9-bit integers: (2k + 1) 2^e halves BF16 units."""
+    cases = [(3.0 * 16, 107 / 128), (3.0 * 2 ** 20, -107 * 2.0 ** -30),
+             (7.0 * 8, 37 / 64), (5.0 * 2 ** 100, 53 * 2.0 ** -120),
+             (3.0 * 2 ** 120, -107.0 * 2 ** -10), (7.0 * 2 ** 60, 37.0 * 2 ** -90),
+             (5.0 * 16, -53.0 * 2 ** 10)]
+    g = oracle.bf16_round(np.array([c[0] for c in cases]))
+    u = oracle.bf16_round(np.array([c[1] for c in cases]))
+    assert np.array_equal(oracle.bf16_decode(g) * 1.0, [c[0] for c in cases])
+    assert np.array_equal(oracle.bf16_decode(u) * 1.0, [c[1] for c in cases])
+    p = oracle.bf16_decode(g) * oracle.bf16_decode(u)
+    got = oracle.swiglu_bf16(np.stack([g, u], axis=1))[:, 0]
+    for pv, b in zip(p, got):
+        a = abs(pv)
+        e = math.floor(math.log2(a))
+        unit = 2.0 ** (e - 7)
+        assert (a / unit) % 1 == 0.5  # a midpoint
+        below = math.floor(a / unit) * unit
+        assert float(oracle.bf16_decode(np.array([b], np.uint16))[0]) == math.copysign(below, pv)
+    # the plain FP64 rounding ties to even instead, which differs for some
+    plain = oracle.bf16_round(oracle.swiglu(np.stack([g, u], axis=1))[:, 0])
+    assert (plain != got).any()
+    # for gates small enough, a 90-digit evaluation agrees
+    small = np.abs(oracle.bf16_decode(g)) < 100
+    want = _mp_swiglu_bf16(g[small], u[small], _bf16_neighbours_table())
+    assert np.array_equal(got[small], want)
+
+
+def test_swiglu_bf16_equals_fp64_rounding_away_from_midpoints():
+    rng = np.random.default_rng(43)
+    h = oracle.bf16_round(rng.standard_normal((256, 512)) * 3)
+    y = oracle.swiglu(h)
+    assert np.array_equal(oracle.swiglu_bf16(h), oracle.bf16_round(y))
