@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxfp8.so")
 SOURCES = ["api.cu", "quantize.cu", "fused.cu", "gemm.cu"]
-HEADERS = ["ptx.cuh", "mx_common.cuh", "internal.h"]
+HEADERS = ["ptx.cuh", "mx_common.cuh", "internal.h", "swiglu_round.cuh", "ff_consts.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -20,6 +20,7 @@
 
 #include "internal.h"
 #include "mx_common.cuh"
+#include "swiglu_round.cuh"
 
 namespace mxfp8 {
 
@@ -146,13 +147,14 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 // product's exact residual (one FMA: Dekker's error-free product) plus
 // -a * (log2(e) - L2E), the constant's own residual (the two-constant
 // argument split of Cody and Waite), so e^-a = 2^p * 2^d with 2^d = 1 + d ln2
-// to first order (|d| < 2^-17).  a is clamped at 128, where 2^p is already
-// below fp32's range and flushes to 0 (as it does from a ~ 87.3 on).
+// to first order (|d| < 2^-17).  2^p flushes to 0 from a ~ 87.3 on; past
+// a ~ 2.4e38 the product a L2E overflows and the result is NaN (the caller
+// redoes such blocks in FP64).
 __device__ __forceinline__ float exp_neg_abs(float g) {
     constexpr float kL2E = 1.44269502163f;       // RN(log2 e), 0x3FB8AA3B
     constexpr float kL2ELo = 1.92596303350e-08f;  // RN(log2 e - kL2E)
     constexpr float kLn2 = 0.693147182465f;       // RN(ln 2)
-    const float a = fminf(fabsf(g), 128.f);
+    const float a = fabsf(g);
     const float p = __fmul_rn(-a, kL2E);
     const float d = __fmaf_rn(-a, kL2ELo, __fmaf_rn(-a, kL2E, -p));
     float e;
@@ -174,8 +176,8 @@ __device__ __forceinline__ float exp_neg_abs(float g) {
 // which also covers BF16-subnormal gates; n u cannot overflow for g < 0).
 // The BF16 rounding of y is therefore the correctly rounded value unless the
 // exact value lies that close to a rounding midpoint, where it may be the
-// neighbour.  NaN propagates; g < -80 (e^g leaves fp32's normal range,
-// including -Inf) takes the exact path below.
+// neighbour.  NaN propagates (and |g| past ~2.4e38 gives NaN); g < -80 (e^g
+// leaves fp32's normal range, including -Inf) takes the exact path below.
 __device__ __forceinline__ float swiglu_fast(float g, float u) {
     const float t = exp_neg_abs(g);
     float r;
@@ -184,29 +186,86 @@ __device__ __forceinline__ float swiglu_fast(float g, float u) {
     return __fmul_rn(__fmul_rn(n, u), r);
 }
 
-// The same value formed in double and rounded once to BF16.
-__device__ __noinline__ uint32_t swiglu_bf16_exact(float g, float u) {
-    const double gd = g;
-    const double e = exp(gd < 0.0 ? gd : -gd);
-    const double sig = gd < 0.0 ? e / (1.0 + e) : 1.0 / (1.0 + e);
-    return bf16_bits_rn(gd * sig * static_cast<double>(u));
+// Magnitude of BF16 bits 0..0x7F80 as a double (0x7F80 taken as 2^128, the
+// value the rounding of the largest finite BF16 steps to).
+__device__ __forceinline__ double bf16_mag(uint32_t b) {
+    return b >= 0x7F80u ? 0x1p128 : static_cast<double>(__uint_as_float(b << 16));
 }
 
-// All 8 values of a chunk with a gate off the fast path, in double.
-__device__ __noinline__ uint4 swiglu8_exact(uint4 g8, uint4 u8) {
-    uint4 v;
-    uint32_t* vv = reinterpret_cast<uint32_t*>(&v);
-    const uint32_t* gg = reinterpret_cast<const uint32_t*>(&g8);
-    const uint32_t* uu = reinterpret_cast<const uint32_t*>(&u8);
-    for (int i = 0; i < 4; ++i) {
-        vv[i] = swiglu_bf16_exact(bf16_lo(gg[i]), bf16_lo(uu[i])) |
-                (swiglu_bf16_exact(bf16_hi(gg[i]), bf16_hi(uu[i])) << 16);
+// The correctly rounded BF16 value of g sigma(g) u evaluated in FP64 (the
+// path for gates below -80, blocks holding Inf or NaN, and the few values the
+// float-float resolver leaves undecided).  The FP64 value v is within a few
+// 2^-53 of the exact one, so its rounding is the exact value's unless v lies
+// next to a BF16 midpoint m; there the side is taken from the cancellation-
+// free forms of swiglu_round.cuh ((|p| - m) - m t for g > 0, t (|p| - m) - m
+// for g < 0, p = g u, t = e^-|g|), with |p| == m and g > 0 below m, and for
+// |g| < 1 rewritten around |p| - 2m with expm1.
+__device__ __noinline__ uint32_t swiglu_bf16_exact(float gf, float uf) {
+    const double g = gf, u = uf, p = g * u;
+    const double t = exp(-fabs(g));
+    const double v = g >= 0.0 ? p / (1.0 + t) : p * t / (1.0 + t);
+    uint16_t b;
+    asm("cvt.rn.bf16.f64 %0, %1;" : "=h"(b) : "d"(v));
+    if (!isfinite(v) || v == 0.0) return b;
+    const double av = fabs(v);
+    const uint32_t bm = b & 0x7FFFu;
+    const uint32_t lo = bf16_mag(bm) > av ? bm - 1 : bm;  // BF16 magnitudes lo <= av < lo + 1
+    if (lo >= 0x7F80u) return b;                         // at or past 2^128: Inf
+    const double m = 0.5 * (bf16_mag(lo) + bf16_mag(lo + 1));
+    if (fabs(av - m) > av * 0x1p-44) return b;
+    const double ap = fabs(p);
+    bool up;
+    if (fabs(g) < 1.0) {
+        // near g = 0 (e^-|g| rounds to 1 below 2^-54) the same forms around
+        // |p| - 2m, which is exact here: the side of |p| == 2m is the sign of g
+        const double e = g > 0.0 ? -m * expm1(-g) : expm1(g) * (ap - m);
+        up = (ap - 2.0 * m) + e > 0.0;
+    } else if (g > 0.0) {
+        const double d = ap - m;
+        up = d != 0.0 && d - m * t > 0.0;
+    } else {
+        up = t * (ap - m) - m > 0.0;
     }
-    return v;
+    return (b & 0x8000u) | (up ? lo + 1 : lo);
 }
 
-__device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2) {
-    return bf16x2_rn(swiglu_fast(bf16_lo(g2), bf16_lo(u2)), swiglu_fast(bf16_hi(g2), bf16_hi(u2)));
+// BF16 bits of one fast-path value next to a rounding midpoint: the
+// float-float resolver, or FP64 where it cannot decide.
+__device__ __noinline__ uint32_t swiglu_bf16_near(float g, float u, float y) {
+    bool undecided;
+    const uint32_t b = ff::swiglu_round_near(g, u, y, &undecided);
+    return undecided ? swiglu_bf16_exact(g, u) : b;
+}
+
+// Near-midpoint test.  The fast value y is within 8.5 fp32 units of the
+// exact one (7.5 2^-24 relative is at most 7.5 units of y's binade, plus one
+// unit where fp32 underflows), so its BF16 rounding can be wrong only when
+// its low 16 bits lie within 8 of 0x8000 (the midpoint pattern).  The test
+// takes a window of kNearHalf = 10: low16 + 0x8000 + 10 (mod 2^16) <= 20.
+constexpr uint32_t kNearHalf = 10;
+constexpr uint32_t kNearOffset = (0x8000u + kNearHalf) * 0x10001u;
+
+__device__ __forceinline__ bool near_one(float y) {
+    return ((__float_as_uint(y) + 0x8000u + kNearHalf) & 0xFFFFu) <= 2 * kNearHalf;
+}
+
+// A running per-half minimum of the offset low halves of word pairs (see
+// swiglu2) holds a near-midpoint value.  In the high half the carry out of
+// the low half's addition can shift the window by one unit (to
+// [0x8000 - 11, 0x8000 + 9]), still wider than the 8 units needed.
+__device__ __forceinline__ bool near_any(uint32_t near) {
+    return min(near & 0xFFFFu, near >> 16) <= 2 * kNearHalf;
+}
+
+// Two fast-path values rounded to BF16; `near` takes the per-half minimum of
+// both values' low 16 bits (y0 in the low half) plus the window offset.
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2, uint32_t& near) {
+    const float y0 = swiglu_fast(bf16_lo(g2), bf16_lo(u2));
+    const float y1 = swiglu_fast(bf16_hi(g2), bf16_hi(u2));
+    uint32_t w;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(__float_as_uint(y0)), "r"(__float_as_uint(y1)));
+    near = min_u16x2(near, w + kNearOffset);
+    return bf16x2_rn(y0, y1);
 }
 
 // Column tiles per CTA of the fused row producers: the tile-row lookup (and,
@@ -222,12 +281,77 @@ __device__ __forceinline__ bool swiglu_rare32(const uint32_t* g) {
     return max(t & 0xFFFFu, t >> 16) > 0xC2A0u;
 }
 
+__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+    return v;
+}
+
+// E4M3 code of the BF16 value b (bits) under the block scale byte.
+__device__ __forceinline__ uint32_t e4m3_of(uint32_t b, uint32_t byte) {
+    if (byte == 0xFFu) return 0x7Fu;
+    return cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(b), inv_scale(byte)), 0.f) & 0xFFu;
+}
+
+// Warp pass over one 32-value block (tile row `row`, columns col..col+31),
+// one value per lane, read again from global memory, writing the block's
+// payload and scale over what its owner wrote.  `exact`: every value in FP64
+// (swiglu_bf16_exact).  Otherwise the fast values, where a value lies next to
+// a BF16 midpoint (near_one) its side is taken only where it matters: when
+// its upper candidate exceeds every settled value of the block (it may set
+// the scale), or when its two candidates quantize to different E4M3 codes
+// under the block's scale; any other near value quantizes the same either
+// way.  All 32 lanes call it with the same arguments.
+template <bool FLOOR>
+__device__ __forceinline__ void swiglu_block_redo(const uint16_t* __restrict__ h, int64_t ld,
+                                                  int64_t f, int64_t row, int64_t col, bool exact,
+                                                  uint8_t* __restrict__ q, uint8_t* s_dst) {
+    const int lane = threadIdx.x & 31;
+    const uint16_t* hp = h + row * ld + col + lane;
+    const float g = __uint_as_float(static_cast<uint32_t>(__ldg(hp)) << 16);
+    const float u = __uint_as_float(static_cast<uint32_t>(__ldg(hp + f)) << 16);
+    uint32_t b;
+    float y = 0.f;
+    bool near = false;
+    if (exact) {
+        b = swiglu_bf16_exact(g, u);
+    } else {
+        y = swiglu_fast(g, u);
+        b = bf16x2_rn(y, 0.f) & 0xFFFFu;
+        near = near_one(y);
+    }
+    // BF16 magnitude bits order like the magnitudes, Inf and NaN above all;
+    // `below` is the magnitude under the midpoint next to y
+    const uint32_t below = (__float_as_uint(y) >> 16) & 0x7FFFu;
+    uint32_t am = warp_max(near ? 0u : (b & 0x7FFFu));
+    const bool top = near && below + 1 > am;
+    if (__any_sync(0xFFFFFFFFu, top)) {
+        if (top) b = swiglu_bf16_near(g, u, y);
+        near = near && !top;
+        am = warp_max(near ? 0u : (b & 0x7FFFu));
+    }
+    const uint32_t byte = e8m0_byte(am, FLOOR);
+    uint32_t code = e4m3_of(b, byte);
+    if (near) {
+        const uint32_t lo = (b & 0x8000u) | below;
+        if (e4m3_of(lo, byte) != e4m3_of(lo + 1, byte)) code = e4m3_of(swiglu_bf16_near(g, u, y), byte);
+    }
+    q[row * f + col + lane] = static_cast<uint8_t>(code);
+    if (lane == 0) *s_dst = static_cast<uint8_t>(byte);
+}
+
 // One thread per 32-value output block (thread t of a 128 x 128 tile owns
 // block t & 3 of tile rows t/4 and t/4 + 64), several column tiles per CTA.
 // The two rows are loaded and converted one after the other, which keeps the
 // kernel at 64 registers: four CTAs (32 warps) per SM hide the load latency
 // better than two CTAs holding both rows in flight (129.7 against 146 us on
 // the 262144 x 512 routed workload).
+//
+// Exact rounding: every block is first quantized from its fast values; a
+// block holding a fast value next to a BF16 midpoint (about one in 80), a
+// gate below -80, or a maximum that is Inf or NaN (an input Inf or NaN, or
+// g u past fp32's range where the exact value may still be finite) is then
+// redone by its warp (swiglu_block_redo), in FP64 for the latter two.
 template <bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 4)
     swiglu_quant_kernel(const uint16_t* __restrict__ h, int64_t rows, int64_t f, int64_t ld,
@@ -256,19 +380,28 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) gw[k] = uw[k] = 0u;
             }
+            const bool rare = in && swiglu_rare32(gw);
             uint32_t v[16];
-            if (in && swiglu_rare32(gw)) {
+            uint32_t near = 0xFFFFFFFFu;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 e = swiglu8_exact(make_uint4(gw[4 * k], gw[4 * k + 1], gw[4 * k + 2], gw[4 * k + 3]),
-                                                  make_uint4(uw[4 * k], uw[4 * k + 1], uw[4 * k + 2], uw[4 * k + 3]));
-                    v[4 * k] = e.x; v[4 * k + 1] = e.y; v[4 * k + 2] = e.z; v[4 * k + 3] = e.w;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = swiglu2(gw[k], uw[k]);
+            for (int k = 0; k < 16; ++k) v[k] = swiglu2(gw[k], uw[k], near);
+            const uint32_t am = block32_amax_bits(v);
+            mx_block32_amax<FLOOR>(v, am, in ? q + row * f + col : nullptr, s_tile + swz_word(r) + j, v8);
+            // lanes out of range hold zeros: value 0, never near a midpoint
+            const bool exact = rare || (in && am >= 0x7F80u);
+            unsigned todo = __ballot_sync(0xFFFFFFFFu, exact || near_any(near));
+            if (todo) {
+                const unsigned ex = __ballot_sync(0xFFFFFFFFu, exact);
+                __syncwarp();  // the owners' stores above come first
+                do {
+                    const int src = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int stid = (tid & ~31) | src;
+                    const int rs = (stid >> 2) + 64 * i;
+                    swiglu_block_redo<FLOOR>(h, ld, f, row_begin + rs, ct * kTile + (stid & 3) * 32,
+                                             (ex >> src) & 1u, q, s_tile + swz_word(rs) + (stid & 3));
+                } while (todo);
             }
-            mx_block32<FLOOR>(v, in ? q + row * f + col : nullptr, s_tile + swz_word(r) + j, v8);
         }
     }
 }

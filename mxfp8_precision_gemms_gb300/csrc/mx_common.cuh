@@ -48,6 +48,13 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Per-half unsigned 16-bit minimum.
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Per-half max(|a|, |b|) of packed BF16 (sign: the XOR of the inputs' signs;
 // a NaN input gives the canonical NaN).
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
@@ -198,24 +205,30 @@ __device__ __forceinline__ bool aligned32(const void* p) {
     return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }
 
-// MX quantization of one 32-value block held by one thread as 16 words of
-// packed BF16 (value 2i in the low half of w[i]).  Writes the 32 E4M3 bytes
-// to q_dst (skipped when null; 32-byte aligned when v8) and the E8M0 byte to
-// *s_dst.  The block maximum is taken with the packed BF16 abs-max (one
-// instruction per pair of words): the magnitudes of non-NaN BF16 values order
-// like their bit patterns, so the masked result is the largest magnitude's
-// bits, and a NaN anywhere gives 0x7FFF, which e8m0_byte maps to the NaN
-// scale as it does any NaN or Inf bits.
-template <bool FLOOR>
-__device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, uint8_t* s_dst,
-                                           bool v8) {
+// Largest BF16 magnitude bits of a 32-value block held by one thread as 16
+// words of packed BF16, with the packed BF16 abs-max (one instruction per
+// pair of words): the magnitudes of non-NaN BF16 values order like their bit
+// patterns, so the masked result is the largest magnitude's bits, and a NaN
+// anywhere gives 0x7FFF, which e8m0_byte maps to the NaN scale as it does
+// any NaN or Inf bits.
+__device__ __forceinline__ uint32_t block32_amax_bits(const uint32_t* w) {
     uint32_t m8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) m8[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) m8[i] = absmax_bf16x2(m8[i], m8[i + 4]);
     const uint32_t m2 = absmax_bf16x2(absmax_bf16x2(m8[0], m8[1]), absmax_bf16x2(m8[2], m8[3])) & 0x7FFF7FFFu;
-    const uint32_t byte = e8m0_byte(max(m2 & 0xFFFFu, m2 >> 16), FLOOR);
+    return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// MX quantization of one 32-value block held by one thread as 16 words of
+// packed BF16 (value 2i in the low half of w[i]) whose largest magnitude's
+// bits are amax_bits (block32_amax_bits).  Writes the 32 E4M3 bytes to q_dst
+// (skipped when null; 32-byte aligned when v8) and the E8M0 byte to *s_dst.
+template <bool FLOOR>
+__device__ __forceinline__ void mx_block32_amax(const uint32_t* w, uint32_t amax_bits,
+                                                uint8_t* q_dst, uint8_t* s_dst, bool v8) {
+    const uint32_t byte = e8m0_byte(amax_bits, FLOOR);
     uint32_t q[8];
     if (byte == 0xFFu) {
 #pragma unroll
@@ -227,6 +240,13 @@ __device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, ui
     }
     if (q_dst != nullptr) st32(q_dst, q, v8);
     *s_dst = static_cast<uint8_t>(byte);
+}
+
+// The same with the block maximum taken here.
+template <bool FLOOR>
+__device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, uint8_t* s_dst,
+                                           bool v8) {
+    mx_block32_amax<FLOOR>(w, block32_amax_bits(w), q_dst, s_dst, v8);
 }
 
 // One rowwise step of a 128 x 128 tile: the half-warp holding tile row r

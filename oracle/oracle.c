@@ -400,9 +400,11 @@ int64_t orc_swiglu_undecided = 0;
  *   g > 0:  |y| = |p| / (1 + e^-g),    |y| > m  <=>  (|p| - m) - m e^-g > 0,
  *           where |p| - m is exact (m lies within a factor of 2 of |p|) and
  *           |p| == m puts |y| below m whatever the size of e^-g > 0;
- *   g < 0:  |y| = |p| e^g / (1 + e^g), |y| > m  <=>  e^g (|p| - m) - m > 0.
- * A form whose value lies within 2^-48 of the magnitude of its terms counts
- * as undecided (the result then falls back to bf16_RNE(v)). */
+ *   g < 0:  |y| = |p| e^g / (1 + e^g), |y| > m  <=>  e^g (|p| - m) - m > 0;
+ * for |g| < 1 the same forms are rewritten around |p| - 2m with expm1 (see
+ * below), since e^-|g| rounds to 1 in FP64 for |g| < 2^-54.  A form whose
+ * value lies within 2^-48 of the magnitude of its rounded term counts as
+ * undecided (the result then falls back to bf16_RNE(v)). */
 static uint16_t swiglu_bf16_one(double g, double u, int64_t* undecided) {
     double v;
     if (g >= 0.0) {
@@ -425,7 +427,19 @@ static uint16_t swiglu_bf16_one(double g, double u, int64_t* undecided) {
     if (fabs(a - m) > ldexp(a, -44)) return orc_bf16_round(v);
     double ap = fabs(g * u);
     int up;
-    if (g > 0.0) {
+    if (fabs(g) < 1.0) {
+        /* near g = 0, with t = 1 + expm1(-|g|) the forms become
+         *   g > 0:  (|p| - 2m) - m expm1(-g),   g < 0:  (|p| - 2m) + expm1(g) (|p| - m),
+         * |p| - 2m exact (m lies between |p| / 4 and |p|); so |p| == 2m puts |y|
+         * on the side of the sign of g however small g is */
+        double e = g > 0.0 ? -m * expm1(-g) : expm1(g) * (ap - m);
+        double z = (ap - 2.0 * m) + e;
+        if (fabs(z) <= ldexp(fabs(e), -48)) {
+            ++*undecided;
+            return orc_bf16_round(v);
+        }
+        up = z > 0.0;
+    } else if (g > 0.0) {
         double d = ap - m;
         if (d == 0.0) {
             up = 0;

@@ -1,8 +1,9 @@
 """GPU parity of the routed-path conversions around the quantizer:
-dequantization (bit-exact), fused SwiGLU + MX quantization (exact outside
-BF16 rounding near-ties, see mx_check) and fused route weighting + MX
-gradient quantization (bit-exact), plain and group-padded, on small ragged
-shapes and at the workloads' full sizes."""
+dequantization, fused SwiGLU + MX quantization (the correctly rounded BF16
+hidden value, including values next to a BF16 rounding midpoint) and fused
+route weighting + MX gradient quantization, plain and group-padded, on small
+ragged shapes and at the workloads' full sizes; every byte against the
+oracle."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +12,6 @@ import mxfp8_precision_gemms_gb300 as m
 import oracle
 import workloads
 from gpu_util import assert_ok, device, filled, host, to_dev_bf16, to_dev_u8
-from mx_check import bf16_candidates, check_set_quantization
 
 pytestmark = pytest.mark.gpu
 
@@ -110,19 +110,26 @@ def test_dequantize_full_size_mlp_up_activation():
 # ----------------------------------------------------- SwiGLU + quantize --
 
 def _swiglu_check(h_dev, offsets=None, floor=False):
+    """Every payload and scale byte of the fused SwiGLU + MX quantization
+    against the oracle's MX quantization of the correctly rounded BF16
+    hidden value."""
     flags = m.MX_SCALE_FLOOR if floor else 0
     off_d = None if offsets is None else torch.from_numpy(offsets).to(device())
     q, s = m.fp8_swiglu_quantize_mx(h_dev, offsets=off_d, flags=flags)
     assert_ok()
-    hb = workloads.bits(h_dev)
-    c, lo, hi = bf16_candidates(oracle.swiglu(hb))
+    y = oracle.swiglu_bf16(workloads.bits(h_dev))
     fl = oracle.SCALE_FLOOR if floor else 0
     if offsets is None:
-        want = oracle.quantize_mx(c, oracle.ROWWISE | fl)
+        want = oracle.quantize_mx(y, oracle.ROWWISE | fl)
         q_exp, s_exp = want["q_row"], want["s_row"]
     else:
-        q_exp, s_exp = oracle.quantize_mx_grouped(c, offsets, oracle.ROWWISE | fl)
-    return check_set_quantization(host(q), host(s), lo, hi, q_exp, s_exp, offsets, floor)
+        q_exp, s_exp = oracle.quantize_mx_grouped(y, offsets, oracle.ROWWISE | fl)
+    qh, sh = host(q), host(s)[: s_exp.size]
+    dq = np.argwhere(qh != q_exp)
+    assert dq.size == 0, f"{len(dq)} payload bytes differ, first at {dq[:4].tolist()}"
+    ds = np.nonzero(sh != s_exp)[0]
+    assert ds.size == 0, f"{ds.size} scale bytes differ, first at {ds[:4]}"
+    return y
 
 
 # documented bound of the fast path: 4.5 * 2^-24 with u = 1 (exhaustive over
@@ -152,13 +159,20 @@ def _swiglu_rel_err(gb, ub, bound):
 
 
 def test_swiglu_fast_path_error_every_gate():
-    """Every finite BF16 gate the fast path takes (g >= -80) with u = 1: the
+    """Every finite BF16 gate the fast path takes (g >= -80, |g| log2(e)
+    within fp32's range) with u = 1: the
     fp32 value the quantizer rounds to BF16 is within the documented bound of
     g sigma(g) computed in FP64 by the oracle; with random ups, within the
     general bound."""
     allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     g = oracle.bf16_decode(allb)
-    gb = allb[np.isfinite(g) & (g >= -80) & (g != 0)]
+    # past |g| log2(e) > fp32's largest value the fast path gives NaN (its
+    # blocks are redone in FP64)
+    huge = np.isfinite(g) & (np.abs(g) * np.log2(np.e) > float(np.finfo(np.float32).max) * (1 + 2.0 ** -20))
+    yh = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(allb[huge]), to_dev_bf16(np.full(int(huge.sum()), 0x3F80, np.uint16))))
+    assert huge.sum() > 0 and np.all(np.isnan(yh))
+    edge = np.abs(g) * np.log2(np.e) > float(np.finfo(np.float32).max) * (1 - 2.0 ** -20)
+    gb = allb[np.isfinite(g) & (g >= -80) & (g != 0) & ~edge]
     rel = _swiglu_rel_err(gb, np.full(gb.shape, 0x3F80, np.uint16), SWIGLU_BOUND_U1)
     assert rel <= SWIGLU_BOUND_U1, rel / 2.0 ** -24
     rng = np.random.default_rng(5)
@@ -168,16 +182,17 @@ def test_swiglu_fast_path_error_every_gate():
 
 
 def test_swiglu_fast_path_special_gates():
-    """+Inf and NaN gates propagate (the quantizer then marks the block),
-    gates past 87 (e^-g flushes to 0) give g u exactly, zero gates give 0."""
-    gb = np.array([0x7F80, 0x7FC0, 0x42B0, 0x4300, 0x7F7F, 0x0000, 0x8000], np.uint16)
-    ub = np.array([0x3F80] * 5 + [0x4000, 0x4000], np.uint16)
+    """NaN gates propagate; gates from 87 up to 2^127 (e^-g flushes to 0)
+    give g u exactly; +Inf and gates past ~2.4e38 give NaN in the fast path
+    (the quantizer redoes a block with a NaN or Inf maximum in FP64); zero
+    gates give 0."""
+    gb = np.array([0x7F80, 0x7FC0, 0x42B0, 0x4300, 0x7F00, 0x7F7F, 0x0000, 0x8000], np.uint16)
+    ub = np.array([0x3F80] * 6 + [0x4000, 0x4000], np.uint16)
     y = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(gb), to_dev_bf16(ub)))
-    assert np.isinf(y[0]) and y[0] > 0
-    assert np.isnan(y[1])
+    assert np.isnan(y[0]) and np.isnan(y[1]) and np.isnan(y[5])
     gd = oracle.bf16_decode(gb)
     assert y[2] == np.float32(gd[2]) and y[3] == np.float32(gd[3]) and y[4] == np.float32(gd[4])
-    assert y[5] == 0 and y[6] == 0
+    assert y[6] == 0 and y[7] == 0
 
 
 @pytest.mark.parametrize("rows,f", SHAPES)
@@ -200,6 +215,10 @@ def test_swiglu_quantize_extremes():
     u[9, :16] = -0.0
     g[10] = np.ldexp(rng.uniform(1, 2, f), rng.integers(-133, -100, f))
     g[11] = rng.uniform(60, 3000, f) * rng.choice([-1, 1], f)
+    g[12] = rng.uniform(2.4e38, 3.3e38, f)  # a |g| L2E past fp32: NaN in the fast path
+    u[12] = rng.standard_normal(f) * 2.0 ** -120
+    g[13, :4] = [np.inf, -np.inf, np.inf, 1.0]
+    u[13, :4] = [1.0, 1.0, 0.0, np.inf]
     h = oracle.bf16_round(np.concatenate([g, u], axis=1))
     _swiglu_check(to_dev_bf16(h))
 
@@ -224,10 +243,83 @@ def test_swiglu_quantize_16_byte_aligned():
 
 
 def test_swiglu_quantize_full_size():
-    """The grouped workload's up/gate output (262144 x 1024, 64 experts)."""
+    """The grouped workload's up/gate output (262144 x 1024, 64 experts):
+    every byte exact, and the workload holds values whose fast fp32 value
+    sits next to a BF16 midpoint (so the resolution runs)."""
     w = workloads.swiglu_hidden(seed=0, device=device())
-    amb = _swiglu_check(w["H"], offsets=w["offsets"])
-    assert amb < 0.05 * (w["H"].shape[0] * 512 // 32)  # near-ties are rare
+    _swiglu_check(w["H"], offsets=w["offsets"])
+    h = w["H"][:4096]
+    f = h.shape[1] // 2
+    y = host(m.mxfp8_debug_swiglu_f32(h[:, :f].contiguous().reshape(-1),
+                                      h[:, f:].contiguous().reshape(-1)))
+    low = y.view(np.uint32) & 0xFFFF
+    assert int((np.abs(low.astype(np.int64) - 0x8000) <= 8).sum()) > 100
+
+
+def _near_midpoint_pairs(n, seed, window=8):
+    """(gate, up) BF16 pairs whose fp32-rounded SwiGLU value has its low 16
+    bits within `window` of 0x8000: the fast path's own rounding of these
+    cannot be trusted (found with the oracle's FP64 SwiGLU)."""
+    rng = np.random.default_rng(seed)
+    gs, us = [], []
+    while sum(map(len, gs)) < n:
+        k = 1 << 20
+        g = oracle.bf16_round(rng.standard_normal(k) * np.exp(rng.uniform(-3, 2.5, k)))
+        u = oracle.bf16_round(rng.standard_normal(k) * np.exp(rng.uniform(-30, 30, k)))
+        y = oracle.swiglu(np.stack([g, u], axis=1))[:, 0].astype(np.float32)
+        low = (y.view(np.uint32) & 0xFFFF).astype(np.int64)
+        hit = (np.abs(low - 0x8000) <= window) & (np.abs(y) > 2.0 ** -70)
+        gs.append(g[hit])
+        us.append(u[hit])
+    return np.concatenate(gs)[:n], np.concatenate(us)[:n]
+
+
+def test_swiglu_quantize_near_midpoints():
+    """Blocks seeded with values next to a BF16 rounding midpoint: one per
+    block, several in one block, in neighbouring lanes of a warp, plus
+    saturated gates whose g u is itself a midpoint.  The fast path's own
+    BF16 rounding is wrong for some of them (checked through the fast-path
+    hook), the quantized bytes never are."""
+    g, u = _near_midpoint_pairs(1500, 51)
+    sat_g = oracle.bf16_round(np.array([48.0, 56.0, 80.0, 3 * 2.0 ** 20, 13.0, 40.0]))
+    sat_u = oracle.bf16_round(np.array([107 / 128, 37 / 64, -53 * 2.0 ** 10, -107 * 2.0 ** -30,
+                                        21.0 / 1024, 107 / 64]))
+    g = np.concatenate([g, sat_g])
+    u = np.concatenate([u, sat_u])
+    rows, f = 384, 256
+    rng = np.random.default_rng(52)
+    h = oracle.bf16_round(rng.standard_normal((rows, 2 * f)) * 2)
+    # positions: most blocks get one value, the first 64 rows get four per block
+    n = g.size
+    pos = rng.choice(rows * f, size=n, replace=False)
+    dense = (np.arange(64)[:, None] * f + np.arange(0, f, 8)[None, :]).reshape(-1)[: n // 4]
+    pos[: dense.size] = dense
+    pos = np.unique(pos)[:n]
+    r, c = pos // f, pos % f
+    h[r, c] = g[: pos.size]
+    h[r, f + c] = u[: pos.size]
+    y = _swiglu_check(to_dev_bf16(h))
+    fast = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(h[r, c]), to_dev_bf16(h[r, f + c])))
+    naive = oracle.bf16_round(fast.astype(np.float64))
+    assert int((naive != y[r, c]).sum()) > 20  # the fast rounding alone is wrong there
+
+
+def test_swiglu_quantize_product_past_fp32():
+    """Gates in (1, 6) with ups near the BF16 maximum: g u leaves fp32's
+    range while g sigma(g) u mostly stays finite (the block is redone in
+    FP64); larger gates give values past the range (Inf, NaN scale)."""
+    rng = np.random.default_rng(53)
+    rows, f = 128, 128
+    g = rng.uniform(1.01, 8.0, (rows, f))
+    u = rng.uniform(2.0 ** 126, 3.3e38, (rows, f)) * rng.choice([-1, 1], (rows, f))
+    g[::2] = rng.standard_normal((rows // 2, f))  # ordinary rows between them
+    u[::2] = rng.standard_normal((rows // 2, f))
+    h = oracle.bf16_round(np.concatenate([g, u], axis=1))
+    y = _swiglu_check(to_dev_bf16(h))
+    v = oracle.bf16_decode(y[1::2])
+    hv = oracle.bf16_decode(h[1::2])
+    past = np.abs(hv[:, :f] * hv[:, f:]) > float(np.finfo(np.float32).max)
+    assert (past & np.isfinite(v)).sum() > 100 and np.isinf(v).any()
 
 
 # ------------------------------------------- route weighting + quantize --

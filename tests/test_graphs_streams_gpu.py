@@ -172,6 +172,8 @@ def test_graph_replay_grouped_and_routed():
         wq, ws_ = oracle.quantize_mx_grouped(_bits(X), o)
         assert np.array_equal(host(qa), wq) and np.array_equal(host(sa)[:ws_.size], ws_)
         assert np.array_equal(_bits(back), oracle.dequantize_mx_grouped(wq, ws_, o))
+        hq, hs = oracle.quantize_mx_grouped(oracle.swiglu_bf16(_bits(H)), o)
+        assert np.array_equal(host(qh), hq) and np.array_equal(host(sh)[:hs.size], hs)
 
 
 def test_two_streams_run_independent_steps():

@@ -16,7 +16,6 @@ import torch
 import mxfp8_precision_gemms_gb300 as m
 import oracle
 from gpu_util import assert_ok, device, gemm_tolerance_check, host
-from mx_check import bf16_candidates, check_set_quantization
 
 pytestmark = pytest.mark.gpu
 
@@ -169,10 +168,9 @@ def test_swiglu_quantize_past_2g_values(big_x):
     nkc = f // 128
     sh = host(s)
     for rt, r0, r1 in _row_tiles(ROWS):
-        c, lo, hi = bf16_candidates(oracle.swiglu(_bits(big_x[r0:r1])))
-        want = oracle.quantize_mx(c, oracle.ROWWISE)
-        check_set_quantization(host(q[r0:r1]), sh[rt * nkc * 512:(rt + 1) * nkc * 512], lo, hi,
-                               want["q_row"], want["s_row"])
+        want = oracle.quantize_mx(oracle.swiglu_bf16(_bits(big_x[r0:r1])), oracle.ROWWISE)
+        assert np.array_equal(host(q[r0:r1]), want["q_row"]), rt
+        assert np.array_equal(sh[rt * nkc * 512:(rt + 1) * nkc * 512], want["s_row"]), rt
     del q, s
 
 

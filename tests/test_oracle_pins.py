@@ -920,3 +920,30 @@ def test_swiglu_bf16_equals_fp64_rounding_away_from_midpoints():
     h = oracle.bf16_round(rng.standard_normal((256, 512)) * 3)
     y = oracle.swiglu(h)
     assert np.array_equal(oracle.swiglu_bf16(h), oracle.bf16_round(y))
+
+
+def test_swiglu_bf16_tiny_gate_half_product_on_a_midpoint():
+    """|g| below 2^-54 with g u / 2 exactly a BF16 midpoint: sigma(g) = 1/2 +
+    g/4 + ..., so |y| lies above the midpoint for g > 0 and below it for
+    g < 0; in FP64 sigma(g) rounds to 1/2 exactly.  Gates near 1e-10 checked
+    against the 90-digit evaluation too."""
+    cases = [(7 * 2.0 ** -110, 37 * 2.0 ** 90), (-7 * 2.0 ** -110, 37 * 2.0 ** 90),
+             (3 * 2.0 ** -120, 107 * 2.0 ** 100), (-3 * 2.0 ** -120, -107 * 2.0 ** 100),
+             (5 * 2.0 ** -125, 53 * 2.0 ** 110), (-3 * 2.0 ** -60, 107.0)]
+    g = oracle.bf16_round(np.array([c[0] for c in cases]))
+    u = oracle.bf16_round(np.array([c[1] for c in cases]))
+    gd, ud = oracle.bf16_decode(g), oracle.bf16_decode(u)
+    assert np.array_equal(gd, [c[0] for c in cases]) and np.array_equal(ud, [c[1] for c in cases])
+    got = oracle.swiglu_bf16(np.stack([g, u], axis=1))[:, 0]
+    for gv, pv, b in zip(gd, gd * ud, got):
+        m = abs(pv) / 2
+        e = math.floor(math.log2(m))
+        unit = 2.0 ** (e - 7)
+        assert (m / unit) % 1 == 0.5  # the half product is a midpoint
+        want = (math.floor(m / unit) + (1 if gv > 0 else 0)) * unit
+        assert float(oracle.bf16_decode(np.array([b], np.uint16))[0]) == math.copysign(want, pv)
+    rng = np.random.default_rng(44)
+    gs = oracle.bf16_round(rng.standard_normal(400) * 1e-10)
+    us = oracle.bf16_round(rng.standard_normal(400) * 1e20)
+    want = _mp_swiglu_bf16(gs, us, _bf16_neighbours_table())
+    assert np.array_equal(oracle.swiglu_bf16(np.stack([gs, us], axis=1))[:, 0], want)
