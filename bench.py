@@ -8,7 +8,9 @@ rowwise + MX GEMM to BF16, weights re-quantized every step (no cache).
 
 Also reported on the same line:
   roofline        the GEMM kernel against the FP8 tensor peak (CUDA events
-                  on the launching stream, averaged over the timed steps)
+                  on the launching stream, averaged over the timed steps):
+                  the measured BF16 rate x 2, burst for a timed region
+                  under 2 s, sustained beyond; also launch time x SM clock
   quantize        the MX quantizer kernel against measured HBM bandwidth
   hot_path_rows   the other rows of the path, each on its own workload:
                   per-tensor FP8 4096^3, MXFP8 backward (dgrad + wgrad with
@@ -16,7 +18,9 @@ Also reported on the same line:
   e2e             the same metric with host-resident inputs: H2D of X and W
                   from pinned memory and D2H of C inside the timed region
   cpu_baseline    the FP64 CPU oracle on a bounded sample of the workload
-  clocks          nvidia-smi samples taken during the timed region
+  clocks          nvidia-smi samples over the timed region and the same
+                  step run untimed after it, 1 s of load in all (a short
+                  timed region holds few of the 200 ms samples)
 
 `--impl reference` times the CPU oracle instead (the reference arm).
 Under torchrun each rank runs an independent replica (no collective on the
@@ -45,6 +49,8 @@ import torch  # noqa: E402
 METRIC = "MXFP8 GEMM TFLOP/s incl. quantize (vs 4500 FP8 peak); quantize GB/s vs HBM"
 UNIT = "TFLOP/s"
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+SUSTAINED_AFTER_S = 2.0  # timed regions at least this long take the sustained BF16 peak
+CLOCK_WINDOW_S = 1.0     # loaded span over which nvidia-smi clocks are summarised
 SWIGLU_Q_BYTES = 4 + 1 + 1 / 32     # read gate and up (BF16), write E4M3 + scale per output
 MX_ROW_BYTES = 2 + 1 + 1 / 32  # algorithmic bytes per value: read BF16, write E4M3 + E8M0/32
 MX_BOTH_BYTES = 2 + 2 * (1 + 1 / 32)
@@ -107,9 +113,12 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.samples.append(parts)
+                self.samples.append((time.monotonic(), parts))
 
-    def stop(self):
+    def stop(self, window=None, timed=None):
+        """Summary of the samples taken inside `window` (host monotonic
+        seconds, the loaded span), with the count inside `timed` (the timed
+        region)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -118,16 +127,21 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm = [float(s[0]) for s in self.samples if _num(s[0])]
-        mx = [float(s[1]) for s in self.samples if _num(s[1])]
-        pw = [float(s[2]) for s in self.samples if _num(s[2])]
+        inside = lambda t, w: w is None or w[0] <= t <= w[1]
+        load = [p for t, p in self.samples if inside(t, window)]
+        sm = [float(s[0]) for s in load if _num(s[0])]
+        mx = [float(s[1]) for s in load if _num(s[1])]
+        pw = [float(s[2]) for s in load if _num(s[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4)
+        reasons = sorted({names[i] for s in load for i in range(4)
                           if s[4 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None,
-                "samples": len(self.samples), "reasons": reasons}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None,
+               "power_w_max": max(pw) if pw else None,
+               "samples": len(load), "reasons": reasons}
+        if timed is not None:
+            out["samples_in_timed_region"] = sum(1 for t, _ in self.samples if inside(t, timed))
+        return out
 
 
 def _num(s):
@@ -851,19 +865,35 @@ def main():
     barrier()
     clocks = ClockSampler(local)
     clocks.start()
+    time.sleep(0.3)  # the sampler's first samples land before the timed region
     timer = Timer()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     nvtx.range_push(f"timed: {args.steps} steps of quantize X and W + MX GEMM")
     # per-kernel spans on every 4th step: events around every launch cost the
     # step ~0.5 % (measured), a quarter of that sampled this way
+    t_begin = time.monotonic()
     ev0.record()
     for i in range(args.steps):
         wl.step(timer if i % 4 == 0 else None, st)
     ev1.record()
     nvtx.range_pop()
     barrier()
-    clk = clocks.stop()
+    t_end = time.monotonic()
+    # clock window: a timed region shorter than the sampler's 200 ms period
+    # would see no sample, so the same step keeps running (untimed) until the
+    # loaded span reaches CLOCK_WINDOW_S; the clock figures are the samples
+    # of the whole span, the timed region's own count reported beside them
+    nvtx.range_push("clock window: the same step, untimed")
+    while time.monotonic() - t_begin < CLOCK_WINDOW_S:
+        for _ in range(50):
+            wl.step(None, st)
+        torch.cuda.synchronize()
+    nvtx.range_pop()
+    t_load = time.monotonic()
+    clk = clocks.stop(window=(t_begin, t_load), timed=(t_begin, t_end))
+    clk["window"] = (f"timed region ({t_end - t_begin:.3f} s) and the same step run untimed "
+                     f"after it, {t_load - t_begin:.2f} s in all")
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     gemm_ms = timer.avg_ms("gemm")
     q_ms = timer.avg_ms("quantize")
@@ -892,7 +922,13 @@ def main():
         return 0
 
     pk = peaks()
-    fp8_peak = pk["bf16_sustained"] * FP8_OVER_BF16
+    # the measured BF16 peak of the matching kind (a burst for a timed region
+    # under SUSTAINED_AFTER_S, the power-capped sustained rate beyond), times
+    # the nominal FP8 / BF16 ratio
+    region_s = ms_total / 1e3
+    kind = "burst" if region_s < SUSTAINED_AFTER_S else "sustained"
+    bf16_peak = pk["bf16"] if kind == "burst" else pk["bf16_sustained"]
+    fp8_peak = bf16_peak * FP8_OVER_BF16
     achieved = wl.flops / (gemm_ms / 1e3) / 1e12
     q_bytes = (wl.M * wl.K + wl.N * wl.K) * MX_ROW_BYTES
     q_gbs = q_bytes / (q_ms / 1e3) / 1e9
@@ -916,8 +952,11 @@ def main():
                    "l2": "inputs larger than L2 (X+W bf16 = 192 MB > 129 MB); no flush"},
         "roofline": {"bound": "tensor", "kernel": "gemm_kernel<MX>", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "peak_source": f"{pk['source']}: bf16 sustained {pk['bf16_sustained']} x {FP8_OVER_BF16} (nominal FP8/BF16)",
+                     "peak_source": (f"{pk['source']}: bf16 {kind} {bf16_peak} x {FP8_OVER_BF16} "
+                                     f"(nominal FP8/BF16); {kind} because the timed region "
+                                     f"lasted {region_s:.3f} s"),
                      "frac_of_4500_nominal": achieved / 4500.0,
+                     "launch_kcycles_at_median_clock": (gemm_ms * clk["sm_mhz"]) if clk.get("sm_mhz") else None,
                      "traffic": recorded_traffic("gemm.cu", "gemm_mx_mlp_up"),
                      "avg_launch_ms": gemm_ms},
         "quantize": {"bound": "hbm", "achieved": q_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",

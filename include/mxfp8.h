@@ -210,8 +210,13 @@ size_t mxfp8_tensor_workspace_bytes(void);
  * The scratch this path needs does not grow with n (it is
  * mxfp8_tensor_workspace_bytes()); a need larger than the static array would
  * be rejected with MXFP8_ERR_UNSUPPORTED_SHAPE before anything runs.
+ * The path uses 68 bytes of the array (one amax word and a grid-barrier
+ * counter, sized for the batched kernel's 16 tensors).
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current) and keeps it for the life of the process; make that
+ * first call before any stream capture.  The address belongs to the device's
+ * context at that moment: after a cudaDeviceReset, or any other teardown of
+ * that context, do not call this entry point again in the same process.
  * All calls on a device share the array and each clears the words it needs
  * on its stream first: calls that overlap on the GPU (e.g. on two streams)
  * race and must not be issued.  Allocates nothing (no cudaMalloc, cudaFree

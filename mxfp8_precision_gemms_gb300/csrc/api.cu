@@ -261,7 +261,7 @@ mxfp8_status fp8_quantize_mx_grouped(const void* x_bf16, int64_t total_rows, int
                        "fp8_quantize_mx_grouped launch");
 }
 
-size_t mxfp8_tensor_workspace_bytes(void) { return 256; }
+size_t mxfp8_tensor_workspace_bytes(void) { return kTensorWorkspaceBytes; }
 
 mxfp8_status fp8_quantize_tensor_scaled(const void* x_bf16, int64_t n, int fmt,
                                         const float* scale_dev, void* q, float* amax_dev,
@@ -480,7 +480,7 @@ mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt,
         (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u))
         return fail(MXFP8_ERR_MISALIGNED, "pointer misaligned");
     // the scratch this path needs must fit the library's static array
-    const size_t need = mxfp8_tensor_workspace_bytes();
+    const size_t need = kTensorScratchBytes;
     if (need > noalloc_scratch_bytes())
         return fail(MXFP8_ERR_UNSUPPORTED_SHAPE,
                     "needs %zu bytes of scratch, the static device array holds %zu", need,

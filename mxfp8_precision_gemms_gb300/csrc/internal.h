@@ -39,6 +39,16 @@ cudaError_t launch_quantize_tensor(const uint16_t* x, int64_t n, int fmt, float*
 // Tensors one batched per-tensor launch accepts.
 constexpr int kMaxBatch = 16;
 
+// Scratch of the single-launch per-tensor path: kMaxBatch + 1 uint32 words
+// (one amax word per tensor, then the grid barrier's arrival count), cleared
+// on the stream before each launch.  kTensorWorkspaceBytes is what
+// mxfp8_tensor_workspace_bytes() reports (the documented size, with room
+// to spare) and what the allocation-free entry point's static array holds.
+constexpr size_t kTensorScratchBytes = (kMaxBatch + 1) * sizeof(uint32_t);
+constexpr size_t kTensorWorkspaceBytes = 256;
+static_assert(kTensorScratchBytes <= kTensorWorkspaceBytes,
+              "the per-tensor scratch must fit the documented workspace");
+
 // Single cooperative launch for `count` tensors (amax[t], scale[t] are
 // consecutive device floats); ws: kMaxBatch + 1 uint32 of device scratch
 // (zeroed here).

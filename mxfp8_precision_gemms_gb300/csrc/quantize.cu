@@ -998,7 +998,7 @@ cudaError_t launch_quantize_tensor_batch(int count, const uint16_t* const* x, co
                                          int fmt, float* amax, float* scale, uint8_t* const* q,
                                          uint32_t* ws, cudaStream_t s) {
     if (count < 1 || count > kMaxBatch) return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(ws, 0, (kMaxBatch + 1) * sizeof(uint32_t), s);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kTensorScratchBytes, s);
     if (e != cudaSuccess) return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1043,8 +1043,9 @@ cudaError_t launch_quantize_tensor_fused(const uint16_t* x, int64_t n, int fmt, 
 // Scratch of fp8_quantize_tensor_noalloc: a file-scope device array, so that
 // entry point needs no memory from its caller.  Every GPU that loads this
 // library holds these 256 bytes until the process exits; all calls on a
-// device share them.
-constexpr size_t kNoAllocScratchBytes = 256;
+// device share them (the launch clears the first kTensorScratchBytes = 68).
+constexpr size_t kNoAllocScratchBytes = kTensorWorkspaceBytes;
+static_assert(kTensorScratchBytes <= kNoAllocScratchBytes, "per-tensor scratch exceeds the static array");
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / 4];
 
 size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
@@ -1052,6 +1053,8 @@ size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the symbol's name is only a host-side stand-in, so the address is looked up
 // with cudaGetSymbolAddress, once per device, while that device is current.
+// The cached address belongs to the device's context of that moment: a
+// cudaDeviceReset (or any other teardown of that context) invalidates it.
 cudaError_t noalloc_scratch_address(uint32_t** out) {
     constexpr int kDevices = 64;
     static std::mutex mu;
