@@ -293,26 +293,43 @@ def hot_path_rows(m, dev, steps, warmup):
                               sw, n, n, n, C.data_ptr(), n, st))
         if e: e.record()
     # X + W (64 MB) and the step's other tensors fit in L2: flush it before
-    # every step (outside the timed spans) so the quantizer reads HBM
+    # every step (outside the timed spans) so the quantizer reads HBM.  The
+    # flush writes 256 MB and then reads another 256 MB buffer: the read
+    # evicts the write's dirty lines, so their write-back to HBM happens in
+    # the flush rather than inside the next quantizer span.  The write-only
+    # flush is timed as well, for comparison.
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        flush.fill_(1)
-        pt(None)
-    torch.cuda.synchronize()
-    t = Timer()
-    for i in range(steps):
-        flush.fill_(i & 0xFF)
-        pt(t)
-    torch.cuda.synchronize()
-    ms = t.avg_ms("quantize") + t.avg_ms("gemm")
-    del flush
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(write_only):
+        for _ in range(warmup):
+            flush.fill_(1)
+            if not write_only:
+                clean.max()
+            pt(None)
+        torch.cuda.synchronize()
+        t = Timer()
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            if not write_only:
+                clean.max()
+            pt(t)
+        torch.cuda.synchronize()
+        return t.avg_ms("quantize"), t.avg_ms("gemm")
+    q_ms_wo, _ = timed(True)
+    q_ms, g_ms = timed(False)
+    ms = q_ms + g_ms
+    del flush, clean
     fl = 2.0 * n ** 3
     rows["per_tensor_4096"] = {
         "ms_per_step": ms, "tflops_incl_quantize": fl / ms / 1e9,
-        "gemm_tflops": fl / t.avg_ms("gemm") / 1e9,
-        "quantize_gbs": 2 * n * n * TENSOR_Q_BYTES / t.avg_ms("quantize") / 1e6,
+        "gemm_tflops": fl / g_ms / 1e9,
+        "quantize_gbs": 2 * n * n * TENSOR_Q_BYTES / q_ms / 1e6,
+        "quantize_gbs_write_only_flush": 2 * n * n * TENSOR_Q_BYTES / q_ms_wo / 1e6,
         "launches_per_step": 2, "quantize_path": "X and W in one cooperative launch (workspace)",
-        "l2": "flushed (256 MB write) before every step; ms_per_step = quantize + GEMM spans"}
+        "l2": ("flushed before every step: a 256 MB write, then a 256 MB read of another buffer "
+               "(the write's dirty lines leave L2 during the flush); ms_per_step = quantize + "
+               "GEMM spans")}
     del X, W, qx, qw, C, w
 
     # backward of a 4096 -> 4096 linear over 8192 tokens
