@@ -12,9 +12,12 @@
   of the ranks' scales, every rank requantizes to it, the payloads are summed
   and the sum carries the scale N * s_g.
 
-The arithmetic runs in the library's kernels (or, in CPU tests, in whatever
-callables the caller passes); this module only keeps state and orders the
-steps.  It never falls back to a host computation of its own.
+The per-tensor casts and the requantization run in the library's kernels
+(fp8_quantize_tensor_delayed, fp8_requantize_tensor) when the caller passes
+them; in shared_scale_reduce the decode of the requantized payload is the
+caller's callable, while the fp32 sum over ranks and the overflow count are
+torch operations over the process group (the protocol is exercised on CPU
+ranks with gloo: every box here has one GPU).
 """
 from __future__ import annotations
 
