@@ -253,6 +253,31 @@ mxfp8_status fp8_scaled_gemm(int mode, int a_fmt, int b_fmt, const void* a,
                              mxfp8_stream_t stream);
 
 /*
+ * fp8_scaled_gemm_pair - two independent fp8_scaled_gemm calls of one mode in
+ * one launch, e.g. the two products of a linear layer's backward: dgrad
+ * dX = dY . W and wgrad dW = dY^T . X ("Olmo-core MoE report", Section
+ * 11.3.2, Eq. 60, with the operands quantized in the orientation each GEMM
+ * consumes).
+ *
+ * Problem i (i = 0, 1) takes a_fmt_i, b_fmt_i, a_i, a_scale_i, b_i,
+ * b_scale_i, M_i, N_i, K_i, c_i, ldc_i with exactly the meaning, layout,
+ * requirements and result of fp8_scaled_gemm's arguments: each C_i is
+ * bit-identical to what fp8_scaled_gemm writes (the same dot products in the
+ * same K order).  The persistent kernel gives each problem its own share of
+ * the SMs' CTA pairs, chosen on the host so that both finish together, which
+ * fills the partial last waves two separate launches would each leave.  If
+ * either problem has M, N or K == 0, the two are run as separate calls.
+ * Argument errors of either problem return before anything is launched.
+ * C_0 and C_1 must not overlap.
+ */
+mxfp8_status fp8_scaled_gemm_pair(int mode, int a_fmt0, int b_fmt0, const void* a0,
+                                  const void* a_scale0, const void* b0, const void* b_scale0,
+                                  int64_t M0, int64_t N0, int64_t K0, void* c0_bf16, int64_t ldc0,
+                                  int a_fmt1, int b_fmt1, const void* a1, const void* a_scale1,
+                                  const void* b1, const void* b_scale1, int64_t M1, int64_t N1,
+                                  int64_t K1, void* c1_bf16, int64_t ldc1, mxfp8_stream_t stream);
+
+/*
  * fp8_grouped_gemm - per-expert MXFP8 GEMM over ragged, row-sorted groups.
  * ("Olmo-core MoE report", Section 11.1.1 and 11.4.1: the grouped expert
  *  GEMMs consume the dispatched activation and the cached expert weights.)

@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_swiglu_quantize_mx": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
                 "fp8_route_weight_quantize_mx": (st, [P, I64, I64, P, P, I64, I64, P, I32, U, P, P, P]),
                 "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
+                "fp8_scaled_gemm_pair": (st, [I] + [I, I, P, P, P, P, I64, I64, I64, P, I64] * 2 + [P]),
                 "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mxfp8_last_device_status": (st, [P]),
                 "mxfp8_status_string": (ctypes.c_char_p, [st]),
@@ -373,6 +374,27 @@ def fp8_scaled_gemm(mode: int, a: torch.Tensor, a_scale: torch.Tensor, b: torch.
     _check(lib().fp8_scaled_gemm(mode, a_fmt, b_fmt, _ptr(a), _ptr(a_scale), _ptr(b), _ptr(b_scale),
                                  M, N, K, _ptr(c), c.stride(0), _stream(stream)))
     return c
+
+
+def fp8_scaled_gemm_pair(mode: int, first, second, stream=None):
+    """Two independent GEMMs of one mode in one launch.  first / second are
+    dicts with a, a_scale, b, b_scale (as fp8_scaled_gemm) and optionally c,
+    a_fmt, b_fmt; returns (C0, C1)."""
+    args, outs = [], []
+    for g in (first, second):
+        a, b = g["a"], g["b"]
+        assert a.dtype == torch.uint8 and b.dtype == torch.uint8 and a.dim() == 2 and b.dim() == 2
+        _need_cuda(a, b, g["a_scale"], g["b_scale"])
+        M, K = a.shape
+        N = b.shape[0]
+        assert b.shape[1] == K and a.is_contiguous() and b.is_contiguous()
+        c = g.get("c")
+        c = c if c is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+        args += [g.get("a_fmt", FP8_E4M3), g.get("b_fmt", FP8_E4M3), _ptr(a), _ptr(g["a_scale"]),
+                 _ptr(b), _ptr(g["b_scale"]), M, N, K, _ptr(c), c.stride(0)]
+        outs.append(c)
+    _check(lib().fp8_scaled_gemm_pair(mode, *args, _stream(stream)))
+    return outs[0], outs[1]
 
 
 def fp8_grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, b: torch.Tensor, b_scale: torch.Tensor,

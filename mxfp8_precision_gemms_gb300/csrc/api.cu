@@ -125,6 +125,70 @@ bool encode_kchunk_map_u8(CUtensorMap* map, const void* base, int64_t rows, int6
     return r == CUDA_SUCCESS;
 }
 
+namespace {
+
+// What a checked GEMM call needs: a launch, nothing (M or N is 0) or a zero
+// fill of C (K == 0).
+enum GemmKind { kGemmLaunch, kGemmNothing, kGemmZero };
+
+mxfp8_status check_gemm(int mode, int a_fmt, int b_fmt, const void* a, const void* a_scale,
+                        const void* b, const void* b_scale, int64_t M, int64_t N, int64_t K,
+                        void* c_bf16, int64_t ldc, GemmArgs* g, GemmKind* kind) {
+    if (mode != GEMM_MX && mode != GEMM_TENSOR) return fail(MXFP8_ERR_INVALID_ARG, "unknown mode %d", mode);
+    if ((a_fmt != FP8_E4M3 && a_fmt != FP8_E5M2) || (b_fmt != FP8_E4M3 && b_fmt != FP8_E5M2))
+        return fail(MXFP8_ERR_INVALID_ARG, "unknown format");
+    if (mode == GEMM_MX && (a_fmt != FP8_E4M3 || b_fmt != FP8_E4M3))
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode takes E4M3 payloads");
+    if (M < 0 || N < 0 || K < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    *g = GemmArgs{};
+    g->M = M;
+    g->N = N;
+    g->c = static_cast<uint16_t*>(c_bf16);
+    g->ldc = ldc;
+    if (M == 0 || N == 0) {
+        *kind = kGemmNothing;
+        return MXFP8_OK;
+    }
+    if (!c_bf16) return fail(MXFP8_ERR_INVALID_ARG, "c is NULL");
+    if (ldc < N) return fail(MXFP8_ERR_INVALID_ARG, "ldc < N");
+    if (N % 8 || ldc % 8 || !aligned16(c_bf16))
+        return fail(MXFP8_ERR_MISALIGNED, "N, ldc or c not 16-byte aligned");
+    if (K == 0) {
+        *kind = kGemmZero;
+        return MXFP8_OK;
+    }
+    if (!a || !b || !a_scale || !b_scale) return fail(MXFP8_ERR_INVALID_ARG, "operand or scale is NULL");
+    if (mode == GEMM_MX && K % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode needs K %% 32 == 0");
+    if (K % 16) return fail(MXFP8_ERR_MISALIGNED, "K %% 16 != 0 (row stride of A/B)");
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    if (!aligned16(a) || !aligned16(b)) return fail(MXFP8_ERR_MISALIGNED, "operand not 16-byte aligned");
+    if (mode == GEMM_MX && (!aligned16(a_scale) || !aligned16(b_scale)))
+        return fail(MXFP8_ERR_MISALIGNED, "scale array not 16-byte aligned");
+    if (mode == GEMM_TENSOR &&
+        ((reinterpret_cast<uintptr_t>(a_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_scale) & 3u)))
+        return fail(MXFP8_ERR_MISALIGNED, "scale scalar not 4-byte aligned");
+    g->mode = mode;
+    g->a_fmt = a_fmt;
+    g->b_fmt = b_fmt;
+    g->a = static_cast<const uint8_t*>(a);
+    g->a_scale = a_scale;
+    g->b = static_cast<const uint8_t*>(b);
+    g->b_scale = b_scale;
+    g->K = K;
+    *kind = kGemmLaunch;
+    return MXFP8_OK;
+}
+
+// One checked GEMM on its own.
+mxfp8_status run_gemm(const GemmArgs& g, GemmKind kind, cudaStream_t s, const char* what) {
+    if (kind == kGemmNothing) return ok();
+    if (kind == kGemmZero) return cuda_result(launch_zero_fill_bf16(g.c, g.M, g.N, g.ldc, s), "zero fill");
+    return cuda_result(launch_gemm(g, s), what);
+}
+
+}  // namespace
+
 }  // namespace mxfp8
 
 using namespace mxfp8;
@@ -498,45 +562,33 @@ mxfp8_status fp8_quantize_tensor_noalloc(const void* x_bf16, int64_t n, int fmt,
 mxfp8_status fp8_scaled_gemm(int mode, int a_fmt, int b_fmt, const void* a, const void* a_scale,
                              const void* b, const void* b_scale, int64_t M, int64_t N, int64_t K,
                              void* c_bf16, int64_t ldc, mxfp8_stream_t stream) {
-    if (mode != GEMM_MX && mode != GEMM_TENSOR) return fail(MXFP8_ERR_INVALID_ARG, "unknown mode %d", mode);
-    if ((a_fmt != FP8_E4M3 && a_fmt != FP8_E5M2) || (b_fmt != FP8_E4M3 && b_fmt != FP8_E5M2))
-        return fail(MXFP8_ERR_INVALID_ARG, "unknown format");
-    if (mode == GEMM_MX && (a_fmt != FP8_E4M3 || b_fmt != FP8_E4M3))
-        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode takes E4M3 payloads");
-    if (M < 0 || N < 0 || K < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
-    if (M == 0 || N == 0) return ok();
-    if (!c_bf16) return fail(MXFP8_ERR_INVALID_ARG, "c is NULL");
-    if (ldc < N) return fail(MXFP8_ERR_INVALID_ARG, "ldc < N");
-    if (N % 8 || ldc % 8 || !aligned16(c_bf16))
-        return fail(MXFP8_ERR_MISALIGNED, "N, ldc or c not 16-byte aligned");
-    if (K == 0) return cuda_result(launch_zero_fill_bf16(static_cast<uint16_t*>(c_bf16), M, N, ldc,
-                                                         reinterpret_cast<cudaStream_t>(stream)),
-                                   "zero fill");
-    if (!a || !b || !a_scale || !b_scale) return fail(MXFP8_ERR_INVALID_ARG, "operand or scale is NULL");
-    if (mode == GEMM_MX && K % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "MX mode needs K %% 32 == 0");
-    if (K % 16) return fail(MXFP8_ERR_MISALIGNED, "K %% 16 != 0 (row stride of A/B)");
-    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
-        return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
-    if (!aligned16(a) || !aligned16(b)) return fail(MXFP8_ERR_MISALIGNED, "operand not 16-byte aligned");
-    if (mode == GEMM_MX && (!aligned16(a_scale) || !aligned16(b_scale)))
-        return fail(MXFP8_ERR_MISALIGNED, "scale array not 16-byte aligned");
-    if (mode == GEMM_TENSOR &&
-        ((reinterpret_cast<uintptr_t>(a_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_scale) & 3u)))
-        return fail(MXFP8_ERR_MISALIGNED, "scale scalar not 4-byte aligned");
-    GemmArgs g{};
-    g.mode = mode;
-    g.a_fmt = a_fmt;
-    g.b_fmt = b_fmt;
-    g.a = static_cast<const uint8_t*>(a);
-    g.a_scale = a_scale;
-    g.b = static_cast<const uint8_t*>(b);
-    g.b_scale = b_scale;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.c = static_cast<uint16_t*>(c_bf16);
-    g.ldc = ldc;
-    return cuda_result(launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "fp8_scaled_gemm launch");
+    GemmArgs g;
+    GemmKind kind;
+    const mxfp8_status st =
+        check_gemm(mode, a_fmt, b_fmt, a, a_scale, b, b_scale, M, N, K, c_bf16, ldc, &g, &kind);
+    if (st != MXFP8_OK) return st;
+    return run_gemm(g, kind, reinterpret_cast<cudaStream_t>(stream), "fp8_scaled_gemm launch");
+}
+
+mxfp8_status fp8_scaled_gemm_pair(int mode, int a_fmt0, int b_fmt0, const void* a0,
+                                  const void* a_scale0, const void* b0, const void* b_scale0,
+                                  int64_t M0, int64_t N0, int64_t K0, void* c0_bf16, int64_t ldc0,
+                                  int a_fmt1, int b_fmt1, const void* a1, const void* a_scale1,
+                                  const void* b1, const void* b_scale1, int64_t M1, int64_t N1,
+                                  int64_t K1, void* c1_bf16, int64_t ldc1, mxfp8_stream_t stream) {
+    GemmArgs g0, g1;
+    GemmKind k0, k1;
+    mxfp8_status st = check_gemm(mode, a_fmt0, b_fmt0, a0, a_scale0, b0, b_scale0, M0, N0, K0,
+                                 c0_bf16, ldc0, &g0, &k0);
+    if (st != MXFP8_OK) return st;
+    st = check_gemm(mode, a_fmt1, b_fmt1, a1, a_scale1, b1, b_scale1, M1, N1, K1, c1_bf16, ldc1, &g1, &k1);
+    if (st != MXFP8_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (k0 == kGemmLaunch && k1 == kGemmLaunch)
+        return cuda_result(launch_gemm_dual(g0, g1, s), "fp8_scaled_gemm_pair launch");
+    st = run_gemm(g0, k0, s, "fp8_scaled_gemm_pair launch (first)");
+    if (st != MXFP8_OK) return st;
+    return run_gemm(g1, k1, s, "fp8_scaled_gemm_pair launch (second)");
 }
 
 mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b, const void* b_scale,

@@ -227,12 +227,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // 2 * SLOTS_PER_BAR rows with p.merged (out-of-range tiles read as 0).
 // tm_c: C as BF16, 32 x 32 boxes with 64-byte swizzle (plain GEMM only; the
 // store clips rows and columns outside M x N).
+// The kernel body for one problem, run by the CTA pairs pair_id of
+// num_pairs (a persistent round robin over the problem's work units).
 template <bool MX, bool GROUPED, bool PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const __grid_constant__ CUtensorMap tm_bh, const __grid_constant__ CUtensorMap tm_sa,
-                const __grid_constant__ CUtensorMap tm_sb, const __grid_constant__ CUtensorMap tm_c,
-                const KParams p) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap* tm_a, const CUtensorMap* tm_b,
+                                          const CUtensorMap* tm_bh, const CUtensorMap* tm_sa,
+                                          const CUtensorMap* tm_sb, const CUtensorMap* tm_c,
+                                          const KParams& p, int64_t pair_id, int64_t num_pairs) {
     using C = Cfg<PAIR>;
     constexpr int CG = C::CG;
     extern __shared__ uint8_t smem_raw[];
@@ -243,8 +244,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0;
     const bool leader = rank == 0;
-    const int64_t pair_id = blockIdx.x / CG;
-    const int64_t num_pairs = gridDim.x / CG;
 
     auto bar = [&](uint32_t i) { return sbase + C::OFF_BAR + 8 * i; };
     constexpr uint32_t NB = C::NBARS;
@@ -331,12 +330,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tm_a);
-            tma_prefetch_desc(&tm_b);
-            if (p.split_from < p.total_units) tma_prefetch_desc(&tm_bh);
+            tma_prefetch_desc(tm_a);
+            tma_prefetch_desc(tm_b);
+            if (p.split_from < p.total_units) tma_prefetch_desc(tm_bh);
             if constexpr (MX) {
-                tma_prefetch_desc(&tm_sa);
-                tma_prefetch_desc(&tm_sb);
+                tma_prefetch_desc(tm_sa);
+                tma_prefetch_desc(tm_sb);
             }
             uint32_t pb = 0, phase = 0;              // slot pair (barrier) and its parity
             uint32_t issued = 0, issued_parity = 0;  // per-barrier bit masks (leader's drain)
@@ -356,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                              p.num_k_tiles;
                 const int32_t b_row =
                     static_cast<int32_t>(tl.b_row + rank * (hu ? C::B_ROWS / 2 : C::B_ROWS));
-                const CUtensorMap* mb = hu ? &tm_bh : &tm_b;  // 2D maps (per-slot copies)
+                const CUtensorMap* mb = hu ? tm_bh : tm_b;  // 2D maps (per-slot copies)
                 const uint32_t slot_tx = hu ? kSlotTxHalf : kSlotTx;
                 for (int kt0 = 0; kt0 < p.num_k_tiles; kt0 += SLOTS_PER_BAR) {
                     const int nslots = min(SLOTS_PER_BAR, p.num_k_tiles - kt0);
@@ -382,30 +381,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt0));
                         if constexpr (PAIR) {
                             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
-                            tma_load_3d_pair(dA, &tm_a, fb, 0, static_cast<int32_t>(tl.a_row), kt0);
+                            tma_load_3d_pair(dA, tm_a, fb, 0, static_cast<int32_t>(tl.a_row), kt0);
                             if (!hu) {
-                                tma_load_3d_pair(dB, &tm_b, fb, 0, b_row, kt0);
+                                tma_load_3d_pair(dB, tm_b, fb, 0, b_row, kt0);
                             } else {  // 2D boxes of B_ROWS / 2 rows, one per slot
                                 for (int j = 0; j < SLOTS_PER_BAR; ++j)
-                                    tma_load_2d_pair(dB + j * C::B_BYTES, &tm_bh, fb, (kt0 + j) * BK, b_row);
+                                    tma_load_2d_pair(dB + j * C::B_BYTES, tm_bh, fb, (kt0 + j) * BK, b_row);
                             }
                             if constexpr (MX) {
-                                tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
-                                tma_load_2d_pair(dSBp, &tm_sb, fb, 0, yb0);
-                                if (!hu) tma_load_2d_pair(dSBp + SLOTS_PER_BAR * 512, &tm_sb, fb, 0, yb1);
+                                tma_load_2d_pair(dSA, tm_sa, fb, 0, ya);
+                                tma_load_2d_pair(dSBp, tm_sb, fb, 0, yb0);
+                                if (!hu) tma_load_2d_pair(dSBp + SLOTS_PER_BAR * 512, tm_sb, fb, 0, yb1);
                             }
                         } else {
-                            tma_load_3d(dA, &tm_a, fb_local, 0, static_cast<int32_t>(tl.a_row), kt0);
+                            tma_load_3d(dA, tm_a, fb_local, 0, static_cast<int32_t>(tl.a_row), kt0);
                             if (!hu) {
-                                tma_load_3d(dB, &tm_b, fb_local, 0, b_row, kt0);
+                                tma_load_3d(dB, tm_b, fb_local, 0, b_row, kt0);
                             } else {
                                 for (int j = 0; j < SLOTS_PER_BAR; ++j)
-                                    tma_load_2d(dB + j * C::B_BYTES, &tm_bh, fb_local, (kt0 + j) * BK, b_row);
+                                    tma_load_2d(dB + j * C::B_BYTES, tm_bh, fb_local, (kt0 + j) * BK, b_row);
                             }
                             if constexpr (MX) {
-                                tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
-                                tma_load_2d(dSBp, &tm_sb, fb_local, 0, yb0);
-                                if (!hu) tma_load_2d(dSBp + SLOTS_PER_BAR * 512, &tm_sb, fb_local, 0, yb1);
+                                tma_load_2d(dSA, tm_sa, fb_local, 0, ya);
+                                tma_load_2d(dSBp, tm_sb, fb_local, 0, yb0);
+                                if (!hu) tma_load_2d(dSBp + SLOTS_PER_BAR * 512, tm_sb, fb_local, 0, yb1);
                             }
                         }
                     } else {
@@ -422,20 +421,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const int32_t yb1 = static_cast<int32_t>(2 * (sfb_base + p.num_k_tiles + kt));
                             if constexpr (PAIR) {
                                 const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
-                                tma_load_2d_pair(dA, &tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
+                                tma_load_2d_pair(dA, tm_a, fb, kt * BK, static_cast<int32_t>(tl.a_row));
                                 tma_load_2d_pair(dB, mb, fb, kt * BK, b_row);
                                 if constexpr (MX) {
-                                    tma_load_2d_pair(dSA, &tm_sa, fb, 0, ya);
-                                    tma_load_2d_pair(dSB0, &tm_sb, fb, 0, yb0);
-                                    if (!hu) tma_load_2d_pair(dSB1, &tm_sb, fb, 0, yb1);
+                                    tma_load_2d_pair(dSA, tm_sa, fb, 0, ya);
+                                    tma_load_2d_pair(dSB0, tm_sb, fb, 0, yb0);
+                                    if (!hu) tma_load_2d_pair(dSB1, tm_sb, fb, 0, yb1);
                                 }
                             } else {
-                                tma_load_2d(dA, &tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
+                                tma_load_2d(dA, tm_a, fb_local, kt * BK, static_cast<int32_t>(tl.a_row));
                                 tma_load_2d(dB, mb, fb_local, kt * BK, b_row);
                                 if constexpr (MX) {
-                                    tma_load_2d(dSA, &tm_sa, fb_local, 0, ya);
-                                    tma_load_2d(dSB0, &tm_sb, fb_local, 0, yb0);
-                                    if (!hu) tma_load_2d(dSB1, &tm_sb, fb_local, 0, yb1);
+                                    tma_load_2d(dSA, tm_sa, fb_local, 0, ya);
+                                    tma_load_2d(dSB0, tm_sb, fb_local, 0, yb0);
+                                    if (!hu) tma_load_2d(dSB1, tm_sb, fb_local, 0, yb1);
                                 }
                             }
                         }
@@ -639,7 +638,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tm_c, stile, x0 + 32 * c, y);
+                            tma_store_2d(tm_c, stile, x0 + 32 * c, y);
                             bulk_commit_group();
                         }
                     }
@@ -686,6 +685,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_dealloc<CG>(tmem, TMEM_COLS);
     }
     if constexpr (PAIR) cluster_sync();
+}
+
+template <bool MX, bool GROUPED, bool PAIR>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_bh, const __grid_constant__ CUtensorMap tm_sa,
+                const __grid_constant__ CUtensorMap tm_sb, const __grid_constant__ CUtensorMap tm_c,
+                const __grid_constant__ KParams p) {
+    constexpr int CG = Cfg<PAIR>::CG;
+    gemm_body<MX, GROUPED, PAIR>(&tm_a, &tm_b, &tm_bh, &tm_sa, &tm_sb, &tm_c, p, blockIdx.x / CG,
+                                 gridDim.x / CG);
+}
+
+// Two independent plain GEMMs in one persistent launch: pairs0 of the CTA
+// pairs, spread evenly over the grid, run problem 0, the others problem 1,
+// each with the pipeline
+// above over its own work units (the host picks pairs0 so that both finish
+// together: the backward's dgrad and wgrad, whose last waves would otherwise
+// each leave pairs idle, and one launch boundary less).
+template <bool MX, bool PAIR>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_dual_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
+                     const __grid_constant__ CUtensorMap bh0, const __grid_constant__ CUtensorMap sa0,
+                     const __grid_constant__ CUtensorMap sb0, const __grid_constant__ CUtensorMap c0,
+                     const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1,
+                     const __grid_constant__ CUtensorMap bh1, const __grid_constant__ CUtensorMap sa1,
+                     const __grid_constant__ CUtensorMap sb1, const __grid_constant__ CUtensorMap c1,
+                     const __grid_constant__ KParams p0, const __grid_constant__ KParams p1,
+                     int32_t pairs0) {
+    constexpr int CG = Cfg<PAIR>::CG;
+    const int64_t pair = blockIdx.x / CG;
+    const int64_t pairs = gridDim.x / CG;
+    // problem 0's pairs spread evenly over the grid (and so over both dies):
+    // c(q) = floor(q pairs0 / pairs) of the pairs below q are problem 0's
+    const int64_t c = pair * pairs0 / pairs;
+    if ((pair + 1) * pairs0 / pairs > c)
+        gemm_body<MX, false, PAIR>(&a0, &b0, &bh0, &sa0, &sb0, &c0, p0, c, pairs0);
+    else
+        gemm_body<MX, false, PAIR>(&a1, &b1, &bh1, &sa1, &sb1, &c1, p1, pair - c, pairs - pairs0);
 }
 
 __global__ void zero_fill_kernel(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc) {
@@ -771,7 +809,17 @@ constexpr bool kPair = GEMM_PAIR != 0;
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+namespace {
+
+// Tensor maps, parameters and unit count of one GEMM.
+struct Prepared {
+    CUtensorMap ta, tb, tbh, tsa, tsb, tc;
+    KParams p;
+    int64_t units;
+    bool can_split;
+};
+
+cudaError_t prepare_gemm(const GemmArgs& g, Prepared* out) {
     using C = Cfg<kPair>;
     const bool grouped = g.groups > 0;
     const bool mx = g.mode == GEMM_MX;
@@ -786,7 +834,10 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     p.num_m_groups = (p.num_m_tiles + C::CG - 1) / C::CG;
     p.n_scale_tiles = static_cast<int32_t>((g.N + 127) / 128);
     p.sfb_group_chunks = static_cast<int64_t>(p.n_scale_tiles) * p.num_k_tiles;
-    CUtensorMap ta, tb, tsa, tsb;
+    CUtensorMap& ta = out->ta;
+    CUtensorMap& tb = out->tb;
+    CUtensorMap& tsa = out->tsa;
+    CUtensorMap& tsb = out->tsb;
     // whole slot pairs in one copy per operand when K splits into full pairs
     p.merged = g.K % (BK * SLOTS_PER_BAR) == 0 &&
                encode_kchunk_map_u8(&ta, g.a, g.M, g.K, BM, SLOTS_PER_BAR) &&
@@ -796,7 +847,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
          !make_map(&tb, g.b, b_rows, g.K, BK, C::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorInvalidValue;
     // half units (plain GEMM): B in boxes of half the rows, one per K step
-    CUtensorMap tbh = tb;
+    CUtensorMap& tbh = out->tbh;
+    tbh = tb;
     const bool can_split =
         !grouped && make_map(&tbh, g.b, b_rows, g.K, BK, C::B_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint32_t sf_box_rows = p.merged ? 2 * SLOTS_PER_BAR : 2;
@@ -823,7 +875,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     p.ldc = g.ldc;
     // C as BF16 32 x 32 boxes (grouped: only warps whose rows all lie in one
     // expert group store through it)
-    CUtensorMap tc;
+    CUtensorMap& tc = out->tc;
     if (!encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.M, g.N, g.ldc * 2, 32, 32,
                               CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
@@ -835,11 +887,121 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
     const int64_t units = grouped
         ? (static_cast<int64_t>(p.num_m_tiles) / C::CG + g.groups + 1) * p.num_n_tiles
         : static_cast<int64_t>(p.num_m_groups) * p.num_n_tiles;
-    if (mx) {
-        return grouped ? launch_kernel<true, true, kPair>(ta, tb, tbh, tsa, tsb, tc, p, units, false, s)
-                       : launch_kernel<true, false, kPair>(ta, tb, tbh, tsa, tsb, tc, p, units, can_split, s);
+    out->p = p;
+    out->units = units;
+    out->can_split = can_split;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+    Prepared d;
+    cudaError_t e = prepare_gemm(g, &d);
+    if (e != cudaSuccess) return e;
+    const bool mx = g.mode == GEMM_MX;
+    if (g.groups > 0)
+        return launch_kernel<true, true, kPair>(d.ta, d.tb, d.tbh, d.tsa, d.tsb, d.tc, d.p, d.units, false, s);
+    if (mx)
+        return launch_kernel<true, false, kPair>(d.ta, d.tb, d.tbh, d.tsa, d.tsb, d.tc, d.p, d.units,
+                                                 d.can_split, s);
+    return launch_kernel<false, false, kPair>(d.ta, d.tb, d.tbh, d.tsa, d.tsb, d.tc, d.p, d.units,
+                                              d.can_split, s);
+}
+
+namespace {
+
+// Units a problem gives `pairs` CTA pairs, as the launcher arranges them: a
+// last wave filling at most half the pairs is split into half units.
+void plan_units(const KParams& p_in, int64_t units, bool can_split, int64_t pairs, KParams* p) {
+    *p = p_in;
+    p->split_from = INT64_MAX;
+    p->total_units = units;
+    if (can_split && pairs > 0) {
+        const int64_t tail = units % pairs;
+        if (tail > 0 && 2 * tail <= pairs) {
+            p->split_from = units - tail;
+            p->total_units = units + tail;
+        }
     }
-    return launch_kernel<false, false, kPair>(ta, tb, tbh, tsa, tsb, tc, p, units, can_split, s);
+}
+
+// Time of a problem on `pairs` pairs in units of one K step: whole waves of
+// num_k_tiles steps, a split last wave at a little over half of that.
+double plan_cost(const KParams& p, int64_t units, bool can_split, int64_t pairs) {
+    if (pairs <= 0) return 1e300;
+    const int64_t waves = units / pairs, tail = units % pairs;
+    double w = static_cast<double>(waves);
+    if (tail > 0) w += (can_split && 2 * tail <= pairs) ? 0.55 : 1.0;
+    return w * p.num_k_tiles;
+}
+
+template <bool MX>
+cudaError_t launch_dual(const Prepared& d0, const Prepared& d1, cudaStream_t s) {
+    using C = Cfg<kPair>;
+    static std::atomic<int> resident[kMaxDevices];
+    const uint32_t smem = C::SMEM_PLAIN + 1024;
+    auto k = gemm_dual_kernel<MX, kPair>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = resident[dev].load(std::memory_order_relaxed);
+    if (max_clusters <= 0) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(C::CG * 64, 1, 1);
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
+        if (e != cudaSuccess || max_clusters <= 0) {
+            (void)cudaGetLastError();
+            max_clusters = sm_count_current_device() / C::CG;
+        }
+        resident[dev].store(max_clusters, std::memory_order_relaxed);
+    }
+    if (max_clusters < 2) return cudaErrorInvalidConfiguration;
+    // the split of the pairs whose slower problem finishes first
+    int64_t best = 1;
+    double best_cost = 1e300;
+    for (int64_t p0 = 1; p0 < max_clusters; ++p0) {
+        const double c = std::max(plan_cost(d0.p, d0.units, d0.can_split, p0),
+                                  plan_cost(d1.p, d1.units, d1.can_split, max_clusters - p0));
+        if (c < best_cost) {
+            best_cost = c;
+            best = p0;
+        }
+    }
+    KParams p0, p1;
+    plan_units(d0.p, d0.units, d0.can_split, best, &p0);
+    plan_units(d1.p, d1.units, d1.can_split, max_clusters - best, &p1);
+    cfg.gridDim = dim3(static_cast<unsigned>(max_clusters * C::CG), 1, 1);
+    const int32_t pairs0 = static_cast<int32_t>(best);
+    e = cudaLaunchKernelEx(&cfg, k, d0.ta, d0.tb, d0.tbh, d0.tsa, d0.tsb, d0.tc, d1.ta, d1.tb, d1.tbh,
+                           d1.tsa, d1.tsb, d1.tc, p0, p1, pairs0);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_dual(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s) {
+    Prepared d0, d1;
+    cudaError_t e = prepare_gemm(g0, &d0);
+    if (e == cudaSuccess) e = prepare_gemm(g1, &d1);
+    if (e != cudaSuccess) return e;
+    // the inject hook applies to the next launch once: give it to problem 0
+    d1.p.inject_timeout = 0;
+    return g0.mode == GEMM_MX ? launch_dual<true>(d0, d1, s) : launch_dual<false>(d0, d1, s);
 }
 
 cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc,

@@ -132,6 +132,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+// Two plain GEMMs of one mode (M, N, K > 0 each) in one persistent launch,
+// the CTA pairs split between them.
+cudaError_t launch_gemm_dual(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s);
 cudaError_t launch_zero_fill_bf16(uint16_t* c, int64_t rows, int64_t cols, int64_t ldc,
                                   cudaStream_t s);
 

@@ -119,6 +119,17 @@ def test_host_validation(lib):
     assert G(m.GEMM_MX, 0, 0, P, P, P, P, 128, 128, 128, P, 64, None) == m.MXFP8_ERR_INVALID_ARG
     assert G(m.GEMM_MX, 0, 0, P + 16, P + 8, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_MISALIGNED
     assert G(m.GEMM_MX, 0, 0, P, P, P, P, 0, 128, 128, P, 128, None) == m.MXFP8_OK
+    # the pair: either problem's bad argument fails the call before any launch
+    GP = lib.fp8_scaled_gemm_pair
+    good = (0, 0, P, P, P, P, 128, 128, 128, P, 128)
+    assert GP(5, *good, *good, None) == m.MXFP8_ERR_INVALID_ARG
+    assert GP(m.GEMM_MX, *good, 0, 0, P, P, P, P, 128, 128, 48, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert GP(m.GEMM_MX, 1, 0, P, P, P, P, 128, 128, 128, P, 128, *good, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert GP(m.GEMM_MX, *good, 0, 0, P, P, P, P, 128, 132, 128, P, 136, None) == m.MXFP8_ERR_MISALIGNED
+    assert GP(m.GEMM_MX, *good, 0, 0, None, P, P, P, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
+    # both empty: nothing to launch
+    empty = (0, 0, P, P, P, P, 0, 128, 128, P, 128)
+    assert GP(m.GEMM_MX, *empty, *empty, None) == m.MXFP8_OK
     # grouped
     GG = lib.fp8_grouped_gemm
     assert GG(P, P, P, P, P, 0, 128, 128, 128, P, 128, None) == m.MXFP8_ERR_INVALID_ARG
