@@ -531,6 +531,21 @@ def routed_conversion_rows(m, dev, steps, warmup):
         "bytes": "dY read once + payload and scales written + token/weight per row",
         "gbs_if_gathered_rows_counted": (R * D * (2 + 1 + 1 / 32) + R * 8) / ms / 1e6,
         "launches_per_step": 1}
+
+    # the same conversion with the routing given per token (each dY row read once)
+    trows = torch.from_numpy(w["token_rows"]).to(dev)
+    twts = torch.from_numpy(w["token_weights"]).to(dev)
+    K_ROUTES = trows.shape[1]
+
+    def rwt(timer):
+        _ok(L.fp8_route_weight_quantize_mx_tokens(dY.data_ptr(), T, D, K_ROUTES, trows.data_ptr(),
+                                                  twts.data_ptr(), R, D, off.data_ptr(), G, 0,
+                                                  qg.data_ptr(), sg.data_ptr(), st))
+    ms, _ = _time_steps(rwt, steps, warmup)
+    rows["route_weight_quantize_tokens_262144x2048"] = {
+        "ms_per_step": ms, "gbs": unique / ms / 1e6,
+        "bytes": "dY read once + payload and scales written + row/weight per route",
+        "launches_per_step": 2, "note": "scale array zeroed first (a memset), then one kernel"}
     del dY, qg, sg, w
     return rows
 

@@ -467,6 +467,39 @@ mxfp8_status fp8_route_weight_quantize_mx(const void* dy_bf16, int64_t tokens, i
                                           mxfp8_stream_t stream);
 
 /*
+ * fp8_route_weight_quantize_mx_tokens - fp8_route_weight_quantize_mx with the
+ * routing given per token: each token's gradient row is read once and its k
+ * route-weighted copies are quantized into their dispatched rows ("Olmo-core
+ * MoE report", Section 11.4.1 and Table 25, route weighting + gradient Q in
+ * combine backward).
+ *
+ *  dy_bf16            device, tokens x cols BF16, leading dimension ld.
+ *  k                  routes per token, 1..16.
+ *  token_rows_dev     device, tokens x k int32: the dispatched row of each of
+ *                     the token's routes (-1: no route in that slot).  A row
+ *                     >= rows records MXFP8_ERR_DEVICE_CHECK and is skipped.
+ *  token_weights_dev  device, tokens x k fp32 route weights.
+ *  rows, cols, group_offsets_dev, groups, flags, q, s: as in
+ *                     fp8_route_weight_quantize_mx (s holds
+ *                     mxfp8_scale_bytes(rows, cols) or, with offsets,
+ *                     mxfp8_grouped_scale_bytes(rows, cols, groups) bytes).
+ * Dispatched row i = (token t, slot j) with token_rows[t k + j] = i gets
+ * bf16_RNE(token_weights[t k + j] * dy[t]), rounded once from the exact
+ * product, MX-quantized rowwise: the same bytes as
+ * fp8_route_weight_quantize_mx with row_token[i] = t and row_weight[i] equal
+ * to that weight.  Every row in [0, rows) must be some token's route
+ * exactly once: a row no token names keeps its previous payload and gets
+ * zero scale bytes (the scale array is zeroed first, so padding reads 0).
+ * Requirements as fp8_route_weight_quantize_mx; groups <= 1024.
+ */
+mxfp8_status fp8_route_weight_quantize_mx_tokens(const void* dy_bf16, int64_t tokens, int64_t ld,
+                                                 int32_t k, const int32_t* token_rows_dev,
+                                                 const float* token_weights_dev, int64_t rows,
+                                                 int64_t cols, const int32_t* group_offsets_dev,
+                                                 int32_t groups, unsigned flags, void* q, void* s,
+                                                 mxfp8_stream_t stream);
+
+/*
  * mxfp8_last_device_status - synchronize `stream`, then return and clear the
  * device status word of the current device: MXFP8_OK, MXFP8_ERR_DEVICE_CHECK
  * or MXFP8_ERR_TIMEOUT (the first one recorded since the last call), or

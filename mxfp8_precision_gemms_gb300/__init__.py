@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_dequantize_mx": (st, [P, P, I64, I64, P, I32, P, I64, P]),
                 "fp8_swiglu_quantize_mx": (st, [P, I64, I64, I64, P, I32, U, P, P, P]),
                 "fp8_route_weight_quantize_mx": (st, [P, I64, I64, P, P, I64, I64, P, I32, U, P, P, P]),
+                "fp8_route_weight_quantize_mx_tokens": (st, [P, I64, I64, I32, P, P, I64, I64, P, I32, U, P, P, P]),
                 "fp8_scaled_gemm": (st, [I, I, I, P, P, P, P, I64, I64, I64, P, I64, P]),
                 "fp8_scaled_gemm_pair": (st, [I] + [I, I, P, P, P, P, I64, I64, I64, P, I64] * 2 + [P]),
                 "fp8_grouped_gemm": (st, [P, P, P, P, P, I32, I64, I64, I64, P, I64, P]),
@@ -356,6 +357,29 @@ def fp8_route_weight_quantize_mx(dy: torch.Tensor, row_token: torch.Tensor, row_
                                               _ptr(row_weight), rows, cols, _ptr(offsets),
                                               _groups(offsets), flags, _ptr(q), _ptr(s),
                                               _stream(stream)))
+    return q, s
+
+
+def fp8_route_weight_quantize_mx_tokens(dy: torch.Tensor, token_rows: torch.Tensor,
+                                        token_weights: torch.Tensor, rows: int, offsets=None,
+                                        flags: int = 0, q=None, s=None, stream=None):
+    """The same conversion with the routing given per token: token_rows
+    (tokens x k int32 dispatched rows, -1 for none) and token_weights
+    (tokens x k fp32); each dY row is read once.  Returns (q, s)."""
+    assert dy.dtype == torch.bfloat16 and dy.dim() == 2 and dy.stride(1) == 1
+    assert token_rows.dtype == torch.int32 and token_weights.dtype == torch.float32
+    assert token_rows.shape == token_weights.shape and token_rows.dim() == 2
+    assert token_rows.is_contiguous() and token_weights.is_contiguous()
+    _need_cuda(dy, token_rows, token_weights, offsets)
+    tokens, cols = dy.shape
+    assert token_rows.shape[0] == tokens
+    k = token_rows.shape[1]
+    q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=dy.device)
+    s = s if s is not None else _scales_for(rows, cols, offsets, dy.device)
+    _check(lib().fp8_route_weight_quantize_mx_tokens(_ptr(dy), tokens, dy.stride(0), k,
+                                                     _ptr(token_rows), _ptr(token_weights), rows,
+                                                     cols, _ptr(offsets), _groups(offsets), flags,
+                                                     _ptr(q), _ptr(s), _stream(stream)))
     return q, s
 
 

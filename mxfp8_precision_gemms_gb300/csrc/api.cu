@@ -629,6 +629,47 @@ mxfp8_status fp8_grouped_gemm(const void* a, const void* a_scale, const void* b,
     return cuda_result(launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "fp8_grouped_gemm launch");
 }
 
+mxfp8_status fp8_route_weight_quantize_mx_tokens(const void* dy_bf16, int64_t tokens, int64_t ld,
+                                                 int32_t k, const int32_t* token_rows_dev,
+                                                 const float* token_weights_dev, int64_t rows,
+                                                 int64_t cols, const int32_t* group_offsets_dev,
+                                                 int32_t groups, unsigned flags, void* q, void* s,
+                                                 mxfp8_stream_t stream) {
+    if (flags & ~(unsigned)(MX_ROWWISE | MX_SCALE_FLOOR))
+        return fail(MXFP8_ERR_INVALID_ARG, "route-weighted quantization is rowwise only");
+    if (rows < 0 || cols < 0 || tokens < 0) return fail(MXFP8_ERR_INVALID_ARG, "negative size");
+    if (k < 1 || k > 16) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "k must be in [1, 16] (k=%d)", k);
+    mxfp8_status st = check_groups(group_offsets_dev, groups, rows);
+    if (st != MXFP8_OK) return st;
+    if (rows == 0 || cols == 0) return ok();
+    if (!dy_bf16 || !token_rows_dev || !token_weights_dev || !q || !s)
+        return fail(MXFP8_ERR_INVALID_ARG, "dy, token_rows, token_weights, q or s is NULL");
+    if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (cols=%lld)", (long long)cols);
+    if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");
+    if (ld % 8 || !aligned16(dy_bf16) || !aligned16(q) || !aligned16(s))
+        return fail(MXFP8_ERR_MISALIGNED, "pointer or ld not 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(token_rows_dev) | reinterpret_cast<uintptr_t>(token_weights_dev)) & 3u)
+        return fail(MXFP8_ERR_MISALIGNED, "token_rows or token_weights not 4-byte aligned");
+    WeightedTokensArgs a{};
+    a.dy = static_cast<const uint16_t*>(dy_bf16);
+    a.tokens = tokens;
+    a.ld = ld;
+    a.k = k;
+    a.token_rows = token_rows_dev;
+    a.token_weights = token_weights_dev;
+    a.rows = rows;
+    a.cols = cols;
+    a.offsets = group_offsets_dev;
+    a.groups = groups;
+    a.flags = flags;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = static_cast<uint8_t*>(s);
+    a.scale_bytes = group_offsets_dev ? mxfp8_grouped_scale_bytes(rows, cols, groups)
+                                      : mxfp8_scale_bytes(rows, cols);
+    return cuda_result(launch_weighted_quantize_tokens_mx(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "fp8_route_weight_quantize_mx_tokens launch");
+}
+
 mxfp8_status mxfp8_last_device_status(mxfp8_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));

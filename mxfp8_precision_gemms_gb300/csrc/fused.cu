@@ -413,17 +413,23 @@ __global__ void __launch_bounds__(kThreads, 4)
 // BF16 rounding midpoint is an fp32 number, so the BF16 rounding of p agrees
 // with that of the exact product unless p lands exactly on a midpoint (its
 // low 16 bits are 0x8000; this covers the fp32-subnormal range too, where
-// fp32 still has 16 more fraction bits than BF16).  `mid` (a running
-// minimum) becomes 0 for such a product, and the chunk is redone exactly in
-// double.  Overflow, Inf and NaN follow the
-// fp32 product, which agrees with the exact one in BF16.
+// fp32 still has 16 more fraction bits than BF16).  `mid` keeps the per-half
+// minimum of both products' low halves xor 0x8000 (one prmt, one xor, one
+// min.u16x2 per pair): a zero half marks such a product, and the chunk is
+// redone exactly in double.  Overflow, Inf and NaN follow the fp32 product,
+// which agrees with the exact one in BF16.
 __device__ __forceinline__ uint32_t weighted2(uint32_t x2, float w, uint32_t& mid) {
     const float p0 = __fmul_rn(bf16_lo(x2), w);
     const float p1 = __fmul_rn(bf16_hi(x2), w);
-    // (bits << 16) + 2^31 is zero exactly when the low half is 0x8000
-    mid = min(mid, min(__float_as_uint(p0) * 65536u + 0x80000000u,
-                       __float_as_uint(p1) * 65536u + 0x80000000u));
+    uint32_t lows;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(lows) : "r"(__float_as_uint(p0)), "r"(__float_as_uint(p1)));
+    mid = min_u16x2(mid, lows ^ 0x80008000u);
     return bf16x2_rn(p0, p1);
+}
+
+// Either half of a `mid` accumulator zero: some product sat on a midpoint.
+__device__ __forceinline__ bool weighted_tie(uint32_t mid) {
+    return (mid & 0xFFFFu) == 0u || (mid >> 16) == 0u;
 }
 
 // 8 products formed exactly in double and rounded once.
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             uint32_t mid = 0xFFFFFFFFu;
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = weighted2(xw[i][k], wv[i], mid);
-            if (mid == 0u) {
+            if (weighted_tie(mid)) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint4 e = weighted8_exact(
@@ -501,6 +507,178 @@ __global__ void __launch_bounds__(kThreads, 4)
                 }
             }
             mx_block32<FLOOR>(v, in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
+        }
+    }
+}
+
+// Token-walk form of the same conversion: each CTA takes kTokensPerCta
+// tokens and reads each token's dY row once; a thread owns one 32-value
+// block of one token and writes, for each of the token's k routes, the
+// weighted block's E4M3 payload into the route's dispatched row and its scale
+// byte into the (group-padded) scale array.  The per-value arithmetic is
+// weighted_quant_kernel's, exact-product ties included.
+constexpr int kTokensPerCta = 16;
+constexpr int kMaxRoutes = 16;
+constexpr int kMaxGroupsTok = 1024;
+
+template <bool FLOOR, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 4)
+    weighted_quant_tokens_kernel(const uint16_t* __restrict__ dy, int64_t tokens, int64_t ld,
+                                 int k, const int32_t* __restrict__ token_rows,
+                                 const float* __restrict__ token_weights, int64_t rows,
+                                 int64_t cols, const int32_t* offsets, int groups,
+                                 uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
+                                 bool v8) {
+    __shared__ int64_t s_row[kTokensPerCta * kMaxRoutes];   // dispatched row, -1: none
+    __shared__ int64_t s_prow[kTokensPerCta * kMaxRoutes];  // its row in the scale array
+    __shared__ float s_w[kTokensPerCta * kMaxRoutes];
+    __shared__ int32_t s_off[GROUPED ? kMaxGroupsTok + 1 : 1];
+    __shared__ int64_t s_pstart[GROUPED ? kMaxGroupsTok + 1 : 1];
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    if constexpr (GROUPED) {
+        // offsets into shared memory (validated: 0 first, non-decreasing,
+        // rows last) and the padded first scale row of every group
+        if (tid < 32) {
+            bool ok = offsets[0] == 0 && static_cast<int64_t>(offsets[groups]) == rows;
+            int64_t base = 0;
+            for (int g0 = 0; g0 <= groups; g0 += 32) {
+                const int g = g0 + tid;
+                int64_t tiles = 0;
+                if (g <= groups) s_off[g] = offsets[g];
+                if (g < groups) {
+                    const int32_t b = offsets[g], e = offsets[g + 1];
+                    if (e < b) ok = false;
+                    tiles = e > b ? (e - b + kTile - 1) / kTile : 0;
+                }
+                int64_t incl = tiles;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                    if (tid >= d) incl += v;
+                }
+                if (g <= groups) s_pstart[g] = (base + incl - tiles) * kTile;
+                base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (tid == 0) s_ok = ok ? 1 : 0;
+        }
+        __syncthreads();
+        if (!s_ok) {
+            if (blockIdx.x == 0 && tid == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
+            return;
+        }
+    }
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerCta;
+    const int nt = static_cast<int>(min(static_cast<int64_t>(kTokensPerCta), tokens - t0));
+    const int64_t nb = cols / 32;
+    // the first (token, block) item's dY loads go out before the route table
+    // is built, so the two latencies overlap
+    uint32_t xw[16];
+    int64_t pi = tid;
+    if (pi < nt * nb) {
+        const int tl = static_cast<int>(pi / nb);
+        const uint16_t* src = dy + (t0 + tl) * ld + (pi - tl * nb) * 32;
+        ld32_stream(src, xw, v8);
+        ld32_stream(src + 16, xw + 8, v8);
+    }
+    bool bad = false;
+    for (int e = tid; e < nt * k; e += blockDim.x) {
+        const int64_t idx = (t0 + e / k) * k + e % k;
+        const int32_t r = __ldg(token_rows + idx);
+        int64_t row = -1, prow = -1;
+        float w = 0.f;
+        if (r >= rows) {
+            bad = true;
+        } else if (r >= 0) {
+            row = r;
+            w = __ldg(token_weights + idx);
+            if constexpr (GROUPED) {
+                int lo = 0, hi = groups - 1;  // the last group starting at or before r
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_off[mid] <= r) lo = mid; else hi = mid - 1;
+                }
+                prow = s_pstart[lo] + (r - s_off[lo]);
+            } else {
+                prow = r;
+            }
+        }
+        s_row[e] = row;
+        s_prow[e] = prow;
+        s_w[e] = w;
+    }
+    if (bad) record_status(MXFP8_ERR_DEVICE_CHECK);
+    __syncthreads();
+    for (; pi < nt * nb; pi += blockDim.x) {
+        const int tl = static_cast<int>(pi / nb);
+        const int64_t b = pi - tl * nb;
+        if (pi != tid) {
+            const uint16_t* src = dy + (t0 + tl) * ld + b * 32;
+            ld32_stream(src, xw, v8);
+            ld32_stream(src + 16, xw + 8, v8);
+        }
+        // a route's block maximum is the correctly rounded |max |x| w|: the
+        // rounding is monotone, so one product per route replaces the
+        // maximum over the 32 weighted values (NaN and Inf carry over)
+        const float ax = __uint_as_float(block32_amax_bits(xw) << 16);
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const int e = tl * k + j;
+            const int64_t row = s_row[e];
+            if (row < 0) continue;
+            const float w = s_w[e];
+            const int64_t prow = s_prow[e];
+            const float pa = __fmul_rn(ax, fabsf(w));
+            const uint32_t am =
+                ((__float_as_uint(pa) & 0xFFFFu) == 0x8000u
+                     ? bf16_bits_rn(static_cast<double>(ax) * fabs(static_cast<double>(w)))
+                     : bf16x2_rn(pa, 0.f)) & 0x7FFFu;
+            uint8_t* s_dst = s + ((prow / kTile) * nkc + b / 4) * 512 +
+                             swz_word(static_cast<int>(prow % kTile)) + (b & 3);
+            uint8_t* q_dst = q + row * cols + b * 32;
+            // With the block scale 2^e known, w' = w 2^-e is exact while it is
+            // a normal fp32 number, and bf16(x w') = bf16(x w) 2^-e for every
+            // value that is BF16-normal; with e >= -116 a BF16-subnormal value
+            // scales below 2^-10 and quantizes to a signed zero either way.
+            // So the products x w' round straight to the scaled BF16 values.
+            const uint32_t byte = e8m0_byte(am, FLOOR);
+            const float ws = __fmul_rn(w, inv_scale(byte));
+            if (byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f) {
+                uint32_t v[16];
+                uint32_t mid = 0xFFFFFFFFu;
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], ws, mid);
+                if (weighted_tie(mid)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint4 x = weighted8_exact(
+                            make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), ws);
+                        v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
+                    }
+                }
+                uint32_t qv[8];
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    qv[kk] = cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk]), bf16_hi(v[2 * kk])) |
+                             (cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk + 1]), bf16_hi(v[2 * kk + 1])) << 16);
+                st32(q_dst, qv, v8);
+                *s_dst = static_cast<uint8_t>(byte);
+                continue;
+            }
+            uint32_t v[16];
+            uint32_t mid = 0xFFFFFFFFu;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], w, mid);
+            if (weighted_tie(mid)) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4 x = weighted8_exact(
+                        make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), w);
+                    v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
+                }
+            }
+            mx_block32_amax<FLOOR>(v, am, q_dst, s_dst, v8);
         }
     }
 }
@@ -578,6 +756,32 @@ cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t
         if (fl) MXFP8_WEIGHTED(true, false); else MXFP8_WEIGHTED(false, false);
     }
 #undef MXFP8_WEIGHTED
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weighted_quantize_tokens_mx(const WeightedTokensArgs& a, cudaStream_t st) {
+    const bool grouped = a.offsets != nullptr;
+    const bool fl = a.flags & MX_SCALE_FLOOR;
+    if (a.k < 1 || a.k > kMaxRoutes || (grouped && a.groups > kMaxGroupsTok)) return cudaErrorInvalidValue;
+    const int64_t nkc = (a.cols + kTile - 1) / kTile;
+    // padding scale bytes (rows past a group's end, blocks past cols) read 0:
+    // the token walk writes only the routed rows' blocks
+    cudaError_t e = cudaMemsetAsync(a.s, 0, a.scale_bytes, st);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = (a.tokens + kTokensPerCta - 1) / kTokensPerCta;
+    if (ctas == 0) return cudaSuccess;
+    if (ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const bool v8 = aligned32_host(a.dy) && a.ld % 16 == 0 && aligned32_host(a.q);
+#define MXFP8_WTOK(FL, GR)                                                                      \
+    weighted_quant_tokens_kernel<FL, GR><<<static_cast<unsigned>(ctas), kThreads, 0, st>>>(      \
+        a.dy, a.tokens, a.ld, a.k, a.token_rows, a.token_weights, a.rows, a.cols, a.offsets,     \
+        a.groups, a.q, a.s, nkc, v8)
+    if (grouped) {
+        if (fl) MXFP8_WTOK(true, true); else MXFP8_WTOK(false, true);
+    } else {
+        if (fl) MXFP8_WTOK(true, false); else MXFP8_WTOK(false, false);
+    }
+#undef MXFP8_WTOK
     return cudaGetLastError();
 }
 

@@ -97,7 +97,23 @@ struct WeightedQuantArgs {
     uint8_t* s;
 };
 
+struct WeightedTokensArgs {
+    const uint16_t* dy;  // tokens x cols, leading dimension ld
+    int64_t tokens, ld;
+    int k;                        // routes per token
+    const int32_t* token_rows;    // tokens x k dispatched rows (-1: none)
+    const float* token_weights;   // tokens x k
+    int64_t rows, cols;
+    const int32_t* offsets;
+    int32_t groups;
+    unsigned flags;
+    uint8_t* q;
+    uint8_t* s;
+    size_t scale_bytes;           // size of s (zeroed first)
+};
+
 cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_weighted_quantize_tokens_mx(const WeightedTokensArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t s);
 cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t s);
 // Test hook: the SwiGLU fast path's fp32 value per element.

@@ -437,3 +437,120 @@ def test_route_weight_quantize_full_size():
     """Combine backward of 32768 tokens x 2048, top-8 of 64 experts."""
     w = workloads.combine_backward(seed=0, device=device())
     assert _weighted_check(w["dY"], w["row_token"], w["row_weight"], offsets=w["offsets"]) == m.MXFP8_OK
+
+
+# --------------------------- route weighting + quantize, per-token form --
+
+def _tokens_check(dy, token_rows, token_weights, rows, offsets=None, floor=False):
+    """fp8_route_weight_quantize_mx_tokens against the oracle (through the
+    equivalent per-row routing) and against the per-row entry point."""
+    off_d = None if offsets is None else torch.from_numpy(offsets).to(device())
+    flags = m.MX_SCALE_FLOOR if floor else 0
+    q, s = m.fp8_route_weight_quantize_mx_tokens(
+        dy, torch.from_numpy(token_rows).to(device()), torch.from_numpy(token_weights).to(device()),
+        rows, offsets=off_d, flags=flags)
+    st = m.mxfp8_last_device_status()
+    row_token = np.full(rows, -1, np.int32)
+    row_weight = np.zeros(rows, np.float32)
+    t_idx, j_idx = np.nonzero((token_rows >= 0) & (token_rows < rows))
+    row_token[token_rows[t_idx, j_idx]] = t_idx
+    row_weight[token_rows[t_idx, j_idx]] = token_weights[t_idx, j_idx]
+    g = oracle.route_weight(workloads.bits(dy), row_token, row_weight)
+    fl = oracle.SCALE_FLOOR if floor else 0
+    if offsets is None:
+        want = oracle.quantize_mx(g, oracle.ROWWISE | fl)
+        q_exp, s_exp = want["q_row"], want["s_row"]
+    else:
+        q_exp, s_exp = oracle.quantize_mx_grouped(g, offsets, oracle.ROWWISE | fl)
+    assert np.array_equal(host(q), q_exp)
+    assert np.array_equal(host(s)[: s_exp.size], s_exp)
+    q2, s2 = m.fp8_route_weight_quantize_mx(dy, torch.from_numpy(row_token).to(device()),
+                                            torch.from_numpy(row_weight).to(device()), offsets=off_d,
+                                            flags=flags)
+    assert torch.equal(q, q2) and torch.equal(s[: s_exp.size], s2[: s_exp.size])
+    return st
+
+
+def _random_routing(tokens, k, rows, rng):
+    perm = rng.permutation(tokens * k)[:rows] if rows <= tokens * k else None
+    tr = np.full(tokens * k, -1, np.int64)
+    tr[perm] = np.arange(rows)  # slot perm[i] routes to dispatched row i
+    return tr.reshape(tokens, k).astype(np.int32), rng.uniform(0, 1, (tokens, k)).astype(np.float32)
+
+
+@pytest.mark.parametrize("tokens,k,cols", [(7, 1, 32), (50, 8, 224), (33, 3, 416), (130, 16, 96)])
+@pytest.mark.parametrize("floor", [False, True])
+def test_route_weight_tokens_plain(tokens, k, cols, floor):
+    rng = np.random.default_rng(tokens * 7 + k)
+    rows = tokens * k - (tokens // 3)  # some slots unused (-1)
+    tr, tw = _random_routing(tokens, k, rows, rng)
+    dy = to_dev_bf16(oracle.bf16_round(rng.standard_normal((tokens, cols)) *
+                                       np.exp(rng.uniform(-25, 5, (tokens, 1)))))
+    assert _tokens_check(dy, tr, tw, rows, floor=floor) == m.MXFP8_OK
+
+
+@pytest.mark.parametrize("counts", GROUP_COUNTS)
+def test_route_weight_tokens_grouped(counts):
+    off = _offsets(counts)
+    rows = int(off[-1])
+    k = 4
+    tokens = (rows + k - 1) // k + 1
+    rng = np.random.default_rng(rows + 5)
+    tr, tw = _random_routing(tokens, k, rows, rng)
+    dy = to_dev_bf16(oracle.bf16_round(rng.standard_normal((tokens, 224)) * 1e-3))
+    assert _tokens_check(dy, tr, tw, rows, offsets=off) == m.MXFP8_OK
+
+
+def test_route_weight_tokens_ties_and_bad_row():
+    """The 32 constructed double-rounding cases (fp32 product on a BF16
+    midpoint, exact product off it) through the per-token form, plus a
+    slot naming a row past the end (recorded, skipped)."""
+    pairs = _fp32_midpoint_pairs(32, 23)
+    cols, k = 64, 2
+    tokens = len(pairs)
+    rng = np.random.default_rng(25)
+    dy = np.zeros((tokens, cols), np.uint16)
+    for i, (xb, _) in enumerate(pairs):
+        dy[i] = oracle.bf16_round(rng.uniform(0.5, 1.0, cols))
+        dy[i, i % cols] = xb
+    rows = tokens  # slot 0 of token i -> row i; slot 1 unused
+    tr = np.full((tokens, k), -1, np.int32)
+    tr[:, 0] = np.arange(tokens)
+    tw = np.zeros((tokens, k), np.float32)
+    tw[:, 0] = [w for _, w in pairs]
+    assert _tokens_check(to_dev_bf16(dy), tr, tw, rows) == m.MXFP8_OK
+    tr[3, 1] = rows + 5
+    assert _tokens_check(to_dev_bf16(dy), tr, tw, rows) == m.MXFP8_ERR_DEVICE_CHECK
+
+
+def test_route_weight_tokens_full_size():
+    """Combine backward of 32768 tokens x 2048, top-8 of 64 experts, routing
+    given per token."""
+    w = workloads.combine_backward(seed=0, device=device())
+    rows = w["token_rows"].size
+    assert _tokens_check(w["dY"], w["token_rows"], w["token_weights"], rows,
+                         offsets=w["offsets"]) == m.MXFP8_OK
+
+
+def test_route_weight_tokens_extremes():
+    """The per-token form on blocks that mix BF16-subnormal products with a
+    block maximum near 2^-100 (the scale folded into the weight still gives
+    their signed zeros), products at the top of the range, subnormal and
+    largest BF16 inputs, weights of 2^-30, 2^-126 and 0, and exact-product
+    ties."""
+    rng = np.random.default_rng(26)
+    tokens, cols, k = 24, 96, 3
+    mag = np.exp(rng.uniform(-80, 80, (tokens, 1)))
+    dy = oracle.bf16_round(rng.standard_normal((tokens, cols)) * mag)
+    dy[0, :8] = [0x3F80, 0xBF80, 0x0001, 0x8001, 0x7F7F, 0x0080, 0x3F81, 0x0000]
+    # row 1: a block spanning 2^-131 .. 2^-100 (BF16 subnormals beside a normal maximum)
+    dy[1, :32] = oracle.bf16_round(np.ldexp(rng.uniform(1, 2, 32), rng.integers(-131, -100, 32)) *
+                                   rng.choice([-1, 1], 32))
+    dy[2, :32] = oracle.bf16_round(np.ldexp(rng.uniform(1, 2, 32), rng.integers(-140, -118, 32)))
+    rows = tokens * k
+    tr = np.arange(rows, dtype=np.int32).reshape(tokens, k)
+    tw = rng.uniform(0, 1, (tokens, k)).astype(np.float32)
+    tw[0] = [1 + 2.0 ** -8, 2.0 ** -30, 2.0 ** -126]
+    tw[1] = [1.0, 0.75, 2.0 ** -20]
+    tw[2] = [0.0, 1.5, 1 + 3 * 2.0 ** -8]
+    assert _tokens_check(to_dev_bf16(dy), tr, tw, rows) == m.MXFP8_OK

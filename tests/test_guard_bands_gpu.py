@@ -193,3 +193,38 @@ def test_grouped_gemm_and_routed_conversions():
     o = {"q": Guarded((total, 160)), "s": Guarded(m.mxfp8_grouped_scale_bytes(total, 160, G))}
     m.fp8_route_weight_quantize_mx(dy, tok, wt, offsets=off_d, q=o["q"].t, s=o["s"].t)
     check_all(o, "route weight quantize grouped")
+
+
+def test_gemm_pair():
+    """Two GEMMs in one launch, both C with a wider row stride."""
+    shapes = [((200, 136, 96), 144), ((300, 512, 384), 520)]
+    gs, guards = [], {}
+    for i, ((M, N, K), ldc) in enumerate(shapes):
+        a = m.fp8_quantize_mx(to_dev_bf16(bits((M, K), 30 + i)), m.MX_ROWWISE)
+        b = m.fp8_quantize_mx(to_dev_bf16(bits((N, K), 40 + i)), m.MX_ROWWISE)
+        c = Guarded((M, N), torch.bfloat16, ld=ldc)
+        guards[f"C{i}"] = c
+        gs.append(dict(a=a["q_row"], a_scale=a["s_row"], b=b["q_row"], b_scale=b["s_row"], c=c.t))
+    m.fp8_scaled_gemm_pair(m.GEMM_MX, gs[0], gs[1])
+    check_all(guards, "gemm pair")
+
+
+def test_route_weight_tokens_grouped():
+    """The per-token route weighting: payload rows and the (zeroed first)
+    group-padded scale array, with ragged groups and unused route slots."""
+    counts = [40, 0, 300, 129, 1]
+    G = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    off_d = torch.from_numpy(off).to(device())
+    rows, k, cols = int(off[-1]), 4, 160
+    tokens = rows // k + 3
+    rng = np.random.default_rng(10)
+    slots = rng.permutation(tokens * k)[:rows]
+    tr = np.full(tokens * k, -1, np.int32)
+    tr[slots] = np.arange(rows)
+    dy = to_dev_bf16(bits((tokens, cols), 11))
+    tw = torch.from_numpy(rng.random((tokens, k)).astype(np.float32)).to(device())
+    o = {"q": Guarded((rows, cols)), "s": Guarded(m.mxfp8_grouped_scale_bytes(rows, cols, G))}
+    m.fp8_route_weight_quantize_mx_tokens(dy, torch.from_numpy(tr.reshape(tokens, k)).to(device()), tw,
+                                          rows, offsets=off_d, q=o["q"].t, s=o["s"].t)
+    check_all(o, "route weight quantize per token")

@@ -150,7 +150,9 @@ def swiglu_hidden(seed=0, device="cpu", tokens=32768, top_k=8, experts=64, ffn=1
 
 def routing(seed=0, tokens=32768, top_k=8, experts=64, zipf_s=1.1):
     """Token -> expert assignments (top_k distinct experts per token, Gumbel
-    top-k on log p_e) sorted by expert then token, with softmax route weights."""
+    top-k on log p_e) sorted by expert then token, with softmax route weights;
+    token_rows / token_weights give the same routing per token (the
+    dispatched row and weight of each of its top_k slots)."""
     rng = np.random.Generator(np.random.PCG64(_stream(seed, 5)))
     logp = -zipf_s * np.log(np.arange(1, experts + 1, dtype=np.float64))
     keys = logp[None, :] + rng.gumbel(size=(tokens, experts))
@@ -162,8 +164,13 @@ def routing(seed=0, tokens=32768, top_k=8, experts=64, zipf_s=1.1):
     exp_ = chosen.reshape(-1)
     order = np.lexsort((tok, exp_))
     counts = np.bincount(exp_, minlength=experts).astype(np.int64)
+    # the same routing from the token side: dispatched row of (token, slot)
+    inv = np.empty(order.size, np.int64)
+    inv[order] = np.arange(order.size)
     return {"row_token": tok[order].astype(np.int32),
             "row_weight": w.reshape(-1)[order].astype(np.float32),
+            "token_rows": inv.reshape(tokens, top_k).astype(np.int32),
+            "token_weights": w.astype(np.float32),
             "counts": counts, "offsets": offsets_from_counts(counts)}
 
 
