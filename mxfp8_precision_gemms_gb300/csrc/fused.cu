@@ -445,6 +445,64 @@ __device__ __noinline__ uint4 weighted8_exact(uint4 x8, float w) {
     return v;
 }
 
+// One weighted block: bf16_RNE(w x) of the 32 BF16 values in xw (rounded
+// once from the exact products), MX-quantized into q_dst (32 bytes, skipped
+// when null) and *s_dst; ax is max |x| over the block as fp32 (the BF16
+// maximum, NaN or Inf as they are).  The block maximum of the weighted values
+// is the correctly rounded |ax w|: the rounding is monotone, so one product
+// replaces the maximum over the 32 weighted values.
+template <bool FLOOR>
+__device__ __forceinline__ void weighted_block_quant(const uint32_t* xw, float ax, float w,
+                                                     uint8_t* q_dst, uint8_t* s_dst, bool v8) {
+    const float pa = __fmul_rn(ax, fabsf(w));
+    const uint32_t am =
+        ((__float_as_uint(pa) & 0xFFFFu) == 0x8000u
+             ? bf16_bits_rn(static_cast<double>(ax) * fabs(static_cast<double>(w)))
+             : bf16x2_rn(pa, 0.f)) & 0x7FFFu;
+    // With the block scale 2^e known, w' = w 2^-e is exact while it is
+    // a normal fp32 number, and bf16(x w') = bf16(x w) 2^-e for every
+    // value that is BF16-normal; with e >= -116 a BF16-subnormal value
+    // scales below 2^-10 and quantizes to a signed zero either way.
+    // So the products x w' round straight to the scaled BF16 values.
+    const uint32_t byte = e8m0_byte(am, FLOOR);
+    const float ws = __fmul_rn(w, inv_scale(byte));
+    if (byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f) {
+        uint32_t v[16];
+        uint32_t mid = 0xFFFFFFFFu;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], ws, mid);
+        if (weighted_tie(mid)) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint4 x = weighted8_exact(
+                    make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), ws);
+                v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
+            }
+        }
+        uint32_t qv[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            qv[kk] = cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk]), bf16_hi(v[2 * kk])) |
+                     (cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk + 1]), bf16_hi(v[2 * kk + 1])) << 16);
+        if (q_dst != nullptr) st32(q_dst, qv, v8);
+        *s_dst = static_cast<uint8_t>(byte);
+        return;
+    }
+    uint32_t v[16];
+    uint32_t mid = 0xFFFFFFFFu;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], w, mid);
+    if (weighted_tie(mid)) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint4 x = weighted8_exact(
+                make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), w);
+            v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
+        }
+    }
+    mx_block32_amax<FLOOR>(v, am, q_dst, s_dst, v8);
+}
+
 // Launch-bounded to 64 registers (four CTAs per SM): 252.6 against 273 us
 // at the default three CTAs on the 262144 x 2048 combine-backward workload.
 template <bool FLOOR, bool GROUPED>
@@ -629,56 +687,9 @@ __global__ void __launch_bounds__(kThreads, 4)
             if (row < 0) continue;
             const float w = s_w[e];
             const int64_t prow = s_prow[e];
-            const float pa = __fmul_rn(ax, fabsf(w));
-            const uint32_t am =
-                ((__float_as_uint(pa) & 0xFFFFu) == 0x8000u
-                     ? bf16_bits_rn(static_cast<double>(ax) * fabs(static_cast<double>(w)))
-                     : bf16x2_rn(pa, 0.f)) & 0x7FFFu;
             uint8_t* s_dst = s + ((prow / kTile) * nkc + b / 4) * 512 +
                              swz_word(static_cast<int>(prow % kTile)) + (b & 3);
-            uint8_t* q_dst = q + row * cols + b * 32;
-            // With the block scale 2^e known, w' = w 2^-e is exact while it is
-            // a normal fp32 number, and bf16(x w') = bf16(x w) 2^-e for every
-            // value that is BF16-normal; with e >= -116 a BF16-subnormal value
-            // scales below 2^-10 and quantizes to a signed zero either way.
-            // So the products x w' round straight to the scaled BF16 values.
-            const uint32_t byte = e8m0_byte(am, FLOOR);
-            const float ws = __fmul_rn(w, inv_scale(byte));
-            if (byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f) {
-                uint32_t v[16];
-                uint32_t mid = 0xFFFFFFFFu;
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], ws, mid);
-                if (weighted_tie(mid)) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint4 x = weighted8_exact(
-                            make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), ws);
-                        v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
-                    }
-                }
-                uint32_t qv[8];
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    qv[kk] = cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk]), bf16_hi(v[2 * kk])) |
-                             (cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk + 1]), bf16_hi(v[2 * kk + 1])) << 16);
-                st32(q_dst, qv, v8);
-                *s_dst = static_cast<uint8_t>(byte);
-                continue;
-            }
-            uint32_t v[16];
-            uint32_t mid = 0xFFFFFFFFu;
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], w, mid);
-            if (weighted_tie(mid)) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint4 x = weighted8_exact(
-                        make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), w);
-                    v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
-                }
-            }
-            mx_block32_amax<FLOOR>(v, am, q_dst, s_dst, v8);
+            weighted_block_quant<FLOOR>(xw, ax, w, q + row * cols + b * 32, s_dst, v8);
         }
     }
 }
