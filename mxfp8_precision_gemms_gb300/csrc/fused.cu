@@ -594,20 +594,44 @@ __global__ void __launch_bounds__(kThreads, 4)
     __shared__ int64_t s_pstart[GROUPED ? kMaxGroupsTok + 1 : 1];
     __shared__ int s_ok;
     const int tid = threadIdx.x;
+    const int64_t nb = cols / 32;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerCta;
+    const int nt = static_cast<int>(min(static_cast<int64_t>(kTokensPerCta), tokens - t0));
+    // this thread's route entry (kTokensPerCta * kMaxRoutes == blockDim.x:
+    // one at most) and its first (token, block) item's dY go out together
+    static_assert(kTokensPerCta * kMaxRoutes == kThreads, "one route entry per thread");
+    const bool has_route = tid < nt * k;
+    int32_t r = -1;
+    float wr = 0.f;
+    if (has_route) {
+        const int64_t idx = (t0 + tid / k) * k + tid % k;
+        r = __ldg(token_rows + idx);
+        wr = __ldg(token_weights + idx);
+    }
+    uint32_t xw[16];
+    int64_t pi = tid;
+    if (pi < nt * nb) {
+        const int tl = static_cast<int>(pi / nb);
+        const uint16_t* src = dy + (t0 + tl) * ld + (pi - tl * nb) * 32;
+        ld32_stream(src, xw, v8);
+        ld32_stream(src + 16, xw + 8, v8);
+    }
     if constexpr (GROUPED) {
-        // offsets into shared memory (validated: 0 first, non-decreasing,
-        // rows last) and the padded first scale row of every group
+        // offsets into shared memory (the whole CTA loads them at once),
+        // validated (0 first, non-decreasing, rows last), and the padded
+        // first scale row of every group (warp 0 scans them)
+        for (int g = tid; g <= groups; g += blockDim.x) s_off[g] = offsets[g];
+        __syncthreads();
         if (tid < 32) {
-            bool ok = offsets[0] == 0 && static_cast<int64_t>(offsets[groups]) == rows;
+            bool ok = s_off[0] == 0 && static_cast<int64_t>(s_off[groups]) == rows;
             int64_t base = 0;
             for (int g0 = 0; g0 <= groups; g0 += 32) {
                 const int g = g0 + tid;
                 int64_t tiles = 0;
-                if (g <= groups) s_off[g] = offsets[g];
                 if (g < groups) {
-                    const int32_t b = offsets[g], e = offsets[g + 1];
-                    if (e < b) ok = false;
-                    tiles = e > b ? (e - b + kTile - 1) / kTile : 0;
+                    const int32_t gb = s_off[g], ge = s_off[g + 1];
+                    if (ge < gb) ok = false;
+                    tiles = ge > gb ? (ge - gb + kTile - 1) / kTile : 0;
                 }
                 int64_t incl = tiles;
 #pragma unroll
@@ -627,30 +651,14 @@ __global__ void __launch_bounds__(kThreads, 4)
             return;
         }
     }
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerCta;
-    const int nt = static_cast<int>(min(static_cast<int64_t>(kTokensPerCta), tokens - t0));
-    const int64_t nb = cols / 32;
-    // the first (token, block) item's dY loads go out before the route table
-    // is built, so the two latencies overlap
-    uint32_t xw[16];
-    int64_t pi = tid;
-    if (pi < nt * nb) {
-        const int tl = static_cast<int>(pi / nb);
-        const uint16_t* src = dy + (t0 + tl) * ld + (pi - tl * nb) * 32;
-        ld32_stream(src, xw, v8);
-        ld32_stream(src + 16, xw + 8, v8);
-    }
-    bool bad = false;
-    for (int e = tid; e < nt * k; e += blockDim.x) {
-        const int64_t idx = (t0 + e / k) * k + e % k;
-        const int32_t r = __ldg(token_rows + idx);
+    if (has_route) {
         int64_t row = -1, prow = -1;
         float w = 0.f;
         if (r >= rows) {
-            bad = true;
+            record_status(MXFP8_ERR_DEVICE_CHECK);
         } else if (r >= 0) {
             row = r;
-            w = __ldg(token_weights + idx);
+            w = wr;
             if constexpr (GROUPED) {
                 int lo = 0, hi = groups - 1;  // the last group starting at or before r
                 while (lo < hi) {
@@ -662,11 +670,10 @@ __global__ void __launch_bounds__(kThreads, 4)
                 prow = r;
             }
         }
-        s_row[e] = row;
-        s_prow[e] = prow;
-        s_w[e] = w;
+        s_row[tid] = row;
+        s_prow[tid] = prow;
+        s_w[tid] = w;
     }
-    if (bad) record_status(MXFP8_ERR_DEVICE_CHECK);
     __syncthreads();
     for (; pi < nt * nb; pi += blockDim.x) {
         const int tl = static_cast<int>(pi / nb);
