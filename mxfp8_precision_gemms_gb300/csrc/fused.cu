@@ -20,6 +20,7 @@
 
 #include "internal.h"
 #include "mx_common.cuh"
+#include "ptx.cuh"
 #include "swiglu_round.cuh"
 
 namespace mxfp8 {
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kThreads)
     dequantize_mx_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                          int64_t rows, int64_t cols, const int32_t* offsets, int groups,
                          uint16_t* __restrict__ out, int64_t ldo, int64_t nkc, bool v8) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -357,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     swiglu_quant_kernel(const uint16_t* __restrict__ h, int64_t rows, int64_t f, int64_t ld,
                         const int32_t* offsets, int groups, uint8_t* __restrict__ q,
                         uint8_t* __restrict__ s, int64_t nkc, bool v8) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -512,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                           int64_t rows, int64_t cols, const int32_t* offsets, int groups,
                           uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
                           bool v8) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -587,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                                  int64_t cols, const int32_t* offsets, int groups,
                                  uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
                                  bool v8) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     __shared__ int64_t s_row[kTokensPerCta * kMaxRoutes];   // dispatched row, -1: none
     __shared__ int64_t s_prow[kTokensPerCta * kMaxRoutes];  // its row in the scale array
     __shared__ float s_w[kTokensPerCta * kMaxRoutes];

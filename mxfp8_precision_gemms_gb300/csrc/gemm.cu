@@ -268,6 +268,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tm_a, const CUtenso
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // Launched with programmatic stream serialization: everything above
+    // touches only shared memory; from here on the kernel reads what the
+    // kernels before it wrote (operands, scales, offsets, per-tensor scales).
+    griddep_wait();
     if constexpr (GROUPED) {
         // Validate the offsets; prefix sums of 128-row tiles and of units of
         // CG tiles per expert group.
@@ -761,7 +765,7 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C::CG;
     attr[0].val.clusterDim.y = 1;
@@ -769,8 +773,12 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    // the kernel may start while the previous kernel on the stream finishes
+    // (it waits for that kernel's results after its prologue)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     int max_clusters = resident[dev].load(std::memory_order_relaxed);
     if (max_clusters <= 0) {
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -947,7 +955,7 @@ cudaError_t launch_dual(const Prepared& d0, const Prepared& d1, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C::CG;
     attr[0].val.clusterDim.y = 1;
@@ -955,8 +963,12 @@ cudaError_t launch_dual(const Prepared& d0, const Prepared& d1, cudaStream_t s) 
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    // the kernel may start while the previous kernel on the stream finishes
+    // (it waits for that kernel's results after its prologue)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     int max_clusters = resident[dev].load(std::memory_order_relaxed);
     if (max_clusters <= 0) {
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

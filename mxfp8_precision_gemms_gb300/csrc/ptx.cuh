@@ -18,6 +18,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it on the stream is still running; griddep_wait blocks
+// until that kernel has completed and its memory writes are visible, so a
+// kernel calls it before its first global memory access.  A kernel calls
+// griddep_launch_dependents to let the kernel after it start early (its
+// own results are still only visible to that kernel after its wait).
+// Without a programmatic dependency both are no-ops.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -36,6 +36,7 @@ __device__ __forceinline__ void record_status(unsigned code) {
 template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_kernel(QuantMxArgs a, int64_t nkc_row, int64_t nkc_col) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     __shared__ __align__(16) uint32_t tile[COL ? kTile * kTile / 2 : 4];
     __shared__ __align__(16) uint8_t col_scales[COL ? kTile * 4 : 16];
     __shared__ int64_t s_rows[2];
@@ -184,6 +185,7 @@ __device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t
 template <bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_row_kernel(QuantMxArgs a, int64_t nkc, bool v8) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     __shared__ int64_t s_rows[2];
     __shared__ int s_ok;
     const int tid = threadIdx.x;
@@ -224,6 +226,7 @@ struct MxRowBatch {
 template <bool FLOOR>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_row_batch_kernel(const __grid_constant__ MxRowBatch b) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     const int64_t blk = blockIdx.x;
     int t = 0;
     while (t + 1 < b.count && blk >= b.tile_end[t]) ++t;
@@ -372,6 +375,7 @@ __device__ __forceinline__ bool tile_quantize(const CUtensorMap* map, const Tile
 template <bool FLOOR>
 __global__ void __launch_bounds__(kTileThreads)
     quantize_mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, TileArgs a, uint64_t limit_ns) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     extern __shared__ uint8_t tile_raw[];
     __shared__ __align__(8) uint64_t bar;
     uint8_t* tile = reinterpret_cast<uint8_t*>(
@@ -400,6 +404,7 @@ struct MxTileBatch {
 template <bool FLOOR>
 __global__ void __launch_bounds__(kTileThreads)
     quantize_mx_tile_batch_kernel(const __grid_constant__ MxTileBatch b, uint64_t limit_ns) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     extern __shared__ uint8_t tile_raw[];
     __shared__ __align__(8) uint64_t bar;
     uint8_t* tile = reinterpret_cast<uint8_t*>(
@@ -459,6 +464,7 @@ template <int FMT>
 __global__ void __launch_bounds__(256)
     tensor_cast_kernel(const uint16_t* __restrict__ x, int64_t n, const unsigned* amax_bits,
                        float* scale_out, uint8_t* __restrict__ q) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     const float amax = __uint_as_float(*amax_bits);
     const float fmax = FMT == FP8_E4M3 ? 448.0f : 57344.0f;
     const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
@@ -576,6 +582,7 @@ __device__ __forceinline__ void cast_share(const uint16_t* __restrict__ x, uint8
 template <int FMT>
 __global__ void __launch_bounds__(kFusedThreads)
     tensor_quant_batch_kernel(const TensorBatch b, uint32_t* ws, uint64_t limit_ns) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     __shared__ uint32_t red[kMaxBatch][kFusedThreads / 32];
     __shared__ int s_ok;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -675,6 +682,7 @@ __global__ void __launch_bounds__(256)
     tensor_cast_scaled_kernel(const uint16_t* __restrict__ x, int64_t n, const float* scale,
                               uint8_t* __restrict__ q, unsigned* amax_bits,
                               unsigned long long* sat) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     const float s = *scale;
     const int64_t n8 = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -760,6 +768,7 @@ template <int FIN, int FOUT>
 __global__ void __launch_bounds__(256)
     requantize_kernel(const uint8_t* __restrict__ q_in, int64_t n, const float* s_in_p,
                       const float* s_out_p, uint8_t* __restrict__ q_out, unsigned long long* sat) {
+    griddep_launch_dependents();  // a dependent GEMM may launch now
     __shared__ uint32_t lut[256];  // one output code per input code, widened to 32 bits
     {
         const float s_in = *s_in_p, s_out = *s_out_p;
