@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kThreads)
                          int64_t rows, int64_t cols, const int32_t* offsets, int groups,
                          uint16_t* __restrict__ out, int64_t ldo, int64_t nkc, bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                         const int32_t* offsets, int groups, uint8_t* __restrict__ q,
                         uint8_t* __restrict__ s, int64_t nkc, bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -516,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                           uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
                           bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     int64_t row_begin, row_end;
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
@@ -592,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                                  uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t nkc,
                                  bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     __shared__ int64_t s_row[kTokensPerCta * kMaxRoutes];   // dispatched row, -1: none
     __shared__ int64_t s_prow[kTokensPerCta * kMaxRoutes];  // its row in the scale array
     __shared__ float s_w[kTokensPerCta * kMaxRoutes];
@@ -729,14 +733,11 @@ cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t st) {
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
     const bool v8 = aligned32_host(a.q) && aligned32_host(a.out) && a.ldo % 16 == 0;
-    if (grouped) {
-        dequantize_mx_kernel<true><<<grid, kThreads, 0, st>>>(a.q, a.s, a.rows, a.cols, a.offsets,
-                                                             a.groups, a.out, a.ldo, nkc, v8);
-    } else {
-        dequantize_mx_kernel<false><<<grid, kThreads, 0, st>>>(a.q, a.s, a.rows, a.cols, nullptr, 0,
-                                                              a.out, a.ldo, nkc, v8);
-    }
-    return cudaGetLastError();
+    if (grouped)
+        return launch_pdl(dequantize_mx_kernel<true>, grid, dim3(kThreads), 0, st, a.q, a.s, a.rows,
+                          a.cols, a.offsets, a.groups, a.out, a.ldo, nkc, v8);
+    return launch_pdl(dequantize_mx_kernel<false>, grid, dim3(kThreads), 0, st, a.q, a.s, a.rows,
+                      a.cols, nullptr, 0, a.out, a.ldo, nkc, v8);
 }
 
 cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t st) {
@@ -748,16 +749,17 @@ cudaError_t launch_swiglu_quantize_mx(const SwigluQuantArgs& a, cudaStream_t st)
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.f + kTile - 1) / kTile;
     const bool v8 = aligned32_host(a.h) && a.ld % 16 == 0 && a.f % 16 == 0 && aligned32_host(a.q);
-#define MXFP8_SWIGLU(FL, GR) \
-    swiglu_quant_kernel<FL, GR><<<grid, kThreads, 0, st>>>(a.h, a.rows, a.f, a.ld, a.offsets, \
-                                                            a.groups, a.q, a.s, nkc, v8)
+#define MXFP8_SWIGLU(FL, GR)                                                                   \
+    launch_pdl(swiglu_quant_kernel<FL, GR>, grid, dim3(kThreads), 0, st, a.h, a.rows, a.f, a.ld, \
+               a.offsets, a.groups, a.q, a.s, nkc, v8)
+    cudaError_t e;
     if (grouped) {
-        if (fl) MXFP8_SWIGLU(true, true); else MXFP8_SWIGLU(false, true);
+        e = fl ? MXFP8_SWIGLU(true, true) : MXFP8_SWIGLU(false, true);
     } else {
-        if (fl) MXFP8_SWIGLU(true, false); else MXFP8_SWIGLU(false, false);
+        e = fl ? MXFP8_SWIGLU(true, false) : MXFP8_SWIGLU(false, false);
     }
 #undef MXFP8_SWIGLU
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t st) {
@@ -769,17 +771,17 @@ cudaError_t launch_weighted_quantize_mx(const WeightedQuantArgs& a, cudaStream_t
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
     const bool v8 = aligned32_host(a.dy) && a.ld % 16 == 0 && aligned32_host(a.q);
-#define MXFP8_WEIGHTED(FL, GR)                                                               \
-    weighted_quant_kernel<FL, GR><<<grid, kThreads, 0, st>>>(                                \
-        a.dy, a.tokens, a.ld, a.row_token, a.row_weight, a.rows, a.cols, a.offsets, a.groups, \
-        a.q, a.s, nkc, v8)
+#define MXFP8_WEIGHTED(FL, GR)                                                                \
+    launch_pdl(weighted_quant_kernel<FL, GR>, grid, dim3(kThreads), 0, st, a.dy, a.tokens, a.ld, \
+               a.row_token, a.row_weight, a.rows, a.cols, a.offsets, a.groups, a.q, a.s, nkc, v8)
+    cudaError_t e;
     if (grouped) {
-        if (fl) MXFP8_WEIGHTED(true, true); else MXFP8_WEIGHTED(false, true);
+        e = fl ? MXFP8_WEIGHTED(true, true) : MXFP8_WEIGHTED(false, true);
     } else {
-        if (fl) MXFP8_WEIGHTED(true, false); else MXFP8_WEIGHTED(false, false);
+        e = fl ? MXFP8_WEIGHTED(true, false) : MXFP8_WEIGHTED(false, false);
     }
 #undef MXFP8_WEIGHTED
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_weighted_quantize_tokens_mx(const WeightedTokensArgs& a, cudaStream_t st) {

@@ -37,6 +37,7 @@ template <bool ROW, bool COL, bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_kernel(QuantMxArgs a, int64_t nkc_row, int64_t nkc_col) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     __shared__ __align__(16) uint32_t tile[COL ? kTile * kTile / 2 : 4];
     __shared__ __align__(16) uint8_t col_scales[COL ? kTile * 4 : 16];
     __shared__ int64_t s_rows[2];
@@ -186,6 +187,7 @@ template <bool FLOOR, bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_row_kernel(QuantMxArgs a, int64_t nkc, bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     __shared__ int64_t s_rows[2];
     __shared__ int s_ok;
     const int tid = threadIdx.x;
@@ -227,6 +229,7 @@ template <bool FLOOR>
 __global__ void __launch_bounds__(kThreads)
     quantize_mx_row_batch_kernel(const __grid_constant__ MxRowBatch b) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     const int64_t blk = blockIdx.x;
     int t = 0;
     while (t + 1 < b.count && blk >= b.tile_end[t]) ++t;
@@ -376,6 +379,7 @@ template <bool FLOOR>
 __global__ void __launch_bounds__(kTileThreads)
     quantize_mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, TileArgs a, uint64_t limit_ns) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     extern __shared__ uint8_t tile_raw[];
     __shared__ __align__(8) uint64_t bar;
     uint8_t* tile = reinterpret_cast<uint8_t*>(
@@ -405,6 +409,7 @@ template <bool FLOOR>
 __global__ void __launch_bounds__(kTileThreads)
     quantize_mx_tile_batch_kernel(const __grid_constant__ MxTileBatch b, uint64_t limit_ns) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     extern __shared__ uint8_t tile_raw[];
     __shared__ __align__(8) uint64_t bar;
     uint8_t* tile = reinterpret_cast<uint8_t*>(
@@ -465,6 +470,7 @@ __global__ void __launch_bounds__(256)
     tensor_cast_kernel(const uint16_t* __restrict__ x, int64_t n, const unsigned* amax_bits,
                        float* scale_out, uint8_t* __restrict__ q) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     const float amax = __uint_as_float(*amax_bits);
     const float fmax = FMT == FP8_E4M3 ? 448.0f : 57344.0f;
     const float s = __fdiv_rn(fmax, amax > 1e-12f ? amax : 1e-12f);
@@ -583,6 +589,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kFusedThreads)
     tensor_quant_batch_kernel(const TensorBatch b, uint32_t* ws, uint64_t limit_ns) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     __shared__ uint32_t red[kMaxBatch][kFusedThreads / 32];
     __shared__ int s_ok;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -683,6 +690,7 @@ __global__ void __launch_bounds__(256)
                               uint8_t* __restrict__ q, unsigned* amax_bits,
                               unsigned long long* sat) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     const float s = *scale;
     const int64_t n8 = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -769,6 +777,7 @@ __global__ void __launch_bounds__(256)
     requantize_kernel(const uint8_t* __restrict__ q_in, int64_t n, const float* s_in_p,
                       const float* s_out_p, uint8_t* __restrict__ q_out, unsigned long long* sat) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
+    griddep_wait();               // the previous kernel's results are visible
     __shared__ uint32_t lut[256];  // one output code per input code, widened to 32 bits
     {
         const float s_in = *s_in_p, s_out = *s_out_p;
@@ -837,11 +846,11 @@ cudaError_t launch_mx(const QuantMxArgs& a, int64_t row_tiles, cudaStream_t s) {
         // 256-bit accesses when every block start is 32-byte aligned
         const bool v8 = (reinterpret_cast<uintptr_t>(a.x) % 32 == 0) && (a.ld % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(a.q_row) % 32 == 0);
-        quantize_mx_row_kernel<FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, v8);
-    } else {
-        quantize_mx_kernel<ROW, COL, FLOOR, GROUPED><<<grid, kThreads, 0, s>>>(a, nkc_row, nkc_col);
+        return launch_pdl(quantize_mx_row_kernel<FLOOR, GROUPED>, grid, dim3(kThreads), 0, s, a,
+                          nkc_row, v8);
     }
-    return cudaGetLastError();
+    return launch_pdl(quantize_mx_kernel<ROW, COL, FLOOR, GROUPED>, grid, dim3(kThreads), 0, s, a,
+                      nkc_row, nkc_col);
 }
 
 }  // namespace
@@ -874,12 +883,9 @@ cudaError_t launch_quantize_mx_rows_batch(int count, const QuantMxArgs* a, cudaS
     if (n == 0) return cudaSuccess;
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     b.count = n;
-    if (floor) {
-        quantize_mx_row_batch_kernel<true><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(b);
-    } else {
-        quantize_mx_row_batch_kernel<false><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(b);
-    }
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(tiles));
+    return floor ? launch_pdl(quantize_mx_row_batch_kernel<true>, grid, dim3(kThreads), 0, s, b)
+                 : launch_pdl(quantize_mx_row_batch_kernel<false>, grid, dim3(kThreads), 0, s, b);
 }
 
 // The tile kernels' view of a tensor; false when its TMA map cannot be made.
@@ -909,12 +915,12 @@ bool tile_args(const QuantMxArgs& a, CUtensorMap* map, TileArgs* t) {
 cudaError_t launch_mx_tile(const QuantMxArgs& a, const CUtensorMap& map, const TileArgs& t,
                            cudaStream_t s) {
     dim3 grid(static_cast<unsigned>(t.nkc_col), static_cast<unsigned>(t.nkc_row));
-    if (a.flags & MX_SCALE_FLOOR) {
-        quantize_mx_tile_kernel<true><<<grid, kTileThreads, kTileSmem + 1024, s>>>(map, t, wait_limit_ns());
-    } else {
-        quantize_mx_tile_kernel<false><<<grid, kTileThreads, kTileSmem + 1024, s>>>(map, t, wait_limit_ns());
-    }
-    return cudaGetLastError();
+    const uint64_t limit = wait_limit_ns();
+    return (a.flags & MX_SCALE_FLOOR)
+               ? launch_pdl(quantize_mx_tile_kernel<true>, grid, dim3(kTileThreads), kTileSmem + 1024, s,
+                            map, t, limit)
+               : launch_pdl(quantize_mx_tile_kernel<false>, grid, dim3(kTileThreads), kTileSmem + 1024, s,
+                            map, t, limit);
 }
 
 cudaError_t launch_quantize_mx(const QuantMxArgs& a, cudaStream_t s) {
@@ -948,15 +954,16 @@ cudaError_t launch_quantize_mx_cols_batch(int count, const QuantMxArgs* a, cudaS
     auto flush = [&]() -> cudaError_t {
         if (n == 0) return cudaSuccess;
         b.count = n;
-        const unsigned grid = static_cast<unsigned>(tiles);
-        if (floor) {
-            quantize_mx_tile_batch_kernel<true><<<grid, kTileThreads, kTileSmem + 1024, s>>>(b, wait_limit_ns());
-        } else {
-            quantize_mx_tile_batch_kernel<false><<<grid, kTileThreads, kTileSmem + 1024, s>>>(b, wait_limit_ns());
-        }
+        const dim3 grid(static_cast<unsigned>(tiles));
+        const uint64_t limit = wait_limit_ns();
+        const cudaError_t r =
+            floor ? launch_pdl(quantize_mx_tile_batch_kernel<true>, grid, dim3(kTileThreads),
+                               kTileSmem + 1024, s, b, limit)
+                  : launch_pdl(quantize_mx_tile_batch_kernel<false>, grid, dim3(kTileThreads),
+                               kTileSmem + 1024, s, b, limit);
         n = 0;
         tiles = 0;
-        return cudaGetLastError();
+        return r;
     };
     for (int t = 0; t < count && e == cudaSuccess; ++t) {
         if (a[t].rows <= 0 || a[t].cols <= 0) continue;
