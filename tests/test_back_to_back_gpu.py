@@ -116,3 +116,42 @@ def test_grouped_pairs_reuse_one_operand_buffer():
         alone.append(m.fp8_grouped_gemm(qi, si, qw, sw, off))
         torch.cuda.synchronize()
     _check_rounds(outs, alone)
+
+
+def test_backward_pairs_reuse_both_orientations():
+    """The backward step: dY quantized both ways into reused buffers, then the
+    dgrad + wgrad launch (fp8_scaled_gemm_pair) reading both orientations."""
+    dev = device()
+    T, din, dout = 1024, 768, 512
+    dys = [_randn((T, dout), 400 + i, 1e-3 * (i + 1)) for i in range(ROUNDS)]
+    qw = m.fp8_quantize_mx(_randn((dout, din), 13, 0.02), m.MX_COLWISE)   # W^T rows: din x dout
+    qx = m.fp8_quantize_mx(_randn((T, din), 14), m.MX_COLWISE)            # X^T rows: din x T
+    q_row = torch.empty((T, dout), dtype=torch.uint8, device=dev)
+    s_row = torch.empty(m.mxfp8_scale_bytes(T, dout), dtype=torch.uint8, device=dev)
+    q_col = torch.empty((dout, T), dtype=torch.uint8, device=dev)
+    s_col = torch.empty(m.mxfp8_scale_bytes(dout, T), dtype=torch.uint8, device=dev)
+    dx = [torch.empty((T, din), dtype=torch.bfloat16, device=dev) for _ in range(ROUNDS)]
+    dw = [torch.empty((dout, din), dtype=torch.bfloat16, device=dev) for _ in range(ROUNDS)]
+    torch.cuda.synchronize()
+    for i in range(ROUNDS):
+        m.fp8_quantize_mx(dys[i], m.MX_ROWWISE | m.MX_COLWISE, q_row=q_row, s_row=s_row,
+                          q_col=q_col, s_col=s_col)
+        m.fp8_scaled_gemm_pair(
+            m.GEMM_MX,
+            dict(a=q_row, a_scale=s_row, b=qw["q_col"], b_scale=qw["s_col"], c=dx[i]),
+            dict(a=q_col, a_scale=s_col, b=qx["q_col"], b_scale=qx["s_col"], c=dw[i]))
+    torch.cuda.synchronize()
+    assert_ok()
+    alone_dx, alone_dw = [], []
+    for i in range(ROUNDS):
+        qd = m.fp8_quantize_mx(dys[i], m.MX_ROWWISE | m.MX_COLWISE)
+        torch.cuda.synchronize()
+        a, b = m.fp8_scaled_gemm_pair(
+            m.GEMM_MX,
+            dict(a=qd["q_row"], a_scale=qd["s_row"], b=qw["q_col"], b_scale=qw["s_col"]),
+            dict(a=qd["q_col"], a_scale=qd["s_col"], b=qx["q_col"], b_scale=qx["s_col"]))
+        torch.cuda.synchronize()
+        alone_dx.append(a)
+        alone_dw.append(b)
+    _check_rounds(dx, alone_dx)
+    _check_rounds(dw, alone_dw)
