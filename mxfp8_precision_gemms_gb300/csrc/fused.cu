@@ -189,6 +189,69 @@ __device__ __forceinline__ float swiglu_fast(float g, float u) {
     return __fmul_rn(__fmul_rn(n, u), r);
 }
 
+// Two fp32 lanes in one 64-bit register pair, for sm_100's packed FP32
+// instructions (each lane rounds to nearest exactly as the scalar one does).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
+
+// swiglu_fast for the two BF16 lanes of g2 and u2 (low half first), with the
+// arithmetic in packed FP32.  Bit-identical to two swiglu_fast calls: the
+// exponent residual is formed with the signs moved onto the constants,
+// d' = fma(a, L2ELo, fma(a, L2E, p)) = -d exactly (each step is the negated
+// scalar step, and rounding to nearest is symmetric), and d' (-ln 2) =
+// d ln 2; the rest is the same operations lane by lane.
+__device__ __forceinline__ void swiglu_fast2(uint32_t g2, uint32_t u2, float& y0, float& y1) {
+    constexpr float kL2E = 1.44269502163f;
+    constexpr float kL2ELo = 1.92596303350e-08f;
+    constexpr float kLn2 = 0.693147182465f;
+    const float g0 = bf16_lo(g2), g1 = bf16_hi(g2);
+    const uint64_t G = f2_pack(g0, g1);
+    const uint64_t U = f2_pack(bf16_lo(u2), bf16_hi(u2));
+    const uint64_t A = f2_pack(fabsf(g0), fabsf(g1));
+    const uint64_t P = f2_mul(A, f2_splat(-kL2E));                       // p = RN(-a L2E)
+    const uint64_t D = f2_fma(A, f2_splat(kL2ELo), f2_fma(A, f2_splat(kL2E), P));  // -d
+    float p0, p1, e0, e1;
+    f2_unpack(P, p0, p1);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(p0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(p1));
+    const uint64_t E = f2_pack(e0, e1);
+    const uint64_t T = f2_fma(E, f2_mul(D, f2_splat(-kLn2)), E);         // t = e^-|g|
+    float s0, s1, r0, r1, gt0, gt1;
+    f2_unpack(f2_add(T, f2_splat(1.f)), s0, s1);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(s0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(s1));
+    f2_unpack(f2_mul(G, T), gt0, gt1);
+    const uint64_t N = f2_pack(fmaxf(g0, gt0), fmaxf(g1, gt1));
+    f2_unpack(f2_mul(f2_mul(N, U), f2_pack(r0, r1)), y0, y1);
+}
+
 // Magnitude of BF16 bits 0..0x7F80 as a double (0x7F80 taken as 2^128, the
 // value the rounding of the largest finite BF16 steps to).
 __device__ __forceinline__ double bf16_mag(uint32_t b) {
@@ -263,8 +326,8 @@ __device__ __forceinline__ bool near_any(uint32_t near) {
 // Two fast-path values rounded to BF16; `near` takes the per-half minimum of
 // both values' low 16 bits (y0 in the low half) plus the window offset.
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2, uint32_t& near) {
-    const float y0 = swiglu_fast(bf16_lo(g2), bf16_lo(u2));
-    const float y1 = swiglu_fast(bf16_hi(g2), bf16_hi(u2));
+    float y0, y1;
+    swiglu_fast2(g2, u2, y0, y1);
     uint32_t w;
     asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(__float_as_uint(y0)), "r"(__float_as_uint(y1)));
     near = min_u16x2(near, w + kNearOffset);
@@ -816,10 +879,17 @@ namespace {
 // rounding, no quantization), for checking its error bound.
 __global__ void swiglu_f32_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                   int64_t n, float* __restrict__ y) {
+    // pairs through the fused kernel's packed path; an odd last value alone
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
-        y[i] = swiglu_fast(__uint_as_float(static_cast<uint32_t>(g[i]) << 16),
-                           __uint_as_float(static_cast<uint32_t>(u[i]) << 16));
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; 2 * i < n; i += stride) {
+        const int64_t k = 2 * i;
+        const uint32_t g2 = g[k] | (k + 1 < n ? static_cast<uint32_t>(g[k + 1]) << 16 : 0u);
+        const uint32_t u2 = u[k] | (k + 1 < n ? static_cast<uint32_t>(u[k + 1]) << 16 : 0u);
+        float y0, y1;
+        swiglu_fast2(g2, u2, y0, y1);
+        y[k] = y0;
+        if (k + 1 < n) y[k + 1] = y1;
+    }
 }
 
 }  // namespace
