@@ -189,37 +189,6 @@ __device__ __forceinline__ float swiglu_fast(float g, float u) {
     return __fmul_rn(__fmul_rn(n, u), r);
 }
 
-// Two fp32 lanes in one 64-bit register pair, for sm_100's packed FP32
-// instructions (each lane rounds to nearest exactly as the scalar one does).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
 
 // swiglu_fast for the two BF16 lanes of g2 and u2 (low half first), with the
 // arithmetic in packed FP32.  Bit-identical to two swiglu_fast calls: the
@@ -568,7 +537,7 @@ __device__ __forceinline__ void weighted_block_quant(const uint32_t* xw, float a
             v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
         }
     }
-    mx_block32_amax<FLOOR>(v, am, q_dst, s_dst, v8);
+    mx_block32_amax<FLOOR, false>(v, am, q_dst, s_dst, v8);  // at 64 registers: scalar products
 }
 
 // Launch-bounded to 64 registers (four CTAs per SM): 252.6 against 273 us
@@ -634,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                     v[4 * k] = e.x; v[4 * k + 1] = e.y; v[4 * k + 2] = e.z; v[4 * k + 3] = e.w;
                 }
             }
-            mx_block32<FLOOR>(v, in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
+            mx_block32<FLOOR, false>(v, in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
         }
     }
 }

@@ -74,6 +74,38 @@ __device__ __forceinline__ uint32_t amax8(const uint4& v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two fp32 lanes in one 64-bit register pair, for sm_100's packed FP32
+// instructions (each lane rounds to nearest exactly as the scalar one does).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
+
 // Saturating RNE conversion of two fp32 values; `lo` lands in the low byte.
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
@@ -86,12 +118,31 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
     return r;
 }
 
+// Four consecutive BF16 values (two words) times an fp32 factor, each
+// product rounded to fp32 and then to FMT: four payload bytes.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant4_scaled(uint32_t w0, uint32_t w1, float f) {
+    const uint64_t F = f2_splat(f);
+    float a0, a1, b0, b1;
+    f2_unpack(f2_mul(f2_pack(bf16_lo(w0), bf16_hi(w0)), F), a0, a1);
+    f2_unpack(f2_mul(f2_pack(bf16_lo(w1), bf16_hi(w1)), F), b0, b1);
+    return cvt_fp8x2<FMT>(a0, a1) | (cvt_fp8x2<FMT>(b0, b1) << 16);
+}
+
 // Four consecutive BF16 values (two words) times a factor -> four E4M3 bytes.
-// The product by a power of two is exact (no FTZ in this file).
+// The product by a power of two is exact (no FTZ in this file).  PACKED: the
+// products in packed FP32 (lane by lane the scalar products; fewer issued
+// instructions, but the register pairs cost registers in kernels already at
+// their bound).
+template <bool PACKED = true>
 __device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float f) {
-    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
-    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
-    return a | (b << 16);
+    if constexpr (PACKED) {
+        return quant4_scaled<FP8_E4M3>(w0, w1, f);
+    } else {
+        const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
+        const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
+        return a | (b << 16);
+    }
 }
 
 // Same for four values held in the low (or high) halves of four words.
@@ -99,9 +150,11 @@ template <bool HIGH>
 __device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
                                                 uint32_t w3, float f) {
     auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
-    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
-    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
-    return a | (b << 16);
+    const uint64_t F = f2_splat(f);
+    float a0, a1, b0, b1;
+    f2_unpack(f2_mul(f2_pack(v(w0), v(w1)), F), a0, a1);
+    f2_unpack(f2_mul(f2_pack(v(w2), v(w3)), F), b0, b1);
+    return cvt_fp8x2<FP8_E4M3>(a0, a1) | (cvt_fp8x2<FP8_E4M3>(b0, b1) << 16);
 }
 
 // Byte offset, inside its 512-byte tile, of the 4-byte group of scales of
@@ -225,7 +278,7 @@ __device__ __forceinline__ uint32_t block32_amax_bits(const uint32_t* w) {
 // packed BF16 (value 2i in the low half of w[i]) whose largest magnitude's
 // bits are amax_bits (block32_amax_bits).  Writes the 32 E4M3 bytes to q_dst
 // (skipped when null; 32-byte aligned when v8) and the E8M0 byte to *s_dst.
-template <bool FLOOR>
+template <bool FLOOR, bool PACKED = true>
 __device__ __forceinline__ void mx_block32_amax(const uint32_t* w, uint32_t amax_bits,
                                                 uint8_t* q_dst, uint8_t* s_dst, bool v8) {
     const uint32_t byte = e8m0_byte(amax_bits, FLOOR);
@@ -236,17 +289,17 @@ __device__ __forceinline__ void mx_block32_amax(const uint32_t* w, uint32_t amax
     } else {
         const float f = inv_scale(byte);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = quant4_e4m3(w[2 * k], w[2 * k + 1], f);
+        for (int k = 0; k < 8; ++k) q[k] = quant4_e4m3<PACKED>(w[2 * k], w[2 * k + 1], f);
     }
     if (q_dst != nullptr) st32(q_dst, q, v8);
     *s_dst = static_cast<uint8_t>(byte);
 }
 
 // The same with the block maximum taken here.
-template <bool FLOOR>
+template <bool FLOOR, bool PACKED = true>
 __device__ __forceinline__ void mx_block32(const uint32_t* w, uint8_t* q_dst, uint8_t* s_dst,
                                            bool v8) {
-    mx_block32_amax<FLOOR>(w, block32_amax_bits(w), q_dst, s_dst, v8);
+    mx_block32_amax<FLOOR, PACKED>(w, block32_amax_bits(w), q_dst, s_dst, v8);
 }
 
 // One rowwise step of a 128 x 128 tile: the half-warp holding tile row r

@@ -482,10 +482,8 @@ __global__ void __launch_bounds__(256)
          i += stride) {
         const uint4 v = x8[i];
         uint2 o;
-        o.x = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s)) |
-              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s)) << 16);
-        o.y = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s)) |
-              (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s)) << 16);
+        o.x = quant4_scaled<FMT>(v.x, v.y, s);
+        o.y = quant4_scaled<FMT>(v.z, v.w, s);
         reinterpret_cast<uint2*>(q)[i] = o;
     }
     for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
@@ -572,9 +570,7 @@ __device__ __forceinline__ void cast_share(const uint16_t* __restrict__ x, uint8
                 uint32_t* po = &o.x;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    po[e] = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(w[k][2 * e]), s), __fmul_rn(bf16_hi(w[k][2 * e]), s)) |
-                            (cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(w[k][2 * e + 1]), s),
-                                            __fmul_rn(bf16_hi(w[k][2 * e + 1]), s)) << 16);
+                    po[e] = quant4_scaled<FMT>(w[k][2 * e], w[k][2 * e + 1], s);
                 reinterpret_cast<uint4*>(q)[c] = o;
             }
         }
