@@ -145,16 +145,16 @@ __device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float 
     }
 }
 
-// Same for four values held in the low (or high) halves of four words.
+// Same for four values held in the low (or high) halves of four words
+// (scalar products: the packed form's register pairs cost the colwise tile
+// kernel 18 registers and a CTA per SM for no gain).
 template <bool HIGH>
 __device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
                                                 uint32_t w3, float f) {
     auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
-    const uint64_t F = f2_splat(f);
-    float a0, a1, b0, b1;
-    f2_unpack(f2_mul(f2_pack(v(w0), v(w1)), F), a0, a1);
-    f2_unpack(f2_mul(f2_pack(v(w2), v(w3)), F), b0, b1);
-    return cvt_fp8x2<FP8_E4M3>(a0, a1) | (cvt_fp8x2<FP8_E4M3>(b0, b1) << 16);
+    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
+    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
+    return a | (b << 16);
 }
 
 // Byte offset, inside its 512-byte tile, of the 4-byte group of scales of
