@@ -17,6 +17,16 @@
  *    kernel attributes and caches occupancy queries).  Calls on different
  *    streams may run concurrently when they share no output buffer (and,
  *    for the entry points that take one, no workspace or history state).
+ *  - Kernels use programmatic dependent launch: the GEMMs and most
+ *    quantizers are launched with programmatic stream serialization, so
+ *    they may start while the kernel before them on the stream finishes,
+ *    and each waits for that kernel's completion (griddepcontrol.wait)
+ *    before touching global memory; every kernel signals early launch of
+ *    the kernel after it.  A kernel of the caller's own that follows a call
+ *    and is itself launched with programmatic stream serialization must
+ *    therefore wait (cudaGridDependencySynchronize) before reading the
+ *    call's outputs, as programmatic dependent launch always requires;
+ *    kernels launched without that attribute are unaffected.
  *  - Errors the host can see (null pointers, bad shapes, misaligned pointers
  *    or strides) are returned at once and launch nothing.  Errors only the
  *    device can see (inconsistent group offsets, a wait that exceeded its
