@@ -542,7 +542,10 @@ void mxfp8_debug_inject_wait_timeout(int enable);
  * Test hook: y[i] = the fp32 value g[i] sigma(g[i]) u[i] that
  * fp8_swiglu_quantize_mx forms on its fast path (gates >= -80), before the
  * BF16 rounding, so its error bound can be checked.  g, u: device BF16[n];
- * y: device fp32[n].
+ * y: device fp32[n].  The fast path runs two values at a time in packed
+ * FP32; each value is also formed one at a time (as the per-block redo
+ * does), and a difference in bits other than two NaNs records
+ * MXFP8_ERR_DEVICE_CHECK for mxfp8_last_device_status().
  */
 mxfp8_status mxfp8_debug_swiglu_f32(const void* g_bf16, const void* u_bf16, int64_t n, float* y,
                                     mxfp8_stream_t stream);

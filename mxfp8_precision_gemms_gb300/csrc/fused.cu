@@ -848,16 +848,26 @@ namespace {
 // rounding, no quantization), for checking its error bound.
 __global__ void swiglu_f32_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                   int64_t n, float* __restrict__ y) {
-    // pairs through the fused kernel's packed path; an odd last value alone
+    // pairs through the fused kernel's packed path (an odd last value alone);
+    // each value is also computed by the scalar path the block redo uses, and
+    // any difference in bits (other than two NaNs) is recorded as a device
+    // check failure: the two paths are meant to be bit-identical
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; 2 * i < n; i += stride) {
         const int64_t k = 2 * i;
-        const uint32_t g2 = g[k] | (k + 1 < n ? static_cast<uint32_t>(g[k + 1]) << 16 : 0u);
-        const uint32_t u2 = u[k] | (k + 1 < n ? static_cast<uint32_t>(u[k + 1]) << 16 : 0u);
+        const bool two = k + 1 < n;
+        const uint32_t g2 = g[k] | (two ? static_cast<uint32_t>(g[k + 1]) << 16 : 0u);
+        const uint32_t u2 = u[k] | (two ? static_cast<uint32_t>(u[k + 1]) << 16 : 0u);
         float y0, y1;
         swiglu_fast2(g2, u2, y0, y1);
+        const float s0 = swiglu_fast(bf16_lo(g2), bf16_lo(u2));
+        const float s1 = swiglu_fast(bf16_hi(g2), bf16_hi(u2));
+        auto same = [](float a, float b) {
+            return __float_as_uint(a) == __float_as_uint(b) || (isnan(a) && isnan(b));
+        };
+        if (!same(y0, s0) || (two && !same(y1, s1))) record_status(MXFP8_ERR_DEVICE_CHECK);
         y[k] = y0;
-        if (k + 1 < n) y[k + 1] = y1;
+        if (two) y[k + 1] = y1;
     }
 }
 

@@ -170,6 +170,7 @@ def test_swiglu_fast_path_error_every_gate():
     # blocks are redone in FP64)
     huge = np.isfinite(g) & (np.abs(g) * np.log2(np.e) > float(np.finfo(np.float32).max) * (1 + 2.0 ** -20))
     yh = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(allb[huge]), to_dev_bf16(np.full(int(huge.sum()), 0x3F80, np.uint16))))
+    assert_ok()  # the packed and scalar fast paths agree bit for bit
     assert huge.sum() > 0 and np.all(np.isnan(yh))
     edge = np.abs(g) * np.log2(np.e) > float(np.finfo(np.float32).max) * (1 - 2.0 ** -20)
     gb = allb[np.isfinite(g) & (g >= -80) & (g != 0) & ~edge]
@@ -189,6 +190,7 @@ def test_swiglu_fast_path_special_gates():
     gb = np.array([0x7F80, 0x7FC0, 0x42B0, 0x4300, 0x7F00, 0x7F7F, 0x0000, 0x8000], np.uint16)
     ub = np.array([0x3F80] * 6 + [0x4000, 0x4000], np.uint16)
     y = host(m.mxfp8_debug_swiglu_f32(to_dev_bf16(gb), to_dev_bf16(ub)))
+    assert_ok()
     assert np.isnan(y[0]) and np.isnan(y[1]) and np.isnan(y[5])
     gd = oracle.bf16_decode(gb)
     assert y[2] == np.float32(gd[2]) and y[3] == np.float32(gd[3]) and y[4] == np.float32(gd[4])
@@ -252,6 +254,7 @@ def test_swiglu_quantize_full_size():
     f = h.shape[1] // 2
     y = host(m.mxfp8_debug_swiglu_f32(h[:, :f].contiguous().reshape(-1),
                                       h[:, f:].contiguous().reshape(-1)))
+    assert_ok()
     low = y.view(np.uint32) & 0xFFFF
     assert int((np.abs(low.astype(np.int64) - 0x8000) <= 8).sum()) > 100
 
