@@ -539,6 +539,12 @@ __device__ __forceinline__ uint32_t amax_share(const uint16_t* __restrict__ x, i
                 for (int e = 0; e < 8; ++e) w[k][e] = 0u;
             }
         }
+        // the next round's chunks into L2 meanwhile (no registers held)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = i + (4 + k) * stride;
+            if (c < n16) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + c * 16));
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             m = max(m, max(amax8(make_uint4(w[k][0], w[k][1], w[k][2], w[k][3])),
