@@ -639,8 +639,10 @@ __global__ void __launch_bounds__(kThreads, 4)
                                  bool v8) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
     griddep_wait();               // the previous kernel's results are visible
-    __shared__ int64_t s_row[kTokensPerCta * kMaxRoutes];   // dispatched row, -1: none
-    __shared__ int64_t s_prow[kTokensPerCta * kMaxRoutes];  // its row in the scale array
+    // per route: its payload row (null: no route) and its row's place in the
+    // swizzled scale array (block 0), so the item loop only adds offsets
+    __shared__ uint8_t* s_qrow[kTokensPerCta * kMaxRoutes];
+    __shared__ uint8_t* s_srow[kTokensPerCta * kMaxRoutes];
     __shared__ float s_w[kTokensPerCta * kMaxRoutes];
     __shared__ int32_t s_off[GROUPED ? kMaxGroupsTok + 1 : 1];
     __shared__ int64_t s_pstart[GROUPED ? kMaxGroupsTok + 1 : 1];
@@ -722,8 +724,9 @@ __global__ void __launch_bounds__(kThreads, 4)
                 prow = r;
             }
         }
-        s_row[tid] = row;
-        s_prow[tid] = prow;
+        s_qrow[tid] = row >= 0 ? q + row * cols : nullptr;
+        s_srow[tid] = row >= 0 ? s + (prow / kTile) * nkc * 512 + swz_word(static_cast<int>(prow % kTile))
+                               : nullptr;
         s_w[tid] = w;
     }
     __syncthreads();
@@ -742,13 +745,11 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
             const int e = tl * k + j;
-            const int64_t row = s_row[e];
-            if (row < 0) continue;
+            uint8_t* const qrow = s_qrow[e];
+            if (qrow == nullptr) continue;
             const float w = s_w[e];
-            const int64_t prow = s_prow[e];
-            uint8_t* s_dst = s + ((prow / kTile) * nkc + b / 4) * 512 +
-                             swz_word(static_cast<int>(prow % kTile)) + (b & 3);
-            weighted_block_quant<FLOOR>(xw, ax, w, q + row * cols + b * 32, s_dst, v8);
+            uint8_t* s_dst = s_srow[e] + (b >> 2) * 512 + (b & 3);
+            weighted_block_quant<FLOOR>(xw, ax, w, qrow + b * 32, s_dst, v8);
         }
     }
 }
