@@ -493,15 +493,78 @@ __device__ __noinline__ uint4 weighted8_exact(uint4 x8, float w) {
     return v;
 }
 
-// One weighted block: bf16_RNE(w x) of the 32 BF16 values in xw (rounded
-// once from the exact products), MX-quantized into q_dst (32 bytes, skipped
-// when null) and *s_dst; ax is max |x| over the block as fp32 (the BF16
-// maximum, NaN or Inf as they are).  The block maximum of the weighted values
-// is the correctly rounded |ax w|: the rounding is monotone, so one product
-// replaces the maximum over the 32 weighted values.
+// Per-half signed 16-bit minimum: 0x8000 is the smallest signed half, so a
+// half of a running minimum is 0x8000 exactly when some input half was.
+__device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16_RNE(x) as an fp32 value (the BF16 bits in the high half, zeros below).
+__device__ __forceinline__ float bf16_round_f32(float x) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x), "f"(0.f));
+    return __uint_as_float(r);
+}
+
+// One route of one block on the fast path: the 32 values as fp32 pairs xf
+// (value 2i low), times ws two at a time, each product rounded to fp32, then
+// to BF16, then to E4M3 (qv, 32 bytes).  The BF16 rounding of an fp32
+// product agrees with that of the exact product unless the product sits on a
+// BF16 midpoint (low half 0x8000, see weighted2); the running signed minimum
+// of the products' low halves finds that case.  Returns false then: the
+// caller redoes the block exactly.
+__device__ __forceinline__ bool weighted32_fast(const uint64_t* xf, float ws, uint32_t* qv) {
+    const uint64_t W = f2_splat(ws);
+    uint32_t mn = 0x7FFF7FFFu;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t h[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float p0, p1;
+            f2_unpack(f2_mul(xf[2 * kk + t], W), p0, p1);
+            uint32_t lows;
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(lows) : "r"(__float_as_uint(p0)), "r"(__float_as_uint(p1)));
+            mn = min_s16x2(mn, lows);
+            h[t] = cvt_fp8x2<FP8_E4M3>(bf16_round_f32(p0), bf16_round_f32(p1));
+        }
+        qv[kk] = h[0] | (h[1] << 16);
+    }
+    return (mn & 0xFFFFu) != 0x8000u && (mn >> 16) != 0x8000u;
+}
+
+// bf16_RNE of the exact product x ws, as an fp32 value, for the values of a
+// block that weighted32_fast flagged: p = fp32_RN(x ws), and when p sits on a
+// BF16 midpoint the product's exact residual x ws - p (one FMA) moves p one
+// fp32 unit toward the exact value, off the midpoint and onto the side the
+// exact product rounds to.  The residual is exact for every product that can
+// reach a nonzero E4M3 code (|p| >= 2^-11: its last bit lies far above
+// fp32's underflow); a smaller p stays below 2^-10 after the one-unit move
+// and quantizes to the same signed zero either way.
+__device__ __forceinline__ float weighted_exact_f32(float x, float ws) {
+    const float p = __fmul_rn(x, ws);
+    const float r = __fmaf_rn(x, ws, -p);
+    uint32_t pb = __float_as_uint(p);
+    if ((pb & 0xFFFFu) == 0x8000u && r != 0.f) pb += ((r > 0.f) == (p > 0.f)) ? 1u : 0xFFFFFFFFu;
+    return bf16_round_f32(__uint_as_float(pb));
+}
+
+// One weighted block: bf16_RNE(w x) of the 32 BF16 values held as fp32 pairs
+// in xf (value 2i low; rounded once from the exact products), MX-quantized
+// into q_dst (32 bytes, skipped when null) and *s_dst; ax is max |x| over the
+// block as fp32 (the BF16 maximum, NaN or Inf as they are).  The block
+// maximum of the weighted values is the correctly rounded |ax w|: the
+// rounding is monotone, so one product replaces the maximum over the 32
+// weighted values.  The rare forms (a flagged block, a scale outside the
+// folded range, NaN / Inf) reread the block's 32 values from src four at a
+// time, so that the unpacked copy is all the registers they share with the
+// fast path.
 template <bool FLOOR>
-__device__ __forceinline__ void weighted_block_quant(const uint32_t* xw, float ax, float w,
-                                                     uint8_t* q_dst, uint8_t* s_dst, bool v8) {
+__device__ __forceinline__ void weighted_block_quant(const uint64_t* xf, const uint16_t* src,
+                                                     float ax, float w, uint8_t* q_dst,
+                                                     uint8_t* s_dst, bool v8) {
     const float pa = __fmul_rn(ax, fabsf(w));
     const uint32_t am =
         ((__float_as_uint(pa) & 0xFFFFu) == 0x8000u
@@ -513,42 +576,48 @@ __device__ __forceinline__ void weighted_block_quant(const uint32_t* xw, float a
     // scales below 2^-10 and quantizes to a signed zero either way.
     // So the products x w' round straight to the scaled BF16 values.
     const uint32_t byte = e8m0_byte(am, FLOOR);
+    *s_dst = static_cast<uint8_t>(byte);
     const float ws = __fmul_rn(w, inv_scale(byte));
-    if (byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f) {
-        uint32_t v[16];
-        uint32_t mid = 0xFFFFFFFFu;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], ws, mid);
-        if (weighted_tie(mid)) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint4 x = weighted8_exact(
-                    make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), ws);
-                v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
-            }
-        }
+    const bool folded = byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f;
+    if (folded) {
         uint32_t qv[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            qv[kk] = cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk]), bf16_hi(v[2 * kk])) |
-                     (cvt_fp8x2<FP8_E4M3>(bf16_lo(v[2 * kk + 1]), bf16_hi(v[2 * kk + 1])) << 16);
-        if (q_dst != nullptr) st32(q_dst, qv, v8);
-        *s_dst = static_cast<uint8_t>(byte);
-        return;
-    }
-    uint32_t v[16];
-    uint32_t mid = 0xFFFFFFFFu;
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) v[kk] = weighted2(xw[kk], w, mid);
-    if (weighted_tie(mid)) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint4 x = weighted8_exact(
-                make_uint4(xw[4 * kk], xw[4 * kk + 1], xw[4 * kk + 2], xw[4 * kk + 3]), w);
-            v[4 * kk] = x.x; v[4 * kk + 1] = x.y; v[4 * kk + 2] = x.z; v[4 * kk + 3] = x.w;
+        if (weighted32_fast(xf, ws, qv)) {
+            if (q_dst != nullptr) st32(q_dst, qv, v8);  // one 32-byte store: each sector written once
+            return;
         }
     }
-    mx_block32_amax<FLOOR, false>(v, am, q_dst, s_dst, v8);  // at 64 registers: scalar products
+    if (q_dst == nullptr) return;
+    const float f = inv_scale(byte);
+#pragma unroll 1
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint2 x = __ldg(reinterpret_cast<const uint2*>(src) + kk);
+        uint32_t q4 = 0x7F7F7F7Fu;  // NaN scale: every payload byte NaN
+        if (folded) {
+            // a product on a BF16 midpoint: the exact residual settles it
+            q4 = cvt_fp8x2<FP8_E4M3>(weighted_exact_f32(bf16_lo(x.x), ws), weighted_exact_f32(bf16_hi(x.x), ws)) |
+                 (cvt_fp8x2<FP8_E4M3>(weighted_exact_f32(bf16_lo(x.y), ws), weighted_exact_f32(bf16_hi(x.y), ws))
+                  << 16);
+        } else if (byte != 0xFFu) {
+            // the unscaled form: bf16(x w) rounded once (the double product
+            // where the fp32 one sits on a midpoint; products here may be
+            // fp32-subnormal), then times 1/s and rounded to E4M3
+            uint32_t h[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint32_t word = t ? x.y : x.x;
+                uint32_t mid = 0xFFFFFFFFu;
+                uint32_t vb = weighted2(word, w, mid);
+                if (weighted_tie(mid)) {
+                    const double wd = w;
+                    vb = bf16_bits_rn(static_cast<double>(bf16_lo(word)) * wd) |
+                         (bf16_bits_rn(static_cast<double>(bf16_hi(word)) * wd) << 16);
+                }
+                h[t] = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(vb), f), __fmul_rn(bf16_hi(vb), f));
+            }
+            q4 = h[0] | (h[1] << 16);
+        }
+        reinterpret_cast<uint32_t*>(q_dst)[kk] = q4;
+    }
 }
 
 // Launch-bounded to 64 registers (four CTAs per SM): 252.6 against 273 us
@@ -623,8 +692,11 @@ __global__ void __launch_bounds__(kThreads, 4)
 // tokens and reads each token's dY row once; a thread owns one 32-value
 // block of one token and writes, for each of the token's k routes, the
 // weighted block's E4M3 payload into the route's dispatched row and its scale
-// byte into the (group-padded) scale array.  The per-value arithmetic is
-// weighted_quant_kernel's, exact-product ties included.
+// byte into the (group-padded) scale array.  The per-value results are
+// weighted_quant_kernel's, exact-product ties included.  The block is
+// unpacked to fp32 pairs once for all of its routes (32 registers held
+// across the route loop); launch-bounded to four CTAs per SM, which costs a
+// few spilled words and still beats three CTAs without spills.
 constexpr int kTokensPerCta = 16;
 constexpr int kMaxRoutes = 16;
 constexpr int kMaxGroupsTok = 1024;
@@ -742,6 +814,10 @@ __global__ void __launch_bounds__(kThreads, 4)
         // rounding is monotone, so one product per route replaces the
         // maximum over the 32 weighted values (NaN and Inf carry over)
         const float ax = __uint_as_float(block32_amax_bits(xw) << 16);
+        // the block as fp32 pairs, unpacked once for all of its routes
+        uint64_t xf[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xf[i] = f2_pack(bf16_lo(xw[i]), bf16_hi(xw[i]));
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
             const int e = tl * k + j;
@@ -749,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             if (qrow == nullptr) continue;
             const float w = s_w[e];
             uint8_t* s_dst = s_srow[e] + (b >> 2) * 512 + (b & 3);
-            weighted_block_quant<FLOOR>(xw, ax, w, qrow + b * 32, s_dst, v8);
+            weighted_block_quant<FLOOR>(xf, dy + (t0 + tl) * ld + b * 32, ax, w, qrow + b * 32, s_dst, v8);
         }
     }
 }

@@ -506,16 +506,17 @@ def test_route_weight_tokens_grouped(counts):
 
 def test_route_weight_tokens_ties_and_bad_row():
     """The 32 constructed double-rounding cases (fp32 product on a BF16
-    midpoint, exact product off it) through the per-token form, plus a
-    slot naming a row past the end (recorded, skipped)."""
+    midpoint, exact product off it) through the per-token form, half of them
+    with the value negated (the correction's direction follows the sign),
+    plus a slot naming a row past the end (recorded, skipped)."""
     pairs = _fp32_midpoint_pairs(32, 23)
     cols, k = 64, 2
     tokens = len(pairs)
     rng = np.random.default_rng(25)
     dy = np.zeros((tokens, cols), np.uint16)
     for i, (xb, _) in enumerate(pairs):
-        dy[i] = oracle.bf16_round(rng.uniform(0.5, 1.0, cols))
-        dy[i, i % cols] = xb
+        dy[i] = oracle.bf16_round(rng.uniform(0.5, 1.0, cols) * rng.choice([-1.0, 1.0], cols))
+        dy[i, i % cols] = xb | (0x8000 if i % 2 else 0)
     rows = tokens  # slot 0 of token i -> row i; slot 1 unused
     tr = np.full((tokens, k), -1, np.int32)
     tr[:, 0] = np.arange(tokens)
@@ -539,8 +540,8 @@ def test_route_weight_tokens_extremes():
     """The per-token form on blocks that mix BF16-subnormal products with a
     block maximum near 2^-100 (the scale folded into the weight still gives
     their signed zeros), products at the top of the range, subnormal and
-    largest BF16 inputs, weights of 2^-30, 2^-126 and 0, and exact-product
-    ties."""
+    largest BF16 inputs, weights of 2^-30, 2^-126 and 0, exact-product ties,
+    and blocks holding Inf or NaN."""
     rng = np.random.default_rng(26)
     tokens, cols, k = 24, 96, 3
     mag = np.exp(rng.uniform(-80, 80, (tokens, 1)))
@@ -550,6 +551,8 @@ def test_route_weight_tokens_extremes():
     dy[1, :32] = oracle.bf16_round(np.ldexp(rng.uniform(1, 2, 32), rng.integers(-131, -100, 32)) *
                                    rng.choice([-1, 1], 32))
     dy[2, :32] = oracle.bf16_round(np.ldexp(rng.uniform(1, 2, 32), rng.integers(-140, -118, 32)))
+    # blocks holding Inf, -Inf and NaN inputs: NaN scale, every payload byte 0x7F
+    dy[3, 0], dy[3, 33], dy[3, 70] = 0x7F80, 0xFF80, 0x7FC0
     rows = tokens * k
     tr = np.arange(rows, dtype=np.int32).reshape(tokens, k)
     tw = rng.uniform(0, 1, (tokens, k)).astype(np.float32)
