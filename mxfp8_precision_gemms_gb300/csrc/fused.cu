@@ -480,19 +480,6 @@ __device__ __forceinline__ bool weighted_tie(uint32_t mid) {
     return (mid & 0xFFFFu) == 0u || (mid >> 16) == 0u;
 }
 
-// 8 products formed exactly in double and rounded once.
-__device__ __noinline__ uint4 weighted8_exact(uint4 x8, float w) {
-    uint4 v;
-    uint32_t* vv = reinterpret_cast<uint32_t*>(&v);
-    const uint32_t* xx = reinterpret_cast<const uint32_t*>(&x8);
-    const double wd = w;
-    for (int i = 0; i < 4; ++i) {
-        vv[i] = bf16_bits_rn(static_cast<double>(bf16_lo(xx[i])) * wd) |
-                (bf16_bits_rn(static_cast<double>(bf16_hi(xx[i])) * wd) << 16);
-    }
-    return v;
-}
-
 // Per-half signed 16-bit minimum: 0x8000 is the smallest signed half, so a
 // half of a running minimum is 0x8000 exactly when some input half was.
 __device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
@@ -508,14 +495,15 @@ __device__ __forceinline__ float bf16_round_f32(float x) {
     return __uint_as_float(r);
 }
 
-// One route of one block on the fast path: the 32 values as fp32 pairs xf
-// (value 2i low), times ws two at a time, each product rounded to fp32, then
-// to BF16, then to E4M3 (qv, 32 bytes).  The BF16 rounding of an fp32
-// product agrees with that of the exact product unless the product sits on a
-// BF16 midpoint (low half 0x8000, see weighted2); the running signed minimum
-// of the products' low halves finds that case.  Returns false then: the
-// caller redoes the block exactly.
-__device__ __forceinline__ bool weighted32_fast(const uint64_t* xf, float ws, uint32_t* qv) {
+// One route of one block on the fast path: the 32 values as fp32 pairs xf(i)
+// (i = 0..15, value 2i low), times ws two at a time, each product rounded to
+// fp32, then to BF16, then to E4M3 (qv, 32 bytes).  The BF16 rounding of an
+// fp32 product agrees with that of the exact product unless the product sits
+// on a BF16 midpoint (low half 0x8000, see weighted2); the running signed
+// minimum of the products' low halves finds that case.  Returns false then:
+// the caller redoes the block exactly.
+template <typename XF>
+__device__ __forceinline__ bool weighted32_fast(const XF& xf, float ws, uint32_t* qv) {
     const uint64_t W = f2_splat(ws);
     uint32_t mn = 0x7FFF7FFFu;
 #pragma unroll
@@ -524,7 +512,7 @@ __device__ __forceinline__ bool weighted32_fast(const uint64_t* xf, float ws, ui
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             float p0, p1;
-            f2_unpack(f2_mul(xf[2 * kk + t], W), p0, p1);
+            f2_unpack(f2_mul(xf(2 * kk + t), W), p0, p1);
             uint32_t lows;
             asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(lows) : "r"(__float_as_uint(p0)), "r"(__float_as_uint(p1)));
             mn = min_s16x2(mn, lows);
@@ -551,42 +539,47 @@ __device__ __forceinline__ float weighted_exact_f32(float x, float ws) {
     return bf16_round_f32(__uint_as_float(pb));
 }
 
-// One weighted block: bf16_RNE(w x) of the 32 BF16 values held as fp32 pairs
-// in xf (value 2i low; rounded once from the exact products), MX-quantized
-// into q_dst (32 bytes, skipped when null) and *s_dst; ax is max |x| over the
+// One weighted block: bf16_RNE(w x) of the 32 BF16 values given as fp32 pairs
+// by xf(i) (value 2i low; rounded once from the exact products), MX-quantized
+// into q_dst (32 bytes; skipped when null, which only QNULL callers pass) and
+// *s_dst; ax is max |x| over the
 // block as fp32 (the BF16 maximum, NaN or Inf as they are).  The block
 // maximum of the weighted values is the correctly rounded |ax w|: the
 // rounding is monotone, so one product replaces the maximum over the 32
 // weighted values.  The rare forms (a flagged block, a scale outside the
 // folded range, NaN / Inf) reread the block's 32 values from src four at a
-// time, so that the unpacked copy is all the registers they share with the
-// fast path.
-template <bool FLOOR>
-__device__ __forceinline__ void weighted_block_quant(const uint64_t* xf, const uint16_t* src,
+// time, so that the values are all the registers they share with the fast
+// path.
+template <bool FLOOR, bool QNULL, typename XF>
+__device__ __forceinline__ void weighted_block_quant(const XF& xf, const uint16_t* src,
                                                      float ax, float w, uint8_t* q_dst,
                                                      uint8_t* s_dst, bool v8) {
+    // pa >= +0 or NaN, so am is the magnitude's bits (a NaN rounds to 0x7FFF)
     const float pa = __fmul_rn(ax, fabsf(w));
-    const uint32_t am =
-        ((__float_as_uint(pa) & 0xFFFFu) == 0x8000u
-             ? bf16_bits_rn(static_cast<double>(ax) * fabs(static_cast<double>(w)))
-             : bf16x2_rn(pa, 0.f)) & 0x7FFFu;
+    const uint32_t am = (__float_as_uint(pa) & 0xFFFFu) == 0x8000u
+                            ? bf16_bits_rn(static_cast<double>(ax) * fabs(static_cast<double>(w)))
+                            : bf16x2_rn(pa, 0.f);
+    // e8m0_byte's rule in one biased add and an arithmetic shift: am + 0x1F
+    // carries into the exponent field exactly when the mantissa field is
+    // above 0x60 (rceil), and a negative sum stands for a clamped byte 0
+    const int t = static_cast<int>(am + (FLOOR ? 0u : 0x1Fu) - 0x400u) >> 7;
+    const uint32_t byte = am >= 0x7F80u ? 0xFFu : static_cast<uint32_t>(max(t, 0));
+    *s_dst = static_cast<uint8_t>(byte);
     // With the block scale 2^e known, w' = w 2^-e is exact while it is
     // a normal fp32 number, and bf16(x w') = bf16(x w) 2^-e for every
     // value that is BF16-normal; with e >= -116 a BF16-subnormal value
     // scales below 2^-10 and quantizes to a signed zero either way.
     // So the products x w' round straight to the scaled BF16 values.
-    const uint32_t byte = e8m0_byte(am, FLOOR);
-    *s_dst = static_cast<uint8_t>(byte);
     const float ws = __fmul_rn(w, inv_scale(byte));
-    const bool folded = byte != 0xFFu && byte >= 11u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f;
+    const bool folded = byte - 11u < 244u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f;  // 11 <= byte <= 254
     if (folded) {
         uint32_t qv[8];
         if (weighted32_fast(xf, ws, qv)) {
-            if (q_dst != nullptr) st32(q_dst, qv, v8);  // one 32-byte store: each sector written once
+            if (!QNULL || q_dst != nullptr) st32(q_dst, qv, v8);  // one 32-byte store: each sector written once
             return;
         }
     }
-    if (q_dst == nullptr) return;
+    if (QNULL && q_dst == nullptr) return;
     const float f = inv_scale(byte);
 #pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
@@ -670,20 +663,19 @@ __global__ void __launch_bounds__(kThreads, 4)
         for (int i = 0; i < 2; ++i) {
             const int r = (tid >> 2) + 64 * i;
             const int64_t row = row_begin + r;
-            const bool in = row < row_end && col < cols;
-            uint32_t v[16];
-            uint32_t mid = 0xFFFFFFFFu;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = weighted2(xw[i][k], wv[i], mid);
-            if (weighted_tie(mid)) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 e = weighted8_exact(
-                        make_uint4(xw[i][4 * k], xw[i][4 * k + 1], xw[i][4 * k + 2], xw[i][4 * k + 3]), wv[i]);
-                    v[4 * k] = e.x; v[4 * k + 1] = e.y; v[4 * k + 2] = e.z; v[4 * k + 3] = e.w;
-                }
+            uint8_t* const q_dst = row < row_end && col < cols ? q + row * cols + col : nullptr;
+            uint8_t* const s_dst = s_tile + swz_word(r) + j;
+            if (tk[i] < 0 || col >= cols) {
+                // no token (or padding, or past the last column): zeros
+                const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (q_dst != nullptr) st32(q_dst, z, v8);
+                *s_dst = 0;
+                continue;
             }
-            mx_block32<FLOOR, false>(v, in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
+            const float ax = __uint_as_float(block32_amax_bits(xw[i]) << 16);
+            weighted_block_quant<FLOOR, true>([&](int k) { return f2_pack(bf16_lo(xw[i][k]), bf16_hi(xw[i][k])); },
+                                        dy + static_cast<int64_t>(tk[i]) * ld + col, ax, wv[i], q_dst, s_dst,
+                                        v8);
         }
     }
 }
@@ -825,7 +817,8 @@ __global__ void __launch_bounds__(kThreads, 4)
             if (qrow == nullptr) continue;
             const float w = s_w[e];
             uint8_t* s_dst = s_srow[e] + (b >> 2) * 512 + (b & 3);
-            weighted_block_quant<FLOOR>(xf, dy + (t0 + tl) * ld + b * 32, ax, w, qrow + b * 32, s_dst, v8);
+            weighted_block_quant<FLOOR, false>([&](int i) { return xf[i]; }, dy + (t0 + tl) * ld + b * 32, ax, w,
+                                        qrow + b * 32, s_dst, v8);
         }
     }
 }
