@@ -500,7 +500,8 @@ mxfp8_status fp8_route_weight_quantize_mx(const void* dy_bf16, int64_t tokens, i
  * to that weight.  Every row in [0, rows) must be some token's route
  * exactly once: a row no token names keeps its previous payload and gets
  * zero scale bytes (the scale array is zeroed first, so padding reads 0).
- * Requirements as fp8_route_weight_quantize_mx; groups <= 1024.
+ * Requirements as fp8_route_weight_quantize_mx; groups <= 1024 and
+ * cols <= 2^30 (else MXFP8_ERR_UNSUPPORTED_SHAPE).
  */
 mxfp8_status fp8_route_weight_quantize_mx_tokens(const void* dy_bf16, int64_t tokens, int64_t ld,
                                                  int32_t k, const int32_t* token_rows_dev,

@@ -645,6 +645,7 @@ mxfp8_status fp8_route_weight_quantize_mx_tokens(const void* dy_bf16, int64_t to
     if (!dy_bf16 || !token_rows_dev || !token_weights_dev || !q || !s)
         return fail(MXFP8_ERR_INVALID_ARG, "dy, token_rows, token_weights, q or s is NULL");
     if (cols % 32) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols %% 32 != 0 (cols=%lld)", (long long)cols);
+    if (cols > (int64_t{1} << 30)) return fail(MXFP8_ERR_UNSUPPORTED_SHAPE, "cols > 2^30 (cols=%lld)", (long long)cols);
     if (ld < cols) return fail(MXFP8_ERR_INVALID_ARG, "ld < cols");
     if (ld % 8 || !aligned16(dy_bf16) || !aligned16(q) || !aligned16(s))
         return fail(MXFP8_ERR_MISALIGNED, "pointer or ld not 16-byte aligned");

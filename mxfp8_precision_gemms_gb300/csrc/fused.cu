@@ -480,6 +480,14 @@ __device__ __forceinline__ bool weighted_tie(uint32_t mid) {
     return (mid & 0xFFFFu) == 0u || (mid >> 16) == 0u;
 }
 
+// p + a m with a 32-bit a m: one wide multiply-add (the FMA pipe) instead of
+// a 64-bit add on the integer pipe.
+__device__ __forceinline__ uint8_t* add_wide(uint8_t* p, uint32_t a, uint32_t m) {
+    uint64_t r;
+    asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(m), "l"(reinterpret_cast<uint64_t>(p)));
+    return reinterpret_cast<uint8_t*>(r);
+}
+
 // Per-half signed 16-bit minimum: 0x8000 is the smallest signed half, so a
 // half of a running minimum is 0x8000 exactly when some input half was.
 __device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
@@ -539,6 +547,34 @@ __device__ __forceinline__ float weighted_exact_f32(float x, float ws) {
     return bf16_round_f32(__uint_as_float(pb));
 }
 
+// What the scale folding needs from a route's weight alone.  For a normal
+// w with exponent field f, w' = w 2^(127 - byte) is the normal fp32 number
+// with exponent field f + 127 - byte (bits: wbias - byte 2^23, exact) for
+// byte in [f - 126, f + 126]; the fold also needs byte >= 11 (see
+// weighted_block_quant) and a finite scale (byte <= 254).  The block takes
+// the folded path iff byte - lo <= span (unsigned); a weight that is zero,
+// subnormal, Inf or NaN never does (lo out of byte range).  Any narrower
+// range gives the same bytes: the unfolded path is exact too.
+struct WeightFold {
+    float w;
+    uint32_t wbias;  // bits(w) + 127 2^23
+    uint32_t lo;
+    uint32_t span;
+};
+
+__host__ __device__ __forceinline__ WeightFold weight_fold(float w, uint32_t wbits) {
+    WeightFold f;
+    f.w = w;
+    f.wbias = wbits + (127u << 23);
+    const int ef = static_cast<int>((wbits >> 23) & 0xFFu);
+    const int lo = ef - 126 > 11 ? ef - 126 : 11;
+    const int hi = ef + 126 < 254 ? ef + 126 : 254;
+    const bool ok = ef != 0 && ef != 0xFF && lo <= hi;
+    f.lo = ok ? static_cast<uint32_t>(lo) : 0x10000u;
+    f.span = ok ? static_cast<uint32_t>(hi - lo) : 0u;
+    return f;
+}
+
 // One weighted block: bf16_RNE(w x) of the 32 BF16 values given as fp32 pairs
 // by xf(i) (value 2i low; rounded once from the exact products), MX-quantized
 // into q_dst (32 bytes; skipped when null, which only QNULL callers pass) and
@@ -552,8 +588,9 @@ __device__ __forceinline__ float weighted_exact_f32(float x, float ws) {
 // path.
 template <bool FLOOR, bool QNULL, typename XF>
 __device__ __forceinline__ void weighted_block_quant(const XF& xf, const uint16_t* src,
-                                                     float ax, float w, uint8_t* q_dst,
+                                                     float ax, const WeightFold& wf, uint8_t* q_dst,
                                                      uint8_t* s_dst, bool v8) {
+    const float w = wf.w;
     // pa >= +0 or NaN, so am is the magnitude's bits (a NaN rounds to 0x7FFF)
     const float pa = __fmul_rn(ax, fabsf(w));
     const uint32_t am = (__float_as_uint(pa) & 0xFFFFu) == 0x8000u
@@ -570,8 +607,8 @@ __device__ __forceinline__ void weighted_block_quant(const XF& xf, const uint16_
     // value that is BF16-normal; with e >= -116 a BF16-subnormal value
     // scales below 2^-10 and quantizes to a signed zero either way.
     // So the products x w' round straight to the scaled BF16 values.
-    const float ws = __fmul_rn(w, inv_scale(byte));
-    const bool folded = byte - 11u < 244u && fabsf(ws) >= 0x1p-126f && fabsf(ws) <= 0x1p127f;  // 11 <= byte <= 254
+    const bool folded = byte - wf.lo <= wf.span;
+    const float ws = __uint_as_float(wf.wbias - (byte << 23));  // w 2^(127 - byte) where folded
     if (folded) {
         uint32_t qv[8];
         if (weighted32_fast(xf, ws, qv)) {
@@ -630,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int j = tid & 3;
     // token and weight of this thread's two rows, once for all column tiles
     int32_t tk[2];
-    float wv[2];
+    WeightFold wf[2];
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -640,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 4)
         const bool valid = t >= 0 && t < tokens;
         bad |= in && !valid;
         tk[i] = valid ? t : -1;
-        wv[i] = valid ? __ldg(row_weight + row) : 0.f;
+        const float w = valid ? __ldg(row_weight + row) : 0.f;
+        wf[i] = weight_fold(w, __float_as_uint(w));
     }
     if (bad && blockIdx.y == 0) record_status(MXFP8_ERR_DEVICE_CHECK);
     for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
@@ -674,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             }
             const float ax = __uint_as_float(block32_amax_bits(xw[i]) << 16);
             weighted_block_quant<FLOOR, true>([&](int k) { return f2_pack(bf16_lo(xw[i][k]), bf16_hi(xw[i][k])); },
-                                        dy + static_cast<int64_t>(tk[i]) * ld + col, ax, wv[i], q_dst, s_dst,
+                                        dy + static_cast<int64_t>(tk[i]) * ld + col, ax, wf[i], q_dst, s_dst,
                                         v8);
         }
     }
@@ -691,6 +729,16 @@ __global__ void __launch_bounds__(kThreads, 4)
 // few spilled words and still beats three CTAs without spills.
 constexpr int kTokensPerCta = 16;
 constexpr int kMaxRoutes = 16;
+
+// One route of the CTA's table: its payload row and its row's place in the
+// swizzled scale array (null: no route), and its weight's fold data; 32
+// bytes, read as two 16-byte shared loads.
+struct __align__(16) RouteEntry {
+    uint8_t* qrow;
+    uint8_t* srow;
+    WeightFold wf;
+};
+static_assert(sizeof(RouteEntry) == 32, "two 16-byte loads per route");
 constexpr int kMaxGroupsTok = 1024;
 
 template <bool FLOOR, bool GROUPED>
@@ -705,9 +753,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     griddep_wait();               // the previous kernel's results are visible
     // per route: its payload row (null: no route) and its row's place in the
     // swizzled scale array (block 0), so the item loop only adds offsets
-    __shared__ uint8_t* s_qrow[kTokensPerCta * kMaxRoutes];
-    __shared__ uint8_t* s_srow[kTokensPerCta * kMaxRoutes];
-    __shared__ float s_w[kTokensPerCta * kMaxRoutes];
+    __shared__ RouteEntry s_route[kTokensPerCta * kMaxRoutes];
     __shared__ int32_t s_off[GROUPED ? kMaxGroupsTok + 1 : 1];
     __shared__ int64_t s_pstart[GROUPED ? kMaxGroupsTok + 1 : 1];
     __shared__ int s_ok;
@@ -788,10 +834,11 @@ __global__ void __launch_bounds__(kThreads, 4)
                 prow = r;
             }
         }
-        s_qrow[tid] = row >= 0 ? q + row * cols : nullptr;
-        s_srow[tid] = row >= 0 ? s + (prow / kTile) * nkc * 512 + swz_word(static_cast<int>(prow % kTile))
-                               : nullptr;
-        s_w[tid] = w;
+        RouteEntry re;
+        re.qrow = row >= 0 ? q + row * cols : nullptr;
+        re.srow = row >= 0 ? s + (prow / kTile) * nkc * 512 + swz_word(static_cast<int>(prow % kTile)) : nullptr;
+        re.wf = weight_fold(w, __float_as_uint(w));
+        s_route[tid] = re;
     }
     __syncthreads();
     for (; pi < nt * nb; pi += blockDim.x) {
@@ -806,19 +853,21 @@ __global__ void __launch_bounds__(kThreads, 4)
         // rounding is monotone, so one product per route replaces the
         // maximum over the 32 weighted values (NaN and Inf carry over)
         const float ax = __uint_as_float(block32_amax_bits(xw) << 16);
-        // the block as fp32 pairs, unpacked once for all of its routes
+        // the block's offsets in a route's payload row and scale rows (32
+        // bits: cols <= 2^30), and the block as fp32 pairs, unpacked once for
+        // all of its routes
+        const uint32_t b32 = static_cast<uint32_t>(b);
+        const uint32_t sb32 = ((b32 >> 2) << 9) | (b32 & 3u);
         uint64_t xf[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) xf[i] = f2_pack(bf16_lo(xw[i]), bf16_hi(xw[i]));
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
             const int e = tl * k + j;
-            uint8_t* const qrow = s_qrow[e];
-            if (qrow == nullptr) continue;
-            const float w = s_w[e];
-            uint8_t* s_dst = s_srow[e] + (b >> 2) * 512 + (b & 3);
-            weighted_block_quant<FLOOR, false>([&](int i) { return xf[i]; }, dy + (t0 + tl) * ld + b * 32, ax, w,
-                                        qrow + b * 32, s_dst, v8);
+            const RouteEntry re = s_route[e];
+            if (re.qrow == nullptr) continue;
+            weighted_block_quant<FLOOR, false>([&](int i) { return xf[i]; }, dy + (t0 + tl) * ld + b * 32, ax, re.wf,
+                                               add_wide(re.qrow, b32, 32u), add_wide(re.srow, sb32, 1u), v8);
         }
     }
 }

@@ -138,11 +138,13 @@ def test_host_validation(lib):
     assert GG(P, P, P, P, P, 4, 128, 128, 96 + 16, P, 128, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
     assert lib.fp8_quantize_mx_grouped(P, 128, 64, 64, P, 4, m.MX_COLWISE, P, P, None) == m.MXFP8_ERR_INVALID_ARG
     assert lib.fp8_quantize_mx_grouped(P, 128, 64, 64, P, 0, 0, P, P, None) == m.MXFP8_ERR_INVALID_ARG
-    # route weighting with the routing per token: k in 1..16, rowwise flags
-    # only, routing tables given (all checked before any device access)
+    # route weighting with the routing per token: k in 1..16, cols <= 2^30,
+    # rowwise flags only, routing tables given (all checked before any device access)
     WT = lib.fp8_route_weight_quantize_mx_tokens
     assert WT(P, 64, 2048, 0, P, P, 512, 2048, None, 0, 0, P, P, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
     assert WT(P, 64, 2048, 17, P, P, 512, 2048, None, 0, 0, P, P, None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
+    assert WT(P, 64, (1 << 30) + 32, 8, P, P, 512, (1 << 30) + 32, None, 0, 0, P, P,
+              None) == m.MXFP8_ERR_UNSUPPORTED_SHAPE
     assert WT(P, 64, 2048, 8, P, P, 512, 2048, None, 0, m.MX_COLWISE, P, P, None) == m.MXFP8_ERR_INVALID_ARG
     assert WT(P, 64, 2048, 8, None, P, 512, 2048, None, 0, 0, P, P, None) == m.MXFP8_ERR_INVALID_ARG
     # every failure leaves a message; status strings exist
