@@ -516,7 +516,7 @@ __device__ __forceinline__ bool weighted32_fast(const XF& xf, float ws, uint32_t
     uint32_t mn = 0x7FFF7FFFu;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        uint32_t h[2];
+        float r[4];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             float p0, p1;
@@ -524,9 +524,10 @@ __device__ __forceinline__ bool weighted32_fast(const XF& xf, float ws, uint32_t
             uint32_t lows;
             asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(lows) : "r"(__float_as_uint(p0)), "r"(__float_as_uint(p1)));
             mn = min_s16x2(mn, lows);
-            h[t] = cvt_fp8x2<FP8_E4M3>(bf16_round_f32(p0), bf16_round_f32(p1));
+            r[2 * t] = bf16_round_f32(p0);
+            r[2 * t + 1] = bf16_round_f32(p1);
         }
-        qv[kk] = h[0] | (h[1] << 16);
+        qv[kk] = cvt_fp8x4<FP8_E4M3>(r[0], r[1], r[2], r[3]);
     }
     return (mn & 0xFFFFu) != 0x8000u && (mn >> 16) != 0x8000u;
 }

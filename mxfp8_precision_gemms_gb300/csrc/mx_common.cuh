@@ -118,6 +118,28 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
     return r;
 }
 
+// Saturating RNE conversion of four fp32 values into one word (a0 in the
+// low byte): the two halves are written as one register pair, which the
+// assembler can merge without a separate byte-permute.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x4(float a0, float a1, float b0, float b1) {
+    uint32_t r;
+    if constexpr (FMT == FP8_E4M3) {
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+    } else {
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+    }
+    return r;
+}
+
 // Four consecutive BF16 values (two words) times an fp32 factor, each
 // product rounded to fp32 and then to FMT: four payload bytes.
 template <int FMT>
@@ -126,7 +148,7 @@ __device__ __forceinline__ uint32_t quant4_scaled(uint32_t w0, uint32_t w1, floa
     float a0, a1, b0, b1;
     f2_unpack(f2_mul(f2_pack(bf16_lo(w0), bf16_hi(w0)), F), a0, a1);
     f2_unpack(f2_mul(f2_pack(bf16_lo(w1), bf16_hi(w1)), F), b0, b1);
-    return cvt_fp8x2<FMT>(a0, a1) | (cvt_fp8x2<FMT>(b0, b1) << 16);
+    return cvt_fp8x4<FMT>(a0, a1, b0, b1);
 }
 
 // Four consecutive BF16 values (two words) times a factor -> four E4M3 bytes.
@@ -139,9 +161,8 @@ __device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float 
     if constexpr (PACKED) {
         return quant4_scaled<FP8_E4M3>(w0, w1, f);
     } else {
-        const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f));
-        const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
-        return a | (b << 16);
+        return cvt_fp8x4<FP8_E4M3>(__fmul_rn(bf16_lo(w0), f), __fmul_rn(bf16_hi(w0), f),
+                                   __fmul_rn(bf16_lo(w1), f), __fmul_rn(bf16_hi(w1), f));
     }
 }
 
@@ -152,9 +173,8 @@ template <bool HIGH>
 __device__ __forceinline__ uint32_t quant4_half(uint32_t w0, uint32_t w1, uint32_t w2,
                                                 uint32_t w3, float f) {
     auto v = [](uint32_t w) { return HIGH ? bf16_hi(w) : bf16_lo(w); };
-    const uint32_t a = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f));
-    const uint32_t b = cvt_fp8x2<FP8_E4M3>(__fmul_rn(v(w2), f), __fmul_rn(v(w3), f));
-    return a | (b << 16);
+    return cvt_fp8x4<FP8_E4M3>(__fmul_rn(v(w0), f), __fmul_rn(v(w1), f), __fmul_rn(v(w2), f),
+                               __fmul_rn(v(w3), f));
 }
 
 // Byte offset, inside its 512-byte tile, of the 4-byte group of scales of

@@ -703,14 +703,15 @@ __global__ void __launch_bounds__(256)
         const uint4 v = x8[i];
         m = max(m, amax8(v));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[2] = {0u, 0u};
+        float y[8];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float lo = __fmul_rn(bf16_lo(w[k]), s), hi = __fmul_rn(bf16_hi(w[k]), s);
-            cnt += saturates<FMT>(lo) + saturates<FMT>(hi);
-            o[k >> 1] |= cvt_fp8x2<FMT>(lo, hi) << (16 * (k & 1));
+            y[2 * k] = __fmul_rn(bf16_lo(w[k]), s);
+            y[2 * k + 1] = __fmul_rn(bf16_hi(w[k]), s);
+            cnt += saturates<FMT>(y[2 * k]) + saturates<FMT>(y[2 * k + 1]);
         }
-        reinterpret_cast<uint2*>(q)[i] = make_uint2(o[0], o[1]);
+        reinterpret_cast<uint2*>(q)[i] = make_uint2(cvt_fp8x4<FMT>(y[0], y[1], y[2], y[3]),
+                                                    cvt_fp8x4<FMT>(y[4], y[5], y[6], y[7]));
     }
     for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
          t += stride) {
