@@ -383,6 +383,8 @@ def test_route_weight_quantize_extremes():
     tok[:6] = 0
     wt = rng.uniform(0, 1, rows).astype(np.float32)
     wt[:6] = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2.0 ** -30, 1.5, 0.0, 2.0 ** -126], np.float32)
+    wt[8:14] = np.array([-0.75, 2.0 ** 20, 2.0 ** -140, -(2.0 ** 100), 2.0 ** 126, -(2.0 ** -149)],
+                        np.float32)  # negative, large, subnormal
     tok[7] = tokens  # out of range
     st = _weighted_check(to_dev_bf16(dy), tok, wt)
     assert st == m.MXFP8_ERR_DEVICE_CHECK
@@ -540,8 +542,8 @@ def test_route_weight_tokens_extremes():
     """The per-token form on blocks that mix BF16-subnormal products with a
     block maximum near 2^-100 (the scale folded into the weight still gives
     their signed zeros), products at the top of the range, subnormal and
-    largest BF16 inputs, weights of 2^-30, 2^-126 and 0, exact-product ties,
-    and blocks holding Inf or NaN."""
+    largest BF16 inputs, weights of 2^-30, 2^-126 and 0, negative, large and
+    subnormal weights, exact-product ties, and blocks holding Inf or NaN."""
     rng = np.random.default_rng(26)
     tokens, cols, k = 24, 96, 3
     mag = np.exp(rng.uniform(-80, 80, (tokens, 1)))
@@ -559,4 +561,9 @@ def test_route_weight_tokens_extremes():
     tw[0] = [1 + 2.0 ** -8, 2.0 ** -30, 2.0 ** -126]
     tw[1] = [1.0, 0.75, 2.0 ** -20]
     tw[2] = [0.0, 1.5, 1 + 3 * 2.0 ** -8]
+    # negative, large and subnormal weights: the folded weight's range and
+    # sign (a subnormal weight never folds; a large one overflows some blocks)
+    tw[4] = [-0.75, 2.0 ** 20, 2.0 ** -140]
+    tw[5] = [-(1 + 2.0 ** -8), -(2.0 ** 100), 2.0 ** -149]
+    tw[6] = [2.0 ** 126, -(2.0 ** -126), 3.0e38]
     assert _tokens_check(to_dev_bf16(dy), tr, tw, rows) == m.MXFP8_OK
