@@ -10,11 +10,13 @@
 //    is its token's output gradient times the route weight, rounded to BF16
 //    and MX-quantized rowwise in the same pass (the "route weighting +
 //    gradient Q" fusion).
+//  - weighted_quant_tokens_kernel: the same conversion walking tokens, so
+//    each token's gradient row is read once for all of its routes.
 //
-// All three share the row quantizer's 128 x 128 tile walk: blockIdx.x is a
-// 128-row scale tile (group-padded when offsets are given), blockIdx.y a
+// The first three share the row quantizer's 128 x 128 tile walk: blockIdx.x
+// is a 128-row scale tile (group-padded when offsets are given), blockIdx.y a
 // 128-column tile (or the first of several); each thread owns whole 32-value
-// blocks.
+// blocks.  The token walk gives each CTA 16 tokens.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -463,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 4)
 // low 16 bits are 0x8000; this covers the fp32-subnormal range too, where
 // fp32 still has 16 more fraction bits than BF16).  `mid` keeps the per-half
 // minimum of both products' low halves xor 0x8000 (one prmt, one xor, one
-// min.u16x2 per pair): a zero half marks such a product, and the chunk is
-// redone exactly in double.  Overflow, Inf and NaN follow the fp32 product,
-// which agrees with the exact one in BF16.
+// min.u16x2 per pair): a zero half marks such a product, and the caller
+// redoes the pair exactly in double.  Overflow, Inf and NaN follow the fp32
+// product, which agrees with the exact one in BF16.
 __device__ __forceinline__ uint32_t weighted2(uint32_t x2, float w, uint32_t& mid) {
     const float p0 = __fmul_rn(bf16_lo(x2), w);
     const float p1 = __fmul_rn(bf16_hi(x2), w);
