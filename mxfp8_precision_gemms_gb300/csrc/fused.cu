@@ -87,7 +87,9 @@ __device__ __forceinline__ uint32_t dq2(uint32_t codes, float s) {
 }
 
 // One thread per 32-value block: thread t of a 128 x 128 tile owns block
-// (t & 3) of tile rows t/4 and t/4 + 64.
+// (t & 3) of tile rows t/4 and t/4 + 64.  A CTA walks column tiles
+// blockIdx.y, + gridDim.y, ... two at a time (both tiles' loads in flight
+// before either is converted), so one group lookup serves several tiles.
 template <bool GROUPED>
 __global__ void __launch_bounds__(kThreads)
     dequantize_mx_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
@@ -99,37 +101,48 @@ __global__ void __launch_bounds__(kThreads)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int j = tid & 3;
-    const int64_t col = static_cast<int64_t>(blockIdx.y) * kTile + j * 32;
-    const uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + blockIdx.y) * 512;
-    uint32_t qw[2][8];
-    uint32_t sb[2];
+    for (int64_t ct0 = blockIdx.y; ct0 < nkc; ct0 += 2 * static_cast<int64_t>(gridDim.y)) {
+        uint32_t qw[2][2][8];
+        uint32_t sb[2][2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int r = (tid >> 2) + 64 * i;
-        const int64_t row = row_begin + r;
-        if (row < row_end && col < cols) {
-            ld32_stream(q + row * cols + col, qw[i], v8);
-            sb[i] = __ldg(s_tile + swz_word(r) + j);
-        } else {
+        for (int t = 0; t < 2; ++t) {
+            const int64_t ct = ct0 + t * static_cast<int64_t>(gridDim.y);
+            const int64_t col = ct * kTile + j * 32;
+            const uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) qw[i][k] = 0u;
-            sb[i] = 0u;
-        }
-    }
+            for (int i = 0; i < 2; ++i) {
+                const int r = (tid >> 2) + 64 * i;
+                const int64_t row = row_begin + r;
+                if (ct < nkc && row < row_end && col < cols) {
+                    ld32_stream(q + row * cols + col, qw[t][i], v8);
+                    sb[t][i] = __ldg(s_tile + swz_word(r) + j);
+                } else {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int64_t row = row_begin + (tid >> 2) + 64 * i;
-        if (row < row_end && col < cols) {
-            const float sc = e8m0_value(sb[i]);
-            uint32_t o[16];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                o[2 * k] = dq2(qw[i][k] & 0xFFFFu, sc);
-                o[2 * k + 1] = dq2(qw[i][k] >> 16, sc);
+                    for (int k = 0; k < 8; ++k) qw[t][i][k] = 0u;
+                    sb[t][i] = 0u;
+                }
             }
-            uint16_t* dst = out + row * ldo + col;
-            st32(dst, o, v8);
-            st32(dst + 16, o + 8, v8);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int64_t ct = ct0 + t * static_cast<int64_t>(gridDim.y);
+            const int64_t col = ct * kTile + j * 32;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int64_t row = row_begin + (tid >> 2) + 64 * i;
+                if (ct < nkc && row < row_end && col < cols) {
+                    const float sc = e8m0_value(sb[t][i]);
+                    uint32_t o[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        o[2 * k] = dq2(qw[t][i][k] & 0xFFFFu, sc);
+                        o[2 * k + 1] = dq2(qw[t][i][k] >> 16, sc);
+                    }
+                    uint16_t* dst = out + row * ldo + col;
+                    st32(dst, o, v8);
+                    st32(dst + 16, o + 8, v8);
+                }
+            }
         }
     }
 }
@@ -894,7 +907,7 @@ bool tile_grid(int64_t rows, int64_t cols, bool grouped, int groups, dim3* grid,
 cudaError_t launch_dequantize_mx(const DequantArgs& a, cudaStream_t st) {
     dim3 grid;
     const bool grouped = a.offsets != nullptr;
-    if (!tile_grid(a.rows, a.cols, grouped, a.groups, &grid)) return cudaErrorInvalidValue;
+    if (!tile_grid(a.rows, a.cols, grouped, a.groups, &grid, kColTilesPerCta)) return cudaErrorInvalidValue;
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     const int64_t nkc = (a.cols + kTile - 1) / kTile;
     const bool v8 = aligned32_host(a.q) && aligned32_host(a.out) && a.ldo % 16 == 0;
