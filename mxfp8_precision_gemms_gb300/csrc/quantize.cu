@@ -781,13 +781,17 @@ __global__ void __launch_bounds__(256)
                       const float* s_out_p, uint8_t* __restrict__ q_out, unsigned long long* sat) {
     griddep_launch_dependents();  // a dependent GEMM may launch now
     griddep_wait();               // the previous kernel's results are visible
-    __shared__ uint32_t lut[256];  // one output code per input code, widened to 32 bits
+    // one output code per input code, in four copies shifted to the four byte
+    // positions of a word, so that a word is three ORs of looked-up values
+    __shared__ uint32_t lut[4][256];
     {
         const float s_in = *s_in_p, s_out = *s_out_p;
         const uint32_t c = threadIdx.x;  // blockDim.x == 256
         const float v = fp8x2_to_f32<FIN>(c).x;
         const float y = __fmul_rn(s_out, __fdiv_rn(v, s_in));
-        lut[c] = cvt_fp8x2<FOUT>(y, 0.0f) & 0xFFu;
+        const uint32_t code = cvt_fp8x2<FOUT>(y, 0.0f) & 0xFFu;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) lut[b][c] = code << (8 * b);
     }
     __syncthreads();
     constexpr uint32_t kMaxCode = FOUT == FP8_E4M3 ? 0x7Eu : 0x7Bu;
@@ -796,8 +800,8 @@ __global__ void __launch_bounds__(256)
     const uint4* in16 = reinterpret_cast<const uint4*>(q_in);
     uint32_t cnt = 0;
     auto map4 = [&](uint32_t w) {
-        const uint32_t o = lut[w & 0xFFu] | (lut[(w >> 8) & 0xFFu] << 8) |
-                           (lut[(w >> 16) & 0xFFu] << 16) | (lut[w >> 24] << 24);
+        const uint32_t o = lut[0][w & 0xFFu] | lut[1][(w >> 8) & 0xFFu] | lut[2][(w >> 16) & 0xFFu] |
+                           lut[3][w >> 24];
         // bytes equal to the largest finite code (either sign): zero bytes of x
         const uint32_t x = (o & 0x7F7F7F7Fu) ^ (kMaxCode * 0x01010101u);
         const uint32_t z = ~(((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x | 0x7F7F7F7Fu);
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(256)
     }
     for (int64_t t = n16 * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
          t += stride) {
-        const uint32_t o = lut[q_in[t]];
+        const uint32_t o = lut[0][q_in[t]];
         cnt += (o & 0x7Fu) == kMaxCode;
         q_out[t] = static_cast<uint8_t>(o);
     }
