@@ -451,9 +451,15 @@ def _tokens_check(dy, token_rows, token_weights, rows, offsets=None, floor=False
     equivalent per-row routing) and against the per-row entry point."""
     off_d = None if offsets is None else torch.from_numpy(offsets).to(device())
     flags = m.MX_SCALE_FLOOR if floor else 0
+    cols = dy.shape[1]
+    # scale bytes pre-filled: every byte of the used layout (padding rows and
+    # blocks past cols included) must be written by the call
+    n_s = (m.mxfp8_scale_bytes(rows, cols) if offsets is None
+           else m.mxfp8_grouped_scale_bytes(rows, cols, len(offsets) - 1))
+    s_buf = filled((max(1, n_s),), 0x77, torch.uint8)
     q, s = m.fp8_route_weight_quantize_mx_tokens(
         dy, torch.from_numpy(token_rows).to(device()), torch.from_numpy(token_weights).to(device()),
-        rows, offsets=off_d, flags=flags)
+        rows, offsets=off_d, flags=flags, s=s_buf)
     st = m.mxfp8_last_device_status()
     row_token = np.full(rows, -1, np.int32)
     row_weight = np.zeros(rows, np.float32)
