@@ -676,10 +676,11 @@ def oracle_sample(x, w, keep=None):
     t0 = time.perf_counter()
     a = oracle.quantize_mx(x, oracle.ROWWISE)
     b = oracle.quantize_mx(w, oracle.ROWWISE)
+    t1 = time.perf_counter()
     c = oracle.gemm_mx(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
     t = time.perf_counter() - t0
     if keep is not None:
-        keep.update(a=a, b=b, c=c)
+        keep.update(a=a, b=b, c=c, t_quantize=t1 - t0, t_gemm=t - (t1 - t0))
     return t, 2.0 * x.shape[0] * w.shape[0] * x.shape[1]
 
 
@@ -718,10 +719,15 @@ def cpu_baseline(m, seed=0, budget_s=15.0):
             m_rows = min(X.shape[0], m_rows * f)
         else:
             n_rows = min(W.shape[0], n_rows * f)
+    q_bytes = (m_rows + n_rows) * X.shape[1] * MX_ROW_BYTES
     return {"value": fl / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"X rows 0..{m_rows - 1} of 8192 and W rows 0..{n_rows - 1} of 16384 "
                       f"(full K=4096), quantized rowwise then multiplied in FP64; {t:.1f} s",
             "seconds": t,
+            # the two parts of the step on their own: the oracle's MX quantizer
+            # (3.03125 algorithmic bytes per value) and its FP64 GEMM
+            "quantize_gbs": q_bytes / keep["t_quantize"] / 1e9,
+            "gemm_gflops": fl / keep["t_gemm"] / 1e9,
             "check": sample_check(m, X[:m_rows], W[:n_rows], keep)}
 
 
