@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(kThreads)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int j = tid & 3;
+    const int64_t n_row_tiles = GROUPED ? rows / kTile + groups : (rows + kTile - 1) / kTile;
+    if (!MX_IN_BOUNDS(static_cast<int64_t>(blockIdx.x) < n_row_tiles)) return;
     for (int64_t ct0 = blockIdx.y; ct0 < nkc; ct0 += 2 * static_cast<int64_t>(gridDim.y)) {
         uint32_t qw[2][2][8];
         uint32_t sb[2][2];
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < 2; ++i) {
                 const int r = (tid >> 2) + 64 * i;
                 const int64_t row = row_begin + r;
-                if (ct < nkc && row < row_end && col < cols) {
+                if (ct < nkc && row < row_end && col < cols && MX_IN_BOUNDS(row < rows && col + 32 <= cols)) {
                     ld32_stream(q + row * cols + col, qw[t][i], v8);
                     sb[t][i] = __ldg(s_tile + swz_word(r) + j);
                 } else {
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int64_t row = row_begin + (tid >> 2) + 64 * i;
-                if (ct < nkc && row < row_end && col < cols) {
+                if (ct < nkc && row < row_end && col < cols && MX_IN_BOUNDS(row < rows && col + 32 <= cols)) {
                     const float sc = e8m0_value(sb[t][i]);
                     uint32_t o[16];
 #pragma unroll
@@ -413,6 +415,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int j = tid & 3;
+    const int64_t n_row_tiles = GROUPED ? rows / kTile + groups : (rows + kTile - 1) / kTile;
+    if (!MX_IN_BOUNDS(static_cast<int64_t>(blockIdx.x) < n_row_tiles)) return;
     for (int64_t ct = blockIdx.y; ct < nkc; ct += gridDim.y) {
         const int64_t col = ct * kTile + j * 32;
         uint8_t* s_tile = s + (static_cast<int64_t>(blockIdx.x) * nkc + ct) * 512;
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         for (int i = 0; i < 2; ++i) {
             const int r = (tid >> 2) + 64 * i;
             const int64_t row = row_begin + r;
-            const bool in = row < row_end && col < f;
+            const bool in = row < row_end && col < f && MX_IN_BOUNDS(row < rows && col + 32 <= f && ld >= 2 * f);
             uint32_t gw[16], uw[16];
             if (in) {
                 const uint16_t* src = h + row * ld + col;
@@ -461,8 +465,9 @@ __global__ void __launch_bounds__(kThreads, 4)
                     todo &= todo - 1;
                     const int stid = (tid & ~31) | src;
                     const int rs = (stid >> 2) + 64 * i;
-                    swiglu_block_redo<FLOOR>(h, ld, f, row_begin + rs, ct * kTile + (stid & 3) * 32,
-                                             (ex >> src) & 1u, q, s_tile + swz_word(rs) + (stid & 3));
+                    if (MX_IN_BOUNDS(row_begin + rs < rows && ct * kTile + (stid & 3) * 32 + 32 <= f))
+                        swiglu_block_redo<FLOOR>(h, ld, f, row_begin + rs, ct * kTile + (stid & 3) * 32,
+                                                 (ex >> src) & 1u, q, s_tile + swz_word(rs) + (stid & 3));
                 } while (todo);
             }
         }
@@ -681,6 +686,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     if (!tile_rows<GROUPED>(offsets, groups, rows, &row_begin, &row_end)) return;
     const int tid = threadIdx.x;
     const int j = tid & 3;
+    const int64_t n_row_tiles = GROUPED ? rows / kTile + groups : (rows + kTile - 1) / kTile;
+    if (!MX_IN_BOUNDS(static_cast<int64_t>(blockIdx.x) < n_row_tiles)) return;
     // token and weight of this thread's two rows, once for all column tiles
     int32_t tk[2];
     WeightFold wf[2];
@@ -688,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int64_t row = row_begin + (tid >> 2) + 64 * i;
-        const bool in = row < row_end;
+        const bool in = row < row_end && MX_IN_BOUNDS(row < rows);
         const int32_t t = in ? __ldg(row_token + row) : -1;
         const bool valid = t >= 0 && t < tokens;
         bad |= in && !valid;
@@ -702,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         uint32_t xw[2][16];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            if (tk[i] >= 0 && col < cols) {
+            if (tk[i] >= 0 && col < cols && MX_IN_BOUNDS(tk[i] < tokens && col + 32 <= cols)) {
                 // cached: each token row is gathered by several dispatched rows
                 const uint16_t* src = dy + static_cast<int64_t>(tk[i]) * ld + col;
                 ld32_cached(src, xw[i], v8);
@@ -717,7 +724,8 @@ __global__ void __launch_bounds__(kThreads, 4)
         for (int i = 0; i < 2; ++i) {
             const int r = (tid >> 2) + 64 * i;
             const int64_t row = row_begin + r;
-            uint8_t* const q_dst = row < row_end && col < cols ? q + row * cols + col : nullptr;
+            uint8_t* const q_dst =
+                row < row_end && col < cols && MX_IN_BOUNDS(row < rows && col + 32 <= cols) ? q + row * cols + col : nullptr;
             uint8_t* const s_dst = s_tile + swz_word(r) + j;
             if (tk[i] < 0 || col >= cols) {
                 // no token (or padding, or past the last column): zeros
@@ -790,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
     uint32_t xw[16];
     int64_t pi = tid;
-    if (pi < nt * nb) {
+    if (pi < nt * nb && MX_IN_BOUNDS(t0 + pi / nb < tokens && (pi % nb + 1) * 32 <= cols)) {
         const int tl = static_cast<int>(pi / nb);
         const uint16_t* src = dy + (t0 + tl) * ld + (pi - tl * nb) * 32;
         ld32_stream(src, xw, v8);
@@ -850,6 +858,9 @@ __global__ void __launch_bounds__(kThreads, 4)
                 prow = r;
             }
         }
+        // the padded scale row lies in the layout's row tiles
+        const int64_t n_row_tiles = GROUPED ? rows / kTile + groups : (rows + kTile - 1) / kTile;
+        if (row >= 0 && !MX_IN_BOUNDS(row < rows && prow / kTile < n_row_tiles)) row = -1;
         RouteEntry re;
         re.qrow = row >= 0 ? q + row * cols : nullptr;
         re.srow = row >= 0 ? s + (prow / kTile) * nkc * 512 + swz_word(static_cast<int>(prow % kTile)) : nullptr;
@@ -860,6 +871,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     for (; pi < nt * nb; pi += blockDim.x) {
         const int tl = static_cast<int>(pi / nb);
         const int64_t b = pi - tl * nb;
+        if (!MX_IN_BOUNDS(t0 + tl < tokens && (b + 1) * 32 <= cols)) continue;
         if (pi != tid) {
             const uint16_t* src = dy + (t0 + tl) * ld + b * 32;
             ld32_stream(src, xw, v8);

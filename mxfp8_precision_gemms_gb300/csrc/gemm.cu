@@ -656,7 +656,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tm_a, const CUtenso
     #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int64_t col = col0 + j * 8;
-                        if (col < p.N) {
+                        if (col < p.N && MX_IN_BOUNDS(row < p.M && col + 8 <= p.N)) {
                             uint4 o;
                             o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * alpha,
                                               __uint_as_float(v[8 * j + 1]) * alpha);

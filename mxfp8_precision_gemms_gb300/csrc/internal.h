@@ -30,6 +30,19 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Index checks of the bounds-checked build (compiled with
+// -DMXFP8_BOUNDS_CHECK into libmxfp8_bc.so): each guards one global access
+// with the extent of the tensor it touches, stated independently of the
+// kernel's own tile arithmetic; a failed check records
+// MXFP8_ERR_DEVICE_CHECK through the kernel file's own record_status and the
+// access is skipped.  In the product build every check is the constant true
+// and compiles away.
+#ifdef MXFP8_BOUNDS_CHECK
+#define MX_IN_BOUNDS(cond) ((cond) || (record_status(MXFP8_ERR_DEVICE_CHECK), false))
+#else
+#define MX_IN_BOUNDS(cond) true
+#endif
+
 // Launch parameters of the MX quantizer (plain or grouped rows).
 struct QuantMxArgs {
     const uint16_t* x;

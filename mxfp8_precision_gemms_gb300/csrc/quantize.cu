@@ -72,20 +72,22 @@ __global__ void __launch_bounds__(kThreads)
     for (int it = 0; it < 8; ++it) {
         const int r = it * 16 + (tid >> 4);
         const int64_t row = row_begin + r;
-        if (row < row_end && col < a.cols) {
+        if (row < row_end && col < a.cols && MX_IN_BOUNDS(row < a.rows && col + 8 <= a.cols)) {
             v[it] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + col));
         } else {
             v[it] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
 
-    if constexpr (ROW) {
+    // the scale layout's row tiles (grouped: every group padded to whole tiles)
+    const int64_t n_row_tiles = GROUPED ? a.rows / kTile + a.groups : (a.rows + kTile - 1) / kTile;
+    if (ROW && MX_IN_BOUNDS(rt < n_row_tiles && ct < nkc_row)) {
         uint8_t* s_tile = a.s_row + (rt * nkc_row + ct) * 512;
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
             const int r = it * 16 + (tid >> 4);
             const int64_t row = row_begin + r;
-            const bool in = row < row_end && col < a.cols;
+            const bool in = row < row_end && col < a.cols && MX_IN_BOUNDS(row < a.rows && col + 8 <= a.cols);
             mx_row_step<FLOOR>(v[it], r, in ? a.q_row + row * a.cols + col : nullptr, s_tile);
         }
     }
@@ -125,19 +127,19 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t k0 = ct * kTile + 2 * cp;  // output row (an input column)
         const int64_t r0 = rt * kTile + j * 32;  // output column (an input row)
         if (r0 < a.rows) {
-            if (k0 < a.cols) {
+            if (k0 < a.cols && MX_IN_BOUNDS(r0 + 32 <= a.rows)) {
                 uint4* dst = reinterpret_cast<uint4*>(a.q_col + k0 * a.rows + r0);
                 dst[0] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
                 dst[1] = make_uint4(qlo[4], qlo[5], qlo[6], qlo[7]);
             }
-            if (k0 + 1 < a.cols) {
+            if (k0 + 1 < a.cols && MX_IN_BOUNDS(r0 + 32 <= a.rows)) {
                 uint4* dst = reinterpret_cast<uint4*>(a.q_col + (k0 + 1) * a.rows + r0);
                 dst[0] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
                 dst[1] = make_uint4(qhi[4], qhi[5], qhi[6], qhi[7]);
             }
         }
         __syncthreads();
-        if (tid < kTile) {
+        if (tid < kTile && MX_IN_BOUNDS(ct < (a.cols + kTile - 1) / kTile && rt < nkc_col)) {
             uint8_t* s_tile = a.s_col + (ct * nkc_col + rt) * 512;
             *reinterpret_cast<uint32_t*>(s_tile + swz_word(tid)) =
                 reinterpret_cast<const uint32_t*>(col_scales)[tid];
@@ -155,8 +157,8 @@ __global__ void __launch_bounds__(kThreads)
 // payload bytes and its scale byte into the tile's 512-byte swizzled scale
 // block s_tile.
 template <bool FLOOR>
-__device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t ld, int64_t cols,
-                                         uint8_t* __restrict__ q, uint8_t* __restrict__ s_tile,
+__device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t ld, int64_t rows,
+                                         int64_t cols, uint8_t* __restrict__ q, uint8_t* __restrict__ s_tile,
                                          int64_t row_begin, int64_t row_end, int64_t ct, bool v8) {
     const int tid = threadIdx.x;
     const int j = tid & 3;
@@ -165,7 +167,7 @@ __device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int64_t row = row_begin + (tid >> 2) + 64 * i;
-        if (row < row_end && col < cols) {
+        if (row < row_end && col < cols && MX_IN_BOUNDS(row < rows && col + 32 <= cols)) {
             const uint16_t* src = x + row * ld + col;
             ld32_stream(src, w[i], v8);
             ld32_stream(src + 16, w[i] + 8, v8);
@@ -178,7 +180,7 @@ __device__ __forceinline__ void row_tile(const uint16_t* __restrict__ x, int64_t
     for (int i = 0; i < 2; ++i) {
         const int r = (tid >> 2) + 64 * i;
         const int64_t row = row_begin + r;
-        const bool in = row < row_end && col < cols;
+        const bool in = row < row_end && col < cols && MX_IN_BOUNDS(row < rows && col + 32 <= cols);
         mx_block32<FLOOR>(w[i], in ? q + row * cols + col : nullptr, s_tile + swz_word(r) + j, v8);
     }
 }
@@ -208,8 +210,10 @@ __global__ void __launch_bounds__(kThreads)
         row_begin = rt * kTile;
         row_end = min(a.rows, row_begin + kTile);
     }
-    row_tile<FLOOR>(a.x, a.ld, a.cols, a.q_row, a.s_row + (rt * nkc + ct) * 512, row_begin, row_end,
-                    ct, v8);
+    const int64_t n_row_tiles = GROUPED ? a.rows / kTile + a.groups : (a.rows + kTile - 1) / kTile;
+    if (!MX_IN_BOUNDS(rt < n_row_tiles && ct < nkc)) return;
+    row_tile<FLOOR>(a.x, a.ld, a.rows, a.cols, a.q_row, a.s_row + (rt * nkc + ct) * 512, row_begin,
+                    row_end, ct, v8);
 }
 
 // Rowwise MX quantization of several tensors in one launch: a 1D grid over
@@ -238,8 +242,9 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t ct = local / b.row_tiles[t];
     const int64_t row_begin = rt * kTile;
     const int64_t row_end = min(b.rows[t], row_begin + kTile);
-    row_tile<FLOOR>(b.x[t], b.ld[t], b.cols[t], b.q[t], b.s[t] + (rt * b.nkc[t] + ct) * 512, row_begin,
-                    row_end, ct, b.v8[t] != 0);
+    if (!MX_IN_BOUNDS(rt < (b.rows[t] + kTile - 1) / kTile && ct < (b.cols[t] + kTile - 1) / kTile)) return;
+    row_tile<FLOOR>(b.x[t], b.ld[t], b.rows[t], b.cols[t], b.q[t], b.s[t] + (rt * b.nkc[t] + ct) * 512,
+                    row_begin, row_end, ct, b.v8[t] != 0);
 }
 
 // Rowwise + colwise (or colwise only) MX quantization of a 128 x 128 tile
@@ -310,11 +315,12 @@ __device__ __forceinline__ bool tile_quantize(const CUtensorMap* map, const Tile
             }
             const int64_t col = ct * kTile + 32 * b;
             uint8_t byte;
-            mx_block32<FLOOR>(w, (row < a.rows && col < a.cols) ? a.q_row + row * a.cols + col : nullptr,
-                              &byte, a.v8);
+            const bool in = row < a.rows && col < a.cols && MX_IN_BOUNDS(col + 32 <= a.cols);
+            mx_block32<FLOOR>(w, in ? a.q_row + row * a.cols + col : nullptr, &byte, a.v8);
             bytes |= static_cast<uint32_t>(byte) << (8 * b);
         }
-        *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = bytes;
+        if (MX_IN_BOUNDS(rt < (a.rows + kTile - 1) / kTile && ct < a.nkc_row))
+            *reinterpret_cast<uint32_t*>(s_tile + swz_word(r)) = bytes;
     }
 
     // colwise
@@ -357,8 +363,9 @@ __device__ __forceinline__ bool tile_quantize(const CUtensorMap* map, const Tile
                 }
             }
             const int64_t k0 = ct * kTile + 4 * g + c;  // output row (an input column)
-            if (k0 < a.cols && r0 < a.rows) st32(a.q_col + k0 * a.rows + r0, q, a.v8);
-            s_tile[swz_word(4 * g + c) + j] = static_cast<uint8_t>(bc[c]);
+            if (k0 < a.cols && r0 < a.rows && MX_IN_BOUNDS(r0 + 32 <= a.rows)) st32(a.q_col + k0 * a.rows + r0, q, a.v8);
+            if (MX_IN_BOUNDS(ct < (a.cols + kTile - 1) / kTile && rt < a.nkc_col))
+                s_tile[swz_word(4 * g + c) + j] = static_cast<uint8_t>(bc[c]);
         }
     }
     return true;
@@ -446,12 +453,12 @@ __global__ void __launch_bounds__(256)
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     uint32_t m = 0;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n8; i += 4 * stride) {
+    for (; i + 3 * stride < n8 && MX_IN_BOUNDS((i + 3 * stride + 1) * 8 <= n); i += 4 * stride) {
         const uint4 a0 = x8[i], a1 = x8[i + stride], a2 = x8[i + 2 * stride],
                     a3 = x8[i + 3 * stride];
         m = max(m, max(max(amax8(a0), amax8(a1)), max(amax8(a2), amax8(a3))));
     }
-    for (; i < n8; i += stride) m = max(m, amax8(x8[i]));
+    for (; i < n8 && MX_IN_BOUNDS((i + 1) * 8 <= n); i += stride) m = max(m, amax8(x8[i]));
     for (int64_t t = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
          t += stride)
         m = max(m, static_cast<uint32_t>(x[t] & 0x7FFFu));
@@ -480,6 +487,7 @@ __global__ void __launch_bounds__(256)
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += stride) {
+        if (!MX_IN_BOUNDS((i + 1) * 8 <= n)) break;
         const uint4 v = x8[i];
         uint2 o;
         o.x = quant4_scaled<FMT>(v.x, v.y, s);
@@ -571,7 +579,7 @@ __device__ __forceinline__ void cast_share(const uint16_t* __restrict__ x, uint8
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int64_t c = i + k * stride;
-            if (c < n16) {
+            if (c < n16 && MX_IN_BOUNDS((c + 1) * 16 <= n)) {
                 uint4 o;
                 uint32_t* po = &o.x;
 #pragma unroll
@@ -700,6 +708,7 @@ __global__ void __launch_bounds__(256)
     uint32_t m = 0, cnt = 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += stride) {
+        if (!MX_IN_BOUNDS((i + 1) * 8 <= n)) break;
         const uint4 v = x8[i];
         m = max(m, amax8(v));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -810,6 +819,7 @@ __global__ void __launch_bounds__(256)
     };
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
          i += stride) {
+        if (!MX_IN_BOUNDS((i + 1) * 16 <= n)) break;
         const uint4 v = __ldcs(in16 + i);
         uint4 o;
         o.x = map4(v.x);
